@@ -1,0 +1,176 @@
+/*
+ * iha.h -- C ABI of the GB300 (sm_103a) Interleaved Head Attention forward pass.
+ *
+ * The operation is Algorithm 1 of "Interleaved Head Attention" (Duvvuri et al.,
+ * arXiv 2602.21371; summary page "交錯頭注意力機制", section 4):
+ *   1. per-head projections      X W_s^(m),              s in {Q, K, V}, m = 1..H
+ *   2. pseudo-head mixing        S~_{h,j} = sum_m alpha_s[m,h,j] X W_s^(m),  j = 1..P
+ *   3. stacking to length P*N and per-head softmax attention
+ *                                Pbar_h = softmax(Qbar_h Kbar_h^T / sqrt(d)) Vbar_h
+ *   4. unstacking and contraction O_h[t] = sum_{h',j} R[h, h'P + j] P_{h',j}[t],
+ *      heads concatenated to X~ [N, D].
+ * The scores are masked by original token position ("注意力机制" eq. (5.12):
+ * visibility by absolute position): pseudo-token (j, t) may read (j', t') iff
+ *   IHA_MASK_NONE:   always;
+ *   IHA_MASK_CAUSAL: t' <= t;
+ *   IHA_MASK_WINDOW: t' <= t and t - t' < window  (window >= N behaves as causal).
+ * Pseudo-tokens of one position see one another; every row has at least P
+ * readable keys, so no row is ever empty.
+ *
+ * Conventions shared by every entry point
+ *   - All arrays are dense, row-major, owned by the caller; the library never
+ *     frees them and never keeps a pointer after a call returns.
+ *   - D = H * d by contract (the signatures carry no D).
+ *   - X [B][N][D]; W_Q, W_K, W_V [D][H*d], column block m (columns m*d..m*d+d-1)
+ *     is W^(m) (the packed layout of "注意力机制" eq. (5.22)); note that torch's
+ *     nn.Linear stores the transpose.
+ *   - alpha_Q/K/V [H(m)][H(h)][P(j)] float32; R [H][H*P] float32, column h'*P + j.
+ *   - out (X~) [B][N][D], D = H*d, head h at columns h*d..h*d+d-1.
+ *   - dtype IHA_DTYPE_BF16: X, W, intermediates and out are bfloat16; products
+ *     accumulate in float32 (tcgen05 tensor cores).  IHA_DTYPE_F32: everything
+ *     float32 with exact fp32 FMA arithmetic (no TF32).  alpha and R are float32
+ *     in both.
+ *   - Device entry points take DEVICE pointers and run asynchronously on the
+ *     given stream (NULL = the legacy default stream).  out must not alias an
+ *     input.
+ *   - Return value: IHA_OK or an IHA_ERR_* code; nothing is thrown across the ABI.
+ *     Argument errors are detected on the host before anything is launched.
+ *     A device-side bounded wait that expires (IHA_ERR_TIMEOUT) is recorded in a
+ *     per-device status word and reported by iha_check_device_status().
+ */
+#ifndef IHA_H
+#define IHA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* exported from libiha.so (everything else in the library is hidden) */
+#if defined(__GNUC__)
+#define IHA_API __attribute__((visibility("default")))
+#else
+#define IHA_API
+#endif
+
+#define IHA_OK 0
+#define IHA_ERR_INVALID_ARG 1   /* null pointer, non-positive size, bad mode/dtype/window */
+#define IHA_ERR_UNSUPPORTED 2   /* valid but not supported here (e.g. bf16 with d not 64/128) */
+#define IHA_ERR_WORKSPACE 3     /* caller workspace smaller than iha_workspace_bytes() */
+#define IHA_ERR_CUDA 4          /* a CUDA call or launch failed */
+#define IHA_ERR_TIMEOUT 5       /* a device-side bounded wait expired */
+
+#define IHA_DTYPE_F32 0
+#define IHA_DTYPE_BF16 1
+
+#define IHA_MASK_NONE 0
+#define IHA_MASK_CAUSAL 1
+#define IHA_MASK_WINDOW 2
+
+/*
+ * iha_forward -- the whole forward pass (steps 1-4) in bfloat16 on the legacy
+ * default stream, with a workspace the library allocates stream-ordered
+ * (cudaMallocAsync) and frees after the last launch.  Asynchronous.
+ * Errors: IHA_ERR_INVALID_ARG, IHA_ERR_UNSUPPORTED (d not in {64, 128}),
+ * IHA_ERR_CUDA (allocation or launch failure).
+ */
+IHA_API int iha_forward(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                const float *alpha_Q, const float *alpha_K, const float *alpha_V,
+                const float *R, int B, int N, int H, int d, int P,
+                int mask_mode, int window, void *out);
+
+/*
+ * iha_forward_ex -- iha_forward with the arithmetic type, the stream and the
+ * workspace chosen by the caller.  workspace may be NULL (allocated and freed
+ * stream-ordered by the library); otherwise it must be a device buffer of at
+ * least iha_workspace_bytes(B, N, H, d, P, dtype) bytes, 256-byte aligned, not
+ * used concurrently by another call.
+ * Errors: as iha_forward, plus IHA_ERR_WORKSPACE.
+ */
+IHA_API int iha_forward_ex(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                   const float *alpha_Q, const float *alpha_K, const float *alpha_V,
+                   const float *R, int B, int N, int H, int d, int P,
+                   int mask_mode, int window, void *out,
+                   int dtype, void *stream, void *workspace, size_t workspace_bytes);
+
+/* Bytes of device workspace one call needs (0 if the sizes are invalid):
+ * folded weights + stacked Qbar, Kbar, Vbar + Pbar, each 256-byte aligned. */
+IHA_API size_t iha_workspace_bytes(int B, int N, int H, int d, int P, int dtype);
+
+/* A static, human-readable name for a status code (never NULL). */
+IHA_API const char *iha_error_string(int status);
+
+/*
+ * iha_check_device_status -- synchronise the stream, then read and clear the
+ * current device's status word.  Returns IHA_OK, IHA_ERR_TIMEOUT (a kernel
+ * gave up a bounded wait since the last check; its output is invalid) or
+ * IHA_ERR_CUDA (the stream reported an error).  If code_out is not NULL it
+ * receives the raw word (0, or the wait site that expired).
+ */
+IHA_API int iha_check_device_status(void *stream, int *code_out);
+
+/*
+ * iha_forward_host -- the forward pass on HOST buffers: copies X, W_*, alpha_*,
+ * R host->device, runs iha_forward_ex, copies out device->host and synchronises
+ * the stream before returning.  Host buffers should be pinned for full copy
+ * bandwidth.  device_buffer may be NULL (allocated and freed by the call) or a
+ * device buffer of at least iha_host_buffer_bytes(...) bytes.
+ * Errors: as iha_forward_ex; IHA_ERR_TIMEOUT if a device wait expired.
+ */
+IHA_API int iha_forward_host(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                     const float *alpha_Q, const float *alpha_K, const float *alpha_V,
+                     const float *R, int B, int N, int H, int d, int P,
+                     int mask_mode, int window, void *out, int dtype, void *stream,
+                     void *device_buffer, size_t device_buffer_bytes);
+
+/* Device bytes iha_forward_host needs: inputs + out + workspace (0 if invalid). */
+IHA_API size_t iha_host_buffer_bytes(int B, int N, int H, int d, int P, int dtype);
+
+/*
+ * iha_selftest_wait_timeout -- launch one tiny kernel whose only wait (on an
+ * mbarrier nothing arrives at) must give up after limit_ms milliseconds
+ * (1..10000), record its site in the status word and return normally.  It
+ * exercises the device-side timeout path used by every pipeline wait; the next
+ * iha_check_device_status() must report IHA_ERR_TIMEOUT.  No counterpart in the
+ * method: it is a failure-detection check of this library.
+ */
+IHA_API int iha_selftest_wait_timeout(void *stream, int limit_ms);
+
+/* ---------------------------------------------------------------------------
+ * The four steps as separate entry points (same validation, same kernels as
+ * iha_forward_ex; asynchronous on the stream).  Intermediate layouts:
+ *   Wt   [3*H*P*d][D]   folded, transposed weights: row s*H*P*d + h*P*d + j*d + c
+ *                       holds  sum_m alpha_s[m,h,j] W_s[:, m*d + c]   (s = Q, K, V)
+ *   Qbar, Kbar, Vbar [B][H][N*P][d]   stacked pseudo-tokens of head h; row t*P + j
+ *                       is pseudo-token (j, t) (t-major interleaving; with a mask
+ *                       on t only this ordering gives the same output as the row
+ *                       concatenation j*N + t, "注意力机制" eq. (5.41))
+ *   Pbar [B][N][H][P][d] attention output of pseudo-token (j, t) of head h
+ * ------------------------------------------------------------------------- */
+
+/* Step 1+2 weights: fold alpha into the projection weights (linearity of the
+ * mixing sum over m).  Wt as above, dtype-sized elements. */
+IHA_API int iha_fold_weights(const void *W_Q, const void *W_K, const void *W_V,
+                     const float *alpha_Q, const float *alpha_K, const float *alpha_V,
+                     int H, int d, int P, int dtype, void *Wt, void *stream);
+
+/* Steps 1+2 and the stacking: [Qbar|Kbar|Vbar] = X Wt^T written in the stacked
+ * layout.  QKV points to 3 consecutive arrays of B*H*N*P*d elements. */
+IHA_API int iha_project(const void *X, const void *Wt, int B, int N, int H, int d, int P,
+                int dtype, void *QKV, void *stream);
+
+/* Step 3: masked softmax attention over each head's stacked sequence.
+ * QKV as written by iha_project; Pbar [B][N][H][P][d]. */
+IHA_API int iha_attention(const void *QKV, int B, int N, int H, int d, int P,
+                  int mask_mode, int window, int dtype, void *Pbar, void *stream);
+
+/* Step 4: unstack and contract with R, heads concatenated into out [B][N][H*d]. */
+IHA_API int iha_contract(const void *Pbar, const float *R, int B, int N, int H, int d, int P,
+                 int dtype, void *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IHA_H */

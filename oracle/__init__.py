@@ -65,6 +65,8 @@ class Oracle:
         i64p = ctypes.POINTER(ctypes.c_longlong)
         lib.iha_oracle_forward.argtypes = [dp] * 8 + [ctypes.c_int] * 8 + [i64p, ctypes.c_int, dp, dp, ctypes.c_int]
         lib.iha_oracle_forward.restype = ctypes.c_int
+        lib.iha_oracle_forward_from_projections.argtypes = [dp] * 7 + [ctypes.c_int] * 8 + [i64p, ctypes.c_int, dp, dp, ctypes.c_int]
+        lib.iha_oracle_forward_from_projections.restype = ctypes.c_int
         lib.iha_oracle_mha.argtypes = [dp] * 4 + [ctypes.c_int] * 6 + [i64p, ctypes.c_int, dp, ctypes.c_int]
         lib.iha_oracle_mha.restype = ctypes.c_int
         lib.iha_oracle_softmax_read.argtypes = [dp, ctypes.POINTER(ctypes.c_ubyte), ctypes.c_int, dp,
@@ -76,7 +78,7 @@ class Oracle:
 
     def forward(self, X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, *, H, d, P,
                 mask_mode=0, window=0, stack_order=0, rows=None, with_weights=False,
-                nthreads=None):
+                nthreads=None, projection="c"):
         """IHA forward (Algorithm 1) in float64.
 
         X [B, N, H*d]; W_s [H*d, H*d]; alpha_s [H, H, P]; R [H, H*P].
@@ -84,6 +86,9 @@ class Oracle:
         default every row.  Returns out [B, N, H*d] or [len(rows), H*d]; with
         with_weights=True also the attention weights [B, H, P*N, P*N] in
         stacked order (stack_order 0: row j*N + t; 1: row t*P + j).
+        projection: "c" computes the per-head projections X W^(m) with the C
+        loop; "numpy" takes them from a float64 library matmul (X @ W_s) and
+        runs every later step in C -- the same arithmetic, faster on large X.
         """
         X = _f64(X)
         B, N, D = X.shape
@@ -105,10 +110,17 @@ class Oracle:
         else:
             out = np.zeros((B, N, D), dtype=np.float64)
         wts = np.zeros((B, H, P * N, P * N), dtype=np.float64) if with_weights else None
-        rc = self.lib.iha_oracle_forward(
-            _dp(X), *[_dp(a) for a in args], B, N, H, d, P, mask_mode, window, stack_order,
-            _i64p(sel), len(sel) if sel is not None else 0, _dp(out), _dp(wts),
-            nthreads or default_threads())
+        common = (B, N, H, d, P, mask_mode, window, stack_order,
+                  _i64p(sel), len(sel) if sel is not None else 0, _dp(out), _dp(wts),
+                  nthreads or default_threads())
+        if projection == "c":
+            rc = self.lib.iha_oracle_forward(_dp(X), *[_dp(a) for a in args], *common)
+        elif projection == "numpy":
+            XW = [np.ascontiguousarray(np.matmul(X, w)) for w in args[:3]]
+            rc = self.lib.iha_oracle_forward_from_projections(*[_dp(a) for a in XW],
+                                                              *[_dp(a) for a in args[3:]], *common)
+        else:
+            raise ValueError("projection must be 'c' or 'numpy'")
         if rc != 0:
             raise RuntimeError(f"iha_oracle_forward failed: {ERRORS.get(rc, rc)}")
         return (out, wts) if with_weights else out

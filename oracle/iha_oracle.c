@@ -131,6 +131,7 @@ static void parallel_for(i64 n, int nthreads, item_fn fn, void *ctx)
 typedef struct {
     /* problem */
     const double *X, *W[3], *alpha[3], *R;
+    const double *XW[3];   /* optional precomputed X W_s, [B][N][H*d]; NULL = compute here */
     int B, N, H, d, P, mask_mode, window, stack_order;
     /* current batch element and token sets */
     int b;
@@ -162,16 +163,21 @@ static void item_project(void *vc, i64 slot)
     fwd_ctx *c = (fwd_ctx *)vc;
     const int D = c->H * c->d, Hd = c->H * c->d, H = c->H, d = c->d;
     const int t = c->tok_of[slot];
-    const double *x = c->X + ((i64)c->b * c->N + t) * D;
+    const double *x = c->X ? c->X + ((i64)c->b * c->N + t) * D : NULL;
     double *acc = (double *)malloc(sizeof(double) * Hd);
     if (!acc) { set_err(c, OR_ENOMEM); return; }
     for (int s = 0; s < 3; s++) {
-        /* acc[col] = sum_k x[k] * W[k][col], col = m*d + cc (column block m = W^(m)) */
-        for (int col = 0; col < Hd; col++) acc[col] = 0.0;
-        for (int k = 0; k < D; k++) {
-            const double xk = x[k];
-            const double *wrow = c->W[s] + (i64)k * Hd;
-            for (int col = 0; col < Hd; col++) acc[col] += xk * wrow[col];
+        if (c->XW[s]) {
+            /* projections supplied by the caller (a library matmul) */
+            memcpy(acc, c->XW[s] + ((i64)c->b * c->N + t) * Hd, sizeof(double) * Hd);
+        } else {
+            /* acc[col] = sum_k x[k] * W[k][col], col = m*d + cc (column block m = W^(m)) */
+            for (int col = 0; col < Hd; col++) acc[col] = 0.0;
+            for (int k = 0; k < D; k++) {
+                const double xk = x[k];
+                const double *wrow = c->W[s] + (i64)k * Hd;
+                for (int col = 0; col < Hd; col++) acc[col] += xk * wrow[col];
+            }
         }
         for (int m = 0; m < H; m++)
             for (int cc = 0; cc < d; cc++)
@@ -304,14 +310,14 @@ static void item_contract(void *vc, i64 qi)
  *          (only with sel == NULL).
  * Returns 0 or a negative error code.
  */
-int iha_oracle_forward(const double *X, const double *W_Q, const double *W_K, const double *W_V,
-                       const double *alpha_Q, const double *alpha_K, const double *alpha_V,
-                       const double *R, int B, int N, int H, int d, int P,
-                       int mask_mode, int window, int stack_order,
-                       const i64 *sel, int n_sel, double *out, double *weights, int nthreads)
+static int forward_impl(const double *X, const double *W_Q, const double *W_K, const double *W_V,
+                        const double *XW_Q, const double *XW_K, const double *XW_V,
+                        const double *alpha_Q, const double *alpha_K, const double *alpha_V,
+                        const double *R, int B, int N, int H, int d, int P,
+                        int mask_mode, int window, int stack_order,
+                        const i64 *sel, int n_sel, double *out, double *weights, int nthreads)
 {
-    if (!X || !W_Q || !W_K || !W_V || !alpha_Q || !alpha_K || !alpha_V || !R || !out)
-        return OR_EINVAL;
+    if (!alpha_Q || !alpha_K || !alpha_V || !R || !out) return OR_EINVAL;
     if (B <= 0 || N <= 0 || H <= 0 || d <= 0 || P <= 0) return OR_EINVAL;
     if (mask_mode < 0 || mask_mode > 2) return OR_EINVAL;
     if (mask_mode == 2 && window < 1) return OR_EINVAL;
@@ -322,6 +328,7 @@ int iha_oracle_forward(const double *X, const double *W_Q, const double *W_K, co
     fwd_ctx c;
     memset(&c, 0, sizeof c);
     c.X = X; c.W[0] = W_Q; c.W[1] = W_K; c.W[2] = W_V;
+    c.XW[0] = XW_Q; c.XW[1] = XW_K; c.XW[2] = XW_V;
     c.alpha[0] = alpha_Q; c.alpha[1] = alpha_K; c.alpha[2] = alpha_V; c.R = R;
     c.B = B; c.N = N; c.H = H; c.d = d; c.P = P;
     c.mask_mode = mask_mode; c.window = window; c.stack_order = stack_order;
@@ -392,6 +399,30 @@ int iha_oracle_forward(const double *X, const double *W_Q, const double *W_K, co
     free(tq); free(c.tok_of);
     pthread_mutex_destroy(&c.lock);
     return rc;
+}
+
+int iha_oracle_forward(const double *X, const double *W_Q, const double *W_K, const double *W_V,
+                       const double *alpha_Q, const double *alpha_K, const double *alpha_V,
+                       const double *R, int B, int N, int H, int d, int P,
+                       int mask_mode, int window, int stack_order,
+                       const i64 *sel, int n_sel, double *out, double *weights, int nthreads)
+{
+    if (!X || !W_Q || !W_K || !W_V) return OR_EINVAL;
+    return forward_impl(X, W_Q, W_K, W_V, NULL, NULL, NULL, alpha_Q, alpha_K, alpha_V, R,
+                        B, N, H, d, P, mask_mode, window, stack_order, sel, n_sel, out, weights, nthreads);
+}
+
+/* The same forward pass starting from the per-head projections: XW_s [B][N][H*d]
+ * holds X W_s, whose column block m is X W_s^(m) (the first half of the mixing step). */
+int iha_oracle_forward_from_projections(const double *XW_Q, const double *XW_K, const double *XW_V,
+                                        const double *alpha_Q, const double *alpha_K, const double *alpha_V,
+                                        const double *R, int B, int N, int H, int d, int P,
+                                        int mask_mode, int window, int stack_order,
+                                        const i64 *sel, int n_sel, double *out, double *weights, int nthreads)
+{
+    if (!XW_Q || !XW_K || !XW_V) return OR_EINVAL;
+    return forward_impl(NULL, NULL, NULL, NULL, XW_Q, XW_K, XW_V, alpha_Q, alpha_K, alpha_V, R,
+                        B, N, H, d, P, mask_mode, window, stack_order, sel, n_sel, out, weights, nthreads);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -1,0 +1,110 @@
+"""The C-ABI library loads, exports every symbol include/iha.h declares, and its
+host-side logic (validation, sizes, error strings) behaves as documented.
+No call here reaches the GPU: every compute call below is rejected during
+argument validation, before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def iha():
+    from transformer_attention_variant_gb300 import build as b
+    b.build()
+    import transformer_attention_variant_gb300 as m
+    return m
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "iha.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(iha_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(iha):
+    syms = declared_symbols()
+    assert len(syms) >= 12
+    lib = ctypes.CDLL(iha.LIB_PATH)
+    for s in syms:
+        assert hasattr(lib, s), f"libiha.so does not export {s}"
+    assert sorted(iha.EXPORTED) == syms
+
+
+def test_binding_has_the_abi_names(iha):
+    for s in declared_symbols():
+        assert callable(getattr(iha, s)), s
+
+
+def test_error_strings(iha):
+    assert iha.iha_error_string(iha.IHA_OK) == "ok"
+    assert "invalid" in iha.iha_error_string(iha.IHA_ERR_INVALID_ARG)
+    assert "timed out" in iha.iha_error_string(iha.IHA_ERR_TIMEOUT)
+    assert iha.iha_error_string(12345) == "unknown status"
+
+
+def test_workspace_bytes(iha):
+    B, N, H, d, P = 2, 1024, 16, 64, 2
+    D = H * d
+    al = lambda x: (x + 255) // 256 * 256
+    for dtype, es in ((iha.IHA_DTYPE_BF16, 2), (iha.IHA_DTYPE_F32, 4)):
+        expect = al(3 * H * P * d * D * es) + al(3 * B * H * N * P * d * es) + al(B * N * H * P * d * es)
+        assert iha.iha_workspace_bytes(B, N, H, d, P, dtype) == expect
+    assert iha.iha_workspace_bytes(0, N, H, d, P, 1) == 0
+    assert iha.iha_workspace_bytes(B, N, H, 96, P, 1) == 0       # bf16 needs d in {64, 128}
+    assert iha.iha_workspace_bytes(B, N, H, 96, P, 0) > 0        # fp32 takes any d <= 256
+    assert iha.iha_workspace_bytes(B, N, H, d, P, 7) == 0
+    assert iha.iha_host_buffer_bytes(B, N, H, d, P, 1) > iha.iha_workspace_bytes(B, N, H, d, P, 1)
+
+
+FAKE = 1 << 20   # a non-null address that is never dereferenced (validation fails first)
+
+
+def fwd(iha, **kw):
+    a = dict(X=FAKE, W_Q=FAKE, W_K=FAKE, W_V=FAKE, alpha_Q=FAKE, alpha_K=FAKE, alpha_V=FAKE, R=FAKE,
+             B=1, N=8, H=2, d=64, P=2, mask_mode=1, window=0, out=FAKE, dtype=1, stream=None,
+             workspace=None, workspace_bytes=0)
+    a.update(kw)
+    return iha.iha_forward_ex(**a)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(X=None), 1), (dict(out=None), 1), (dict(R=None), 1), (dict(alpha_V=None), 1),
+    (dict(B=0), 1), (dict(N=-1), 1), (dict(H=0), 1), (dict(P=0), 1), (dict(d=0), 1),
+    (dict(mask_mode=3), 1), (dict(mask_mode=-1), 1), (dict(mask_mode=2, window=0), 1),
+    (dict(dtype=2), 1), (dict(d=96), 2), (dict(d=32), 2), (dict(dtype=0, d=300), 2),
+    (dict(N=1 << 24, P=2), 2),
+    (dict(workspace=FAKE, workspace_bytes=16), 3),
+    (dict(workspace=FAKE + 8, workspace_bytes=1 << 40), 3),
+])
+def test_forward_rejects_bad_arguments(iha, kw, status):
+    assert fwd(iha, **kw) == status
+
+
+def test_step_entry_points_reject_bad_arguments(iha):
+    assert iha.iha_fold_weights(None, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 64, 2, 1, FAKE) == 1
+    assert iha.iha_project(FAKE, FAKE, 1, 8, 2, 64, 0, 1, FAKE) == 1
+    assert iha.iha_attention(FAKE, 1, 8, 2, 64, 2, 2, 0, 1, FAKE) == 1
+    assert iha.iha_attention(FAKE, 1, 8, 2, 48, 2, 1, 0, 1, FAKE) == 2
+    assert iha.iha_contract(FAKE, None, 1, 8, 2, 64, 2, 1, FAKE) == 1
+    assert iha.iha_forward(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 64, 2, 1, 0, FAKE) == 1
+    assert iha.iha_forward_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 64, 2, 5, 0, FAKE, 1) == 1
+    assert iha.iha_selftest_wait_timeout(None, 0) == 1
+    assert iha.iha_selftest_wait_timeout(None, 20000) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    """Importing the binding when libiha.so is absent raises, naming the fix;
+    there is no fallback path."""
+    import subprocess
+    import sys
+    import shutil
+    pkg = tmp_path / "transformer_attention_variant_gb300"
+    pkg.mkdir()
+    shutil.copy(os.path.join(ROOT, "transformer_attention_variant_gb300", "__init__.py"), pkg / "__init__.py")
+    r = subprocess.run([sys.executable, "-c", "import transformer_attention_variant_gb300"], cwd=tmp_path,
+                       capture_output=True, text=True)
+    assert r.returncode != 0 and "libiha.so is missing" in r.stderr

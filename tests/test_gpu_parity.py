@@ -1,0 +1,280 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Tolerances (written here, derived in the design notes):
+  float32 path:  max|err| <= 1e-4 * max|O|
+  bfloat16 path: RMS(err) <= 2e-2 * RMS(O) over the compared rows, and every
+                 compared row within 0.1 of its own RMS (a structural error --
+                 a wrong index, mask or scale -- gives O(1) per-row errors,
+                 while bf16 rounding of Qbar/Kbar/Vbar, P and the output gives
+                 about 1e-2 at most).
+Small problems compare every output element; the five full-size workloads
+compare sampled rows (first/last tokens, tile and window edges) of the very
+launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import iha_inputs as gi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+BF16_RMS_TOL = 2e-2
+BF16_ROW_TOL = 0.1
+F32_MAX_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def iha():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import transformer_attention_variant_gb300 as m
+    return m
+
+
+def to_dev(inp):
+    return {k: v.to("cuda:0").contiguous() for k, v in inp.items()}
+
+
+def run_gpu(iha, w, inp=None, dinp=None):
+    if dinp is None:
+        dinp = to_dev(inp)
+    out = iha.forward(dinp, H=w.H, d=w.d, P=w.P, mask_mode=w.mask_mode, window=w.window)
+    torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status()
+    assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
+    return out
+
+
+def oracle_rows(w, inp, rows=None, projection="c"):
+    f = gi.as_f64(inp)
+    return oracle.forward(f["X"], f["W_Q"], f["W_K"], f["W_V"], f["alpha_Q"], f["alpha_K"], f["alpha_V"],
+                          f["R"], H=w.H, d=w.d, P=w.P, mask_mode=w.mask_mode, window=w.window, rows=rows,
+                          projection=projection)
+
+
+def rms(a):
+    return float(np.sqrt(np.mean(np.square(a))))
+
+
+def assert_parity(w, got, ref):
+    got = np.asarray(got, dtype=np.float64).reshape(-1, w.D)
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1, w.D)
+    assert np.isfinite(got).all()
+    err = got - ref
+    if w.dtype == "f32":
+        e = float(np.max(np.abs(err)) / np.max(np.abs(ref)))
+        assert e <= F32_MAX_TOL, f"{w.name}: max|err|/max|O| = {e:.3e}"
+        return e
+    e = rms(err) / rms(ref)
+    row = np.sqrt(np.mean(err ** 2, axis=1)) / np.maximum(np.sqrt(np.mean(ref ** 2, axis=1)), 1e-30)
+    assert e <= BF16_RMS_TOL, f"{w.name}: RMS(err)/RMS(O) = {e:.3e}"
+    assert row.max() <= BF16_ROW_TOL, f"{w.name}: worst row error {row.max():.3e} at row {int(row.argmax())}"
+    return e
+
+
+# ---------------------------------------------------------------------------
+# every element, against the oracle
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny_f32_nomask", "bf16_causal_n1024"])
+def test_small_workloads_every_element(iha, name):
+    w = gi.WORKLOADS[name]
+    inp = gi.make_inputs(w)
+    got = run_gpu(iha, w, inp).double().cpu().numpy()
+    assert_parity(w, got, oracle_rows(w, inp))
+
+
+W = gi.Workload
+C, NM, WN = gi.MASK_CAUSAL, gi.MASK_NONE, gi.MASK_WINDOW
+EDGE = [
+    W("n1_p1", B=1, N=1, H=2, d=64, P=1, mask_mode=C, window=0, dtype="bf16", seed=21),
+    W("n1_p4_nomask", B=2, N=1, H=2, d=128, P=4, mask_mode=NM, window=0, dtype="bf16", seed=22),
+    W("n3_nomask", B=1, N=3, H=2, d=64, P=2, mask_mode=NM, window=0, dtype="bf16", seed=23),
+    W("one_tile", B=1, N=64, H=2, d=64, P=2, mask_mode=C, window=0, dtype="bf16", seed=24),
+    W("ragged_window_D192", B=2, N=100, H=3, d=64, P=2, mask_mode=WN, window=7, dtype="bf16", seed=25),
+    W("ragged_p3", B=1, N=333, H=2, d=128, P=3, mask_mode=C, window=0, dtype="bf16", seed=26),
+    W("l129_nomask", B=1, N=129, H=2, d=64, P=1, mask_mode=NM, window=0, dtype="bf16", seed=27),
+    W("window1_p4", B=1, N=300, H=2, d=128, P=4, mask_mode=WN, window=1, dtype="bf16", seed=28),
+    W("window_ge_n", B=1, N=257, H=2, d=64, P=2, mask_mode=WN, window=1000, dtype="bf16", seed=29),
+    W("h1_narrow_gemm", B=3, N=130, H=1, d=64, P=1, mask_mode=C, window=0, dtype="bf16", seed=30),
+    W("multi_tile_window", B=1, N=1000, H=2, d=128, P=2, mask_mode=WN, window=300, dtype="bf16", seed=31),
+    W("p4_causal_d64", B=2, N=200, H=4, d=64, P=4, mask_mode=C, window=0, dtype="bf16", seed=32),
+    W("f32_odd_d", B=2, N=37, H=3, d=17, P=3, mask_mode=C, window=0, dtype="f32", seed=33),
+    W("f32_window", B=1, N=50, H=2, d=40, P=2, mask_mode=WN, window=4, dtype="f32", seed=34),
+    W("f32_n1", B=1, N=1, H=1, d=8, P=1, mask_mode=NM, window=0, dtype="f32", seed=35),
+]
+
+
+@pytest.mark.parametrize("w", EDGE, ids=[w.name for w in EDGE])
+def test_edge_shapes_every_element(iha, w):
+    inp = gi.make_inputs(w)
+    got = run_gpu(iha, w, inp).double().cpu().numpy()
+    assert_parity(w, got, oracle_rows(w, inp))
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: sampled rows
+# ---------------------------------------------------------------------------
+
+def sample_rows(w):
+    toks = {0, 1, 2, 63, 64, 127, 128, 129, 255, 256, w.N // 2, w.N // 2 + 1, w.N - 2, w.N - 1}
+    if w.mask_mode == WN:
+        toks |= {w.window - 1, w.window, w.window + 1, 2 * w.window}
+    toks = sorted(t for t in toks if 0 <= t < w.N)
+    bs = sorted({0, w.B - 1})
+    return [b * w.N + t for b in bs for t in toks]
+
+
+FULL = ["bf16_window1024_n4096", "bf16_causal_p4_n8192", "bf16_window4096_n16384"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(iha, name):
+    w = gi.WORKLOADS[name]
+    inp = gi.make_inputs(w)
+    got = run_gpu(iha, w, inp).double().cpu().numpy().reshape(w.B * w.N, w.D)
+    rows = sample_rows(w)
+    ref = oracle_rows(w, inp, rows=rows, projection="numpy")
+    assert_parity(w, got[rows], ref)
+    # properties that hold at every row
+    assert np.isfinite(got).all()
+
+
+def test_full_size_mha_special_case(iha):
+    """Long-context shape with P = 1, alpha = identity, R = identity: IHA must be
+    plain MHA (Definition 1).  Early rows against the independent MHA loop, all
+    sampled rows against the IHA oracle (equal to MHA by the inclusion pin)."""
+    w = gi.WORKLOADS["bf16_window4096_n16384"].with_(P=1, window=4096, name="mha_case")
+    inp = gi.make_inputs(w)
+    inp["alpha_Q"] = inp["alpha_K"] = inp["alpha_V"] = gi.identity_mixing(w.H, 1)
+    inp["R"] = gi.first_block_contraction(w.H, 1)
+    got = run_gpu(iha, w, inp).double().cpu().numpy().reshape(w.N, w.D)
+    early = [0, 1, 100, 255]
+    f = gi.as_f64(inp)
+    ref_mha = oracle.mha(f["X"], f["W_Q"], f["W_K"], f["W_V"], H=w.H, d=w.d, mask_mode=w.mask_mode,
+                         window=w.window, rows=early)
+    assert_parity(w, got[early], ref_mha)
+    rows = sample_rows(w)
+    assert_parity(w, got[rows], oracle_rows(w, inp, rows=rows, projection="numpy"))
+
+
+# ---------------------------------------------------------------------------
+# invariants on the GPU
+# ---------------------------------------------------------------------------
+
+def test_prefix_isolation_and_determinism(iha):
+    """Causal: changing tokens after t0 leaves outputs at t <= t0 bit-identical;
+    the same inputs give bit-identical outputs twice."""
+    w = W("prefix", B=1, N=700, H=4, d=128, P=2, mask_mode=C, window=0, dtype="bf16", seed=40)
+    inp = gi.make_inputs(w)
+    a = run_gpu(iha, w, inp)
+    a2 = run_gpu(iha, w, inp)
+    assert torch.equal(a, a2)
+    t0 = 300
+    inp2 = dict(inp)
+    X2 = inp["X"].clone()
+    X2[:, t0 + 1:] = -X2[:, t0 + 1:] * 2
+    inp2["X"] = X2
+    b = run_gpu(iha, w, inp2)
+    assert torch.equal(a[:, :t0 + 1], b[:, :t0 + 1])
+    assert not torch.equal(a[:, t0 + 1:], b[:, t0 + 1:])
+
+
+def test_window_at_least_n_equals_causal(iha):
+    w = W("wgen", B=2, N=300, H=2, d=64, P=2, mask_mode=C, window=0, dtype="bf16", seed=41)
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    a = run_gpu(iha, w, dinp=dinp)
+    b = run_gpu(iha, w.with_(mask_mode=WN, window=w.N), dinp=dinp)
+    assert torch.equal(a, b)
+
+
+def test_repeated_tokens_gpu(iha):
+    """All tokens equal: every output row equals the oracle's row (the
+    repeated-token closed form is pinned on the oracle side)."""
+    w = W("repeat", B=1, N=400, H=4, d=64, P=2, mask_mode=WN, window=50, dtype="bf16", seed=42)
+    inp = gi.make_inputs(w)
+    inp["X"] = inp["X"][:, :1].repeat(1, w.N, 1).contiguous()
+    got = run_gpu(iha, w, inp).double().cpu().numpy()
+    assert_parity(w, got, oracle_rows(w, inp))
+
+
+# ---------------------------------------------------------------------------
+# the other entry points give the same bits as iha_forward_ex
+# ---------------------------------------------------------------------------
+
+def test_step_entry_points_match_forward(iha):
+    w = W("steps", B=2, N=260, H=4, d=64, P=2, mask_mode=WN, window=40, dtype="bf16", seed=43)
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    ref = run_gpu(iha, w, dinp=dinp)
+    dt = iha.IHA_DTYPE_BF16
+    Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=torch.bfloat16, device="cuda:0")
+    QKV = torch.empty(3, w.B, w.H, w.N * w.P, w.d, dtype=torch.bfloat16, device="cuda:0")
+    Pbar = torch.empty(w.B, w.N, w.H, w.P, w.d, dtype=torch.bfloat16, device="cuda:0")
+    out = torch.empty_like(ref)
+    s = torch.cuda.current_stream()
+    iha.check(iha.iha_fold_weights(dinp["W_Q"], dinp["W_K"], dinp["W_V"], dinp["alpha_Q"], dinp["alpha_K"],
+                                   dinp["alpha_V"], w.H, w.d, w.P, dt, Wt, s))
+    iha.check(iha.iha_project(dinp["X"], Wt, w.B, w.N, w.H, w.d, w.P, dt, QKV, s))
+    iha.check(iha.iha_attention(QKV, w.B, w.N, w.H, w.d, w.P, w.mask_mode, w.window, dt, Pbar, s))
+    iha.check(iha.iha_contract(Pbar, dinp["R"], w.B, w.N, w.H, w.d, w.P, dt, out, s))
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    # the folded weights are the mixing sum (checked in float64 on a slice)
+    f = gi.as_f64(inp)
+    h, j, c = 1, 1, 5
+    col = sum(f["alpha_K"][m, h, j] * f["W_K"][:, m * w.d + c] for m in range(w.H))
+    row = Wt[1 * w.H * w.P * w.d + h * w.P * w.d + j * w.d + c].double().cpu().numpy()
+    np.testing.assert_allclose(row, col, rtol=1e-2, atol=1e-2 * np.abs(col).max())
+
+
+def test_caller_workspace_and_default_stream_entry(iha):
+    w = W("ws", B=1, N=200, H=2, d=128, P=2, mask_mode=C, window=0, dtype="bf16", seed=44)
+    dinp = to_dev(gi.make_inputs(w))
+    ref = run_gpu(iha, w, dinp=dinp)
+    nbytes = iha.iha_workspace_bytes(w.B, w.N, w.H, w.d, w.P, iha.IHA_DTYPE_BF16)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
+    out = iha.forward(dinp, H=w.H, d=w.d, P=w.P, mask_mode=w.mask_mode, window=w.window, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    out2 = torch.empty_like(ref)
+    torch.cuda.synchronize()
+    iha.check(iha.iha_forward(dinp["X"], dinp["W_Q"], dinp["W_K"], dinp["W_V"], dinp["alpha_Q"],
+                              dinp["alpha_K"], dinp["alpha_V"], dinp["R"], w.B, w.N, w.H, w.d, w.P,
+                              w.mask_mode, w.window, out2))
+    torch.cuda.synchronize()
+    assert torch.equal(out2, ref)
+
+
+def test_forward_host_buffers(iha):
+    w = W("host", B=2, N=150, H=2, d=64, P=2, mask_mode=C, window=0, dtype="bf16", seed=45)
+    inp = gi.make_inputs(w)
+    ref = run_gpu(iha, w, inp)
+    hin = {k: v.contiguous().pin_memory() for k, v in inp.items()}
+    out = torch.empty(w.B, w.N, w.D, dtype=torch.bfloat16).pin_memory()
+    s = torch.cuda.Stream()
+    nbytes = iha.iha_host_buffer_bytes(w.B, w.N, w.H, w.d, w.P, iha.IHA_DTYPE_BF16)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
+    for dev_buf in (None, buf):
+        out.zero_()
+        rc = iha.iha_forward_host(hin["X"], hin["W_Q"], hin["W_K"], hin["W_V"], hin["alpha_Q"], hin["alpha_K"],
+                                  hin["alpha_V"], hin["R"], w.B, w.N, w.H, w.d, w.P, w.mask_mode, w.window, out,
+                                  iha.IHA_DTYPE_BF16, s, dev_buf, nbytes if dev_buf is not None else 0)
+        iha.check(rc, "iha_forward_host")
+        assert torch.equal(out, ref.cpu())
+
+
+def test_device_wait_timeout_is_reported(iha):
+    """A wait that nothing will satisfy gives up after its limit, records its
+    site, and the host reads IHA_ERR_TIMEOUT; the context stays usable."""
+    assert iha.iha_check_device_status()[0] == iha.IHA_OK
+    iha.check(iha.iha_selftest_wait_timeout(None, 20))
+    rc, code = iha.iha_check_device_status()
+    assert rc == iha.IHA_ERR_TIMEOUT and code == 0x1000 | 99
+    assert iha.iha_check_device_status() == (iha.IHA_OK, 0)
+    w = W("after_timeout", B=1, N=64, H=2, d=64, P=2, mask_mode=C, window=0, dtype="bf16", seed=46)
+    inp = gi.make_inputs(w)
+    assert_parity(w, run_gpu(iha, w, inp).double().cpu().numpy(), oracle_rows(w, inp))

@@ -47,18 +47,19 @@ MASKS = [(0, 0), (1, 0), (2, 1), (2, 3), (2, 100)]
 # Values the pages print
 # ---------------------------------------------------------------------------
 
-def check_worked_example_causal(orc, g):
+def check_worked_example_causal(orc, g, projection="c"):
     """"注意力机制" section 5.4, eqs. (5.13)-(5.17): IHA with H = P = 1,
     alpha = 1, R = 1 is single-head attention; weights and outputs as printed."""
     one = np.ones((1, 1, 1))
     out, w = orc.forward(g["X"][None], g["W_Q"], g["W_K"], g["W_V"], one, one, one, np.ones((1, 1)),
-                         H=1, d=2, P=1, mask_mode=1, with_weights=True)
+                         H=1, d=2, P=1, mask_mode=1, with_weights=True, projection=projection)
     np.testing.assert_allclose(w[0, 0], g["A"], atol=TOL_PRINTED, rtol=0)
     np.testing.assert_allclose(out[0], g["O"], atol=TOL_PRINTED, rtol=0)
 
 
-def test_worked_example_causal(golden):
-    check_worked_example_causal(oracle.get(), golden("causal_single_head_example.txt"))
+@pytest.mark.parametrize("projection", ["c", "numpy"])
+def test_worked_example_causal(golden, projection):
+    check_worked_example_causal(oracle.get(), golden("causal_single_head_example.txt"), projection)
 
 
 def test_worked_example_unmasked_first_row(golden):
@@ -98,7 +99,7 @@ def test_softmax_core_rejects_empty_allowed_set():
         oracle.softmax_read([0.0, 1.0], [0, 0], np.eye(2))
 
 
-def check_scale_is_head_dim(orc, g):
+def check_scale_is_head_dim(orc, g, projection="c"):
     """Algorithm 1 scales scores by 1/sqrt(d), d = D/H the head width, not
     1/sqrt(D).  Embed the printed example as head 0 of an H = 2, d = 2
     (D = 4) problem; head 0 must still give eq. (5.17)."""
@@ -113,19 +114,20 @@ def check_scale_is_head_dim(orc, g):
     WQ, WK, WV = embed(g["W_Q"]), embed(g["W_K"]), embed(g["W_V"])
     a = identity_mixing(H, P).numpy().astype(np.float64)
     R = np.eye(H)
-    out = orc.forward(X, WQ, WK, WV, a, a, a, R, H=H, d=d, P=P, mask_mode=1)
+    out = orc.forward(X, WQ, WK, WV, a, a, a, R, H=H, d=d, P=P, mask_mode=1, projection=projection)
     np.testing.assert_allclose(out[0, :, 0:2], g["O"], atol=TOL_PRINTED, rtol=0)
 
 
-def test_scale_is_head_dim(golden):
-    check_scale_is_head_dim(oracle.get(), golden("causal_single_head_example.txt"))
+@pytest.mark.parametrize("projection", ["c", "numpy"])
+def test_scale_is_head_dim(golden, projection):
+    check_scale_is_head_dim(oracle.get(), golden("causal_single_head_example.txt"), projection)
 
 
 # ---------------------------------------------------------------------------
 # Theorem 2: inclusion of MHA, strictness on repeated tokens, parameter count
 # ---------------------------------------------------------------------------
 
-def check_contains_mha(orc, mask_mode, window, P):
+def check_contains_mha(orc, mask_mode, window, P, projection="c"):
     """Theorem 2 inclusion: alpha_{m,h,j} = 1(m = h), R keeps each head's first
     pseudo-block => IHA == MHA (Definition 1).  For P >= 2 the duplicated
     pseudo-tokens at one position only rescale equal terms, so the identity
@@ -135,15 +137,16 @@ def check_contains_mha(orc, mask_mode, window, P):
     p = rand_problem(rng, B, N, H, d, P)
     a = identity_mixing(H, P).numpy().astype(np.float64)
     p.update(alpha_Q=a, alpha_K=a, alpha_V=a, R=first_block_contraction(H, P).numpy().astype(np.float64))
-    got = run(orc, p, H, d, P, mask_mode=mask_mode, window=window)
+    got = run(orc, p, H, d, P, mask_mode=mask_mode, window=window, projection=projection)
     ref = orc.mha(p["X"], p["W_Q"], p["W_K"], p["W_V"], H=H, d=d, mask_mode=mask_mode, window=window)
     np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
 
 
+@pytest.mark.parametrize("projection", ["c", "numpy"])
 @pytest.mark.parametrize("mask_mode,window", MASKS)
 @pytest.mark.parametrize("P", [1, 2, 3])
-def test_contains_mha(mask_mode, window, P):
-    check_contains_mha(oracle.get(), mask_mode, window, P)
+def test_contains_mha(mask_mode, window, P, projection):
+    check_contains_mha(oracle.get(), mask_mode, window, P, projection)
 
 
 def repeated_token_closed_form(x, p, H, d, P):
@@ -175,7 +178,7 @@ def repeated_token_closed_form(x, p, H, d, P):
     return O.reshape(-1)
 
 
-def check_repeated_tokens(orc, mask_mode, window, P):
+def check_repeated_tokens(orc, mask_mode, window, P, projection="c"):
     """Theorem 2 strictness setting (repeated-token subspace X = 1 x^T) with
     general alpha and R: the oracle must equal the closed form above."""
     rng = np.random.default_rng(200 + P + 10 * mask_mode)
@@ -183,16 +186,17 @@ def check_repeated_tokens(orc, mask_mode, window, P):
     p = rand_problem(rng, B, N, H, d, P)
     x = rng.standard_normal(H * d)
     p["X"] = np.tile(x, (B, N, 1))
-    got = run(orc, p, H, d, P, mask_mode=mask_mode, window=window)
+    got = run(orc, p, H, d, P, mask_mode=mask_mode, window=window, projection=projection)
     ref = repeated_token_closed_form(x, p, H, d, P)
     for t in range(N):
         np.testing.assert_allclose(got[0, t], ref, atol=1e-12, rtol=0)
 
 
+@pytest.mark.parametrize("projection", ["c", "numpy"])
 @pytest.mark.parametrize("mask_mode,window", MASKS)
 @pytest.mark.parametrize("P", [1, 2, 3])
-def test_repeated_tokens_closed_form(mask_mode, window, P):
-    check_repeated_tokens(oracle.get(), mask_mode, window, P)
+def test_repeated_tokens_closed_form(mask_mode, window, P, projection):
+    check_repeated_tokens(oracle.get(), mask_mode, window, P, projection)
 
 
 def test_repeated_tokens_uniform_softmax():
@@ -334,17 +338,18 @@ def window_one_closed_form(p, H, d, P):
     return out.reshape(1, N, H * d)
 
 
-def check_window_one(orc):
+def check_window_one(orc, projection="c"):
     """The window's edge: t - t' < w with w = 1 admits t' = t only."""
     rng = np.random.default_rng(900)
     B, N, H, d, P = 1, 5, 2, 3, 3
     p = rand_problem(rng, B, N, H, d, P)
-    got = run(orc, p, H, d, P, mask_mode=2, window=1)
+    got = run(orc, p, H, d, P, mask_mode=2, window=1, projection=projection)
     np.testing.assert_allclose(got, window_one_closed_form(p, H, d, P), atol=1e-12, rtol=0)
 
 
-def test_window_one_closed_form():
-    check_window_one(oracle.get())
+@pytest.mark.parametrize("projection", ["c", "numpy"])
+def test_window_one_closed_form(projection):
+    check_window_one(oracle.get(), projection)
 
 
 def test_linear_in_R_and_alpha_V():
@@ -358,6 +363,18 @@ def test_linear_in_R_and_alpha_V():
     np.testing.assert_allclose(f(R=p["R"] + 2 * R2), f() + 2 * f(R=R2), atol=1e-12)
     A2 = rng.standard_normal(p["alpha_V"].shape)
     np.testing.assert_allclose(f(alpha_V=p["alpha_V"] - 3 * A2), f() - 3 * f(alpha_V=A2), atol=1e-12)
+
+
+def test_projection_modes_agree():
+    """The C projection loop and the library-matmul projection give the same
+    forward pass (rounding only)."""
+    rng = np.random.default_rng(1050)
+    B, N, H, d, P = 2, 11, 3, 4, 2
+    p = rand_problem(rng, B, N, H, d, P)
+    for mm, w in MASKS:
+        a = run(oracle.get(), p, H, d, P, mask_mode=mm, window=w, projection="c")
+        b = run(oracle.get(), p, H, d, P, mask_mode=mm, window=w, projection="numpy")
+        np.testing.assert_allclose(a, b, atol=1e-13, rtol=0)
 
 
 def test_selected_rows_match_full_run():
@@ -438,7 +455,8 @@ MUTANTS = {
 def _pin_suite(orc, g):
     checks = [lambda: check_worked_example_causal(orc, g),
               lambda: check_scale_is_head_dim(orc, g),
-              lambda: check_window_one(orc)]
+              lambda: check_window_one(orc),
+              lambda: check_window_one(orc, "numpy")]
     for P in (1, 2, 3):
         for mm, w in MASKS:
             checks.append(lambda P=P, mm=mm, w=w: check_contains_mha(orc, mm, w, P))

@@ -1,0 +1,274 @@
+// iha_api.cu -- the C ABI declared in include/iha.h: argument validation, workspace
+// layout, the per-device status word, and the launch sequence fold -> project ->
+// attention -> contract of "Interleaved Head Attention" Algorithm 1.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "iha.h"
+#include "iha_internal.h"
+
+namespace iha {
+
+// Per-device word that kernels set (first writer wins) when a bounded wait expires.
+static __device__ int g_status_word;
+
+static constexpr int kMaxDevices = 64;
+static int *g_status_ptr[kMaxDevices];
+static std::mutex g_mu;
+
+static int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+// Device address of g_status_word on the current device (looked up once per device;
+// the host-side name of the variable is only a stand-in for it).
+static int *status_ptr() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int device_sm_count() {
+    static int counts[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 1;
+    if (!counts[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        counts[dev] = n > 0 ? n : 1;
+    }
+    return counts[dev];
+}
+
+static size_t elem_size(int dtype) { return dtype == IHA_DTYPE_BF16 ? 2 : 4; }
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static int validate_shape(int B, int N, int H, int d, int P, int dtype) {
+    if (B <= 0 || N <= 0 || H <= 0 || d <= 0 || P <= 0) return IHA_ERR_INVALID_ARG;
+    if (dtype != IHA_DTYPE_F32 && dtype != IHA_DTYPE_BF16) return IHA_ERR_INVALID_ARG;
+    const long long L = (long long)N * P, D = (long long)H * d;
+    // index ranges the kernels use: int for rows/columns, grid dims < 2^31 / 65536
+    if (L > 65535LL * 256 || D > (1LL << 20) || (long long)B * N > INT_MAX / 2 || (long long)B * H > INT_MAX / 2 ||
+        3LL * H * P * d > INT_MAX / 2)
+        return IHA_ERR_UNSUPPORTED;
+    if (dtype == IHA_DTYPE_BF16 && d != 64 && d != 128) return IHA_ERR_UNSUPPORTED;
+    if (dtype == IHA_DTYPE_F32 && d > 256) return IHA_ERR_UNSUPPORTED;
+    return IHA_OK;
+}
+
+static int validate_mask(int mask_mode, int window) {
+    if (mask_mode < IHA_MASK_NONE || mask_mode > IHA_MASK_WINDOW) return IHA_ERR_INVALID_ARG;
+    if (mask_mode == IHA_MASK_WINDOW && window < 1) return IHA_ERR_INVALID_ARG;
+    return IHA_OK;
+}
+
+struct WsLayout {
+    size_t wt, qkv, pbar, total;
+};
+
+static WsLayout ws_layout(const Shape &sh, int dtype) {
+    const size_t es = elem_size(dtype);
+    WsLayout w;
+    w.wt = 0;
+    w.qkv = align256((size_t)sh.wt_rows() * (size_t)sh.D() * es);
+    w.pbar = w.qkv + align256(3 * (size_t)sh.qkv_elems() * es);
+    w.total = w.pbar + align256((size_t)sh.B * sh.N * sh.H * sh.P * sh.d * es);
+    return w;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? IHA_OK : IHA_ERR_CUDA; }
+
+static int run_forward(const void *X, const void *WQ, const void *WK, const void *WV, const float *aQ,
+                       const float *aK, const float *aV, const float *R, const Shape &sh, int mask_mode, int window,
+                       void *out, int dtype, cudaStream_t st, void *workspace, size_t workspace_bytes) {
+    const WsLayout lay = ws_layout(sh, dtype);
+    bool own = false;
+    if (!workspace) {
+        if (cudaMallocAsync(&workspace, lay.total, st) != cudaSuccess) return IHA_ERR_CUDA;
+        own = true;
+    } else if (workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255)) {
+        return IHA_ERR_WORKSPACE;
+    }
+    int *status = status_ptr();
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *Wt = ws + lay.wt, *QKV = ws + lay.qkv, *Pbar = ws + lay.pbar;
+    cudaError_t e = launch_fold(WQ, WK, WV, aQ, aK, aV, sh, dtype, Wt, st);
+    if (e == cudaSuccess) e = launch_project(X, Wt, sh, dtype, QKV, st, status);
+    if (e == cudaSuccess) e = launch_attention(QKV, sh, mask_mode, window, dtype, Pbar, st, status);
+    if (e == cudaSuccess) e = launch_contract(Pbar, R, sh, dtype, out, st);
+    if (own) {
+        const cudaError_t e2 = cudaFreeAsync(workspace, st);
+        if (e == cudaSuccess) e = e2;
+    }
+    return cuda_status(e);
+}
+
+}  // namespace iha
+
+using namespace iha;
+
+extern "C" {
+
+const char *iha_error_string(int status) {
+    switch (status) {
+        case IHA_OK: return "ok";
+        case IHA_ERR_INVALID_ARG: return "invalid argument";
+        case IHA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case IHA_ERR_WORKSPACE: return "workspace too small or misaligned";
+        case IHA_ERR_CUDA: return "CUDA error";
+        case IHA_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+size_t iha_workspace_bytes(int B, int N, int H, int d, int P, int dtype) {
+    if (validate_shape(B, N, H, d, P, dtype) != IHA_OK) return 0;
+    return ws_layout(Shape{B, N, H, d, P}, dtype).total;
+}
+
+int iha_forward_ex(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
+                   const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
+                   int mask_mode, int window, void *out, int dtype, void *stream, void *workspace,
+                   size_t workspace_bytes) {
+    if (!X || !W_Q || !W_K || !W_V || !alpha_Q || !alpha_K || !alpha_V || !R || !out) return IHA_ERR_INVALID_ARG;
+    int rc = validate_shape(B, N, H, d, P, dtype);
+    if (rc == IHA_OK) rc = validate_mask(mask_mode, window);
+    if (rc != IHA_OK) return rc;
+    return run_forward(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, Shape{B, N, H, d, P}, mask_mode, window, out,
+                       dtype, static_cast<cudaStream_t>(stream), workspace, workspace_bytes);
+}
+
+int iha_forward(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
+                const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
+                int mask_mode, int window, void *out) {
+    return iha_forward_ex(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, out,
+                          IHA_DTYPE_BF16, nullptr, nullptr, 0);
+}
+
+int iha_check_device_status(void *stream, int *code_out) {
+    if (code_out) *code_out = 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return IHA_ERR_CUDA;
+    int *p = status_ptr();
+    if (!p) return IHA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return IHA_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return IHA_ERR_CUDA;
+    }
+    if (code_out) *code_out = word;
+    return word ? IHA_ERR_TIMEOUT : IHA_OK;
+}
+
+size_t iha_host_buffer_bytes(int B, int N, int H, int d, int P, int dtype) {
+    if (validate_shape(B, N, H, d, P, dtype) != IHA_OK) return 0;
+    const Shape sh{B, N, H, d, P};
+    const size_t es = elem_size(dtype);
+    const size_t x = (size_t)B * N * sh.D() * es, w = (size_t)sh.D() * sh.D() * es;
+    const size_t a = (size_t)H * H * P * sizeof(float), r = (size_t)H * H * P * sizeof(float);
+    return align256(x) + 3 * align256(w) + 3 * align256(a) + align256(r) + align256(x) + ws_layout(sh, dtype).total;
+}
+
+int iha_forward_host(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
+                     const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
+                     int mask_mode, int window, void *out, int dtype, void *stream, void *device_buffer,
+                     size_t device_buffer_bytes) {
+    if (!X || !W_Q || !W_K || !W_V || !alpha_Q || !alpha_K || !alpha_V || !R || !out) return IHA_ERR_INVALID_ARG;
+    int rc = validate_shape(B, N, H, d, P, dtype);
+    if (rc == IHA_OK) rc = validate_mask(mask_mode, window);
+    if (rc != IHA_OK) return rc;
+    const Shape sh{B, N, H, d, P};
+    const size_t need = iha_host_buffer_bytes(B, N, H, d, P, dtype);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool own = false;
+    if (!device_buffer) {
+        if (cudaMallocAsync(&device_buffer, need, st) != cudaSuccess) return IHA_ERR_CUDA;
+        own = true;
+    } else if (device_buffer_bytes < need || (reinterpret_cast<uintptr_t>(device_buffer) & 255)) {
+        return IHA_ERR_WORKSPACE;
+    }
+    const size_t es = elem_size(dtype);
+    const size_t xb = (size_t)B * N * sh.D() * es, wb = (size_t)sh.D() * sh.D() * es;
+    const size_t ab = (size_t)H * H * P * sizeof(float), rb = ab;
+    uint8_t *p = static_cast<uint8_t *>(device_buffer);
+    auto take = [&](size_t bytes) {
+        uint8_t *q = p;
+        p += align256(bytes);
+        return q;
+    };
+    void *dX = take(xb), *dWQ = take(wb), *dWK = take(wb), *dWV = take(wb);
+    float *daQ = (float *)take(ab), *daK = (float *)take(ab), *daV = (float *)take(ab), *dR = (float *)take(rb);
+    void *dOut = take(xb);
+    void *ws = p;
+    cudaError_t e = cudaSuccess;
+    const void *srcs[8] = {X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R};
+    void *dsts[8] = {dX, dWQ, dWK, dWV, daQ, daK, daV, dR};
+    const size_t sizes[8] = {xb, wb, wb, wb, ab, ab, ab, rb};
+    for (int i = 0; i < 8 && e == cudaSuccess; ++i)
+        e = cudaMemcpyAsync(dsts[i], srcs[i], sizes[i], cudaMemcpyHostToDevice, st);
+    rc = e == cudaSuccess ? IHA_OK : IHA_ERR_CUDA;
+    if (rc == IHA_OK)
+        rc = run_forward(dX, dWQ, dWK, dWV, daQ, daK, daV, dR, sh, mask_mode, window, dOut, dtype, st, ws,
+                         ws_layout(sh, dtype).total);
+    if (rc == IHA_OK && cudaMemcpyAsync(out, dOut, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess) rc = IHA_ERR_CUDA;
+    if (own && cudaFreeAsync(device_buffer, st) != cudaSuccess && rc == IHA_OK) rc = IHA_ERR_CUDA;
+    const int rc2 = iha_check_device_status(stream, nullptr);
+    return rc != IHA_OK ? rc : rc2;
+}
+
+int iha_selftest_wait_timeout(void *stream, int limit_ms) {
+    if (limit_ms < 1 || limit_ms > 10000) return IHA_ERR_INVALID_ARG;
+    int *status = status_ptr();
+    if (!status) return IHA_ERR_CUDA;
+    return cuda_status(
+        launch_wait_selftest(status, (unsigned long long)limit_ms * 1000000ull, static_cast<cudaStream_t>(stream)));
+}
+
+int iha_fold_weights(const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q, const float *alpha_K,
+                     const float *alpha_V, int H, int d, int P, int dtype, void *Wt, void *stream) {
+    if (!W_Q || !W_K || !W_V || !alpha_Q || !alpha_K || !alpha_V || !Wt) return IHA_ERR_INVALID_ARG;
+    const int rc = validate_shape(1, 1, H, d, P, dtype);
+    if (rc != IHA_OK) return rc;
+    return cuda_status(launch_fold(W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, Shape{1, 1, H, d, P}, dtype, Wt,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int iha_project(const void *X, const void *Wt, int B, int N, int H, int d, int P, int dtype, void *QKV,
+                void *stream) {
+    if (!X || !Wt || !QKV) return IHA_ERR_INVALID_ARG;
+    const int rc = validate_shape(B, N, H, d, P, dtype);
+    if (rc != IHA_OK) return rc;
+    return cuda_status(
+        launch_project(X, Wt, Shape{B, N, H, d, P}, dtype, QKV, static_cast<cudaStream_t>(stream), status_ptr()));
+}
+
+int iha_attention(const void *QKV, int B, int N, int H, int d, int P, int mask_mode, int window, int dtype,
+                  void *Pbar, void *stream) {
+    if (!QKV || !Pbar) return IHA_ERR_INVALID_ARG;
+    int rc = validate_shape(B, N, H, d, P, dtype);
+    if (rc == IHA_OK) rc = validate_mask(mask_mode, window);
+    if (rc != IHA_OK) return rc;
+    return cuda_status(launch_attention(QKV, Shape{B, N, H, d, P}, mask_mode, window, dtype, Pbar,
+                                        static_cast<cudaStream_t>(stream), status_ptr()));
+}
+
+int iha_contract(const void *Pbar, const float *R, int B, int N, int H, int d, int P, int dtype, void *out,
+                 void *stream) {
+    if (!Pbar || !R || !out) return IHA_ERR_INVALID_ARG;
+    const int rc = validate_shape(B, N, H, d, P, dtype);
+    if (rc != IHA_OK) return rc;
+    return cuda_status(launch_contract(Pbar, R, Shape{B, N, H, d, P}, dtype, out, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,57 @@
+// iha_internal.h -- launchers shared by the C-ABI translation unit and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace iha {
+
+// Wait-site codes written to the status word (low 12 bits) when a bounded wait expires.
+enum WaitSite {
+    kSiteProjProducer = 1,
+    kSiteProjMma = 2,
+    kSiteProjEpilogue = 3,
+    kSiteProjMmaAcc = 4,
+    kSiteAttnProducer = 16,
+    kSiteAttnMmaQ = 17,
+    kSiteAttnMmaK = 18,
+    kSiteAttnMmaP = 19,
+    kSiteAttnMmaV = 20,
+    kSiteAttnSoftmax = 21,
+    kSiteAttnEpilogue = 22,
+    kSiteSelfTest = 99,
+};
+
+struct Shape {
+    int B, N, H, d, P;
+    long long D() const { return (long long)H * d; }
+    long long L() const { return (long long)N * P; }                     // stacked length
+    long long qkv_elems() const { return (long long)B * H * N * P * d; }  // one of Qbar/Kbar/Vbar
+    long long wt_rows() const { return 3LL * H * P * d; }
+};
+
+// Step 1+2 weights: Wt[(s,h,j,c)][k] = sum_m alpha_s[m,h,j] W_s[k][m*d + c].
+cudaError_t launch_fold(const void *WQ, const void *WK, const void *WV, const float *aQ, const float *aK,
+                        const float *aV, const Shape &sh, int dtype, void *Wt, cudaStream_t st);
+
+// Steps 1+2 + stacking: QKV = X Wt^T in the stacked [s][B][H][N*P][d] layout.
+cudaError_t launch_project(const void *X, const void *Wt, const Shape &sh, int dtype, void *QKV,
+                           cudaStream_t st, int *status);
+
+// Step 3: masked softmax attention per head over the stacked sequence -> Pbar [B][N][H][P][d].
+cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
+                             void *Pbar, cudaStream_t st, int *status);
+
+// Step 4: out[b][t][h][:] = sum_i R[h][i] Pbar[b][t][i][:], i = h'*P + j.
+cudaError_t launch_contract(const void *Pbar, const float *R, const Shape &sh, int dtype, void *out,
+                            cudaStream_t st);
+
+// A kernel whose only wait can never be satisfied: it must give up after limit_ns and
+// record kSiteSelfTest in the status word (exercises the failure path of every wait).
+cudaError_t launch_wait_selftest(int *status, unsigned long long limit_ns, cudaStream_t st);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace iha
