@@ -1,0 +1,438 @@
+"""Benchmark of the Interleaved Head Attention forward pass on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+fold (alpha into W) -> projection GEMM into the stacked layout -> attention over
+the stacked sequence -> R contraction, launched through the library's step
+entry points on one stream, each kernel bracketed by CUDA events on that stream.
+L2 is flushed (256 MiB write) between steps, outside the timed events.
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica of the workload (weak scaling; the forward pass has no
+cross-sample exchange), and the step time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the method: the pages ship no code) on the host cores, on a bounded sample of
+the same workload, and prints the same JSON line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import iha_inputs as gi  # noqa: E402
+
+METRIC = "IHA fwd pseudo-tokens/s and TFLOP/s (% of GB300 dense BF16 peak), 1 GPU"
+UNIT = "pseudo-tokens/s"
+DEFAULT_WORKLOAD = "bf16_causal_p4_n8192"
+DATA = ("synthetic: seeded SplitMix64 + Box-Muller; X~N(0,1), W~N(0,1/D), alpha~N(0,1/H), "
+        "R~N(0,1/(H*P)); random-init weights, bf16-rounded")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return dict(hbm=m["hbm_gbs"], bf16=m["bf16_tflops"], bf16_sustained=m["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# work accounting (algorithmic, per step)
+# ---------------------------------------------------------------------------
+
+def token_pairs(w) -> int:
+    """Readable (query token, key token) pairs of one sequence under the mask."""
+    N = w.N
+    if w.mask_mode == gi.MASK_NONE:
+        return N * N
+    if w.mask_mode == gi.MASK_CAUSAL or w.window >= N:
+        return N * (N + 1) // 2
+    ww = w.window
+    # sum_t min(t + 1, w)
+    return ww * (ww + 1) // 2 + (N - ww) * ww
+
+
+def work(w):
+    B, N, H, d, P, D = w.B, w.N, w.H, w.d, w.P, w.D
+    pairs = B * H * P * P * token_pairs(w)              # readable pseudo-token pairs
+    attn = 4.0 * d * pairs                              # QK^T and PV, 2 flops per MAC
+    proj_folded = 2.0 * B * N * D * (3 * H * P * d)     # executed GEMM
+    proj_heads = 2.0 * B * N * D * 3 * D                # X W^(m), all heads, Q/K/V
+    mixing = 2.0 * B * N * 3 * (H * P) * D              # sum over m of alpha * (X W^(m))
+    contract = 2.0 * B * N * (H * P) * D                # R contraction
+    es = 2
+    bytes_contract = es * (B * N * H * P * d + B * N * D)
+    bytes_fold = es * (3 * D * D + 3 * H * P * d * D)
+    return dict(pairs=pairs, attn=attn, proj_folded=proj_folded, algorithmic=proj_heads + mixing + attn + contract,
+                executed=proj_folded + attn + contract, bytes_contract=bytes_contract, bytes_fold=bytes_fold,
+                pseudo_tokens=B * P * N)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rows(w, n_tokens):
+    """n_tokens query tokens of batch element 0, evenly spaced over [0, N), so the
+    sample's average cost per token is the workload's."""
+    n = min(n_tokens, w.N)
+    toks = sorted({int(round((i + 0.5) * w.N / n)) for i in range(n)})
+    return [t for t in toks if t < w.N]
+
+
+def time_oracle(w, inp_f64, n_tokens):
+    import oracle
+    rows = oracle_sample_rows(w, n_tokens)
+    f = inp_f64
+    t0 = time.perf_counter()
+    oracle.forward(f["X"][:1], f["W_Q"], f["W_K"], f["W_V"], f["alpha_Q"], f["alpha_K"], f["alpha_V"], f["R"],
+                   H=w.H, d=w.d, P=w.P, mask_mode=w.mask_mode, window=w.window, rows=rows, projection="numpy")
+    dt = time.perf_counter() - t0
+    return w.P * len(rows) / dt, dt, len(rows)
+
+
+def oracle_sample_desc(w, n):
+    return (f"batch element 0, {n} query tokens evenly spaced over N={w.N} (all P={w.P} pseudo-rows each, "
+            f"every head); projections of the tokens they read by float64 BLAS matmul, the rest in C")
+
+
+# ---------------------------------------------------------------------------
+# distributed setup (torchrun); every rank is an independent replica
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def max_over_ranks(x: float, dist, device):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, w):
+    rank, world, local, dist = dist_setup(args.gpus)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    import oracle
+    oracle.build()
+    f = gi.as_f64(gi.make_inputs(w))
+    per_step_tokens = args.ref_tokens
+    times, vals = [], []
+    for i in range(args.warmup + args.steps):
+        v, dt, n = time_oracle(w, f, per_step_tokens)
+        if i >= args.warmup:
+            times.append(dt)
+            vals.append(v)
+    value = w.P * n * len(times) / sum(times)
+    cores = oracle.default_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+        "config": config_of(w, l2="host memory"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": oracle_sample_desc(w, n) + " per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def config_of(w, l2):
+    return {"workload": w.name, "B": w.B, "N": w.N, "D": w.D, "H": w.H, "d": w.d, "P": w.P,
+            "stacked_length": w.PN, "mask": ["none", "causal", "causal+window"][w.mask_mode],
+            "window": w.window if w.mask_mode == gi.MASK_WINDOW else None, "l2": l2}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, w):
+    rank, world, local, dist = dist_setup(args.gpus)
+    import transformer_attention_variant_gb300 as iha
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    wk = work(w)
+    dt = iha.IHA_DTYPE_BF16 if w.dtype == "bf16" else iha.IHA_DTYPE_F32
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    es = 2 if w.dtype == "bf16" else 4
+
+    host = gi.make_inputs(w)
+    d = {k: v.to(dev).contiguous() for k, v in host.items()}
+    Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=tdt, device=dev)
+    QKV = torch.empty(3, w.B, w.H, w.N * w.P, w.d, dtype=tdt, device=dev)
+    Pbar = torch.empty(w.B, w.N, w.H, w.P, w.d, dtype=tdt, device=dev)
+    out = torch.empty(w.B, w.N, w.D, dtype=tdt, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(ev=None):
+        s = stream
+        if ev is not None:
+            ev[0].record(s)
+        iha.check(iha.iha_fold_weights(d["W_Q"], d["W_K"], d["W_V"], d["alpha_Q"], d["alpha_K"], d["alpha_V"],
+                                       w.H, w.d, w.P, dt, Wt, s), "fold")
+        if ev is not None:
+            ev[1].record(s)
+        iha.check(iha.iha_project(d["X"], Wt, w.B, w.N, w.H, w.d, w.P, dt, QKV, s), "project")
+        if ev is not None:
+            ev[2].record(s)
+        iha.check(iha.iha_attention(QKV, w.B, w.N, w.H, w.d, w.P, w.mask_mode, w.window, dt, Pbar, s), "attention")
+        if ev is not None:
+            ev[3].record(s)
+        iha.check(iha.iha_contract(Pbar, d["R"], w.B, w.N, w.H, w.d, w.P, dt, out, s), "contract")
+        if ev is not None:
+            ev[4].record(s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step()
+    torch.cuda.synchronize(dev)
+    rc, code = iha.iha_check_device_status(stream)
+    iha.check(rc, f"device status after warm-up ({code:#x})")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)          # evict L2 between steps (outside the events)
+                step(events[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    barrier(dist)
+    rc, code = iha.iha_check_device_status(stream)
+    iha.check(rc, f"device status after timed steps ({code:#x})")
+
+    names = ["fold", "project", "attention", "contract"]
+    k_ms = {n: [] for n in names}
+    step_ms = []
+    for ev in events:
+        for j, n in enumerate(names):
+            k_ms[n].append(ev[j].elapsed_time(ev[j + 1]))
+        step_ms.append(ev[0].elapsed_time(ev[4]))
+    mean_step = sum(step_ms) / len(step_ms)
+    mean_step = max_over_ranks(mean_step, dist, dev)
+    kmean = {n: sum(v) / len(v) for n, v in k_ms.items()}
+    value = world * wk["pseudo_tokens"] / (mean_step * 1e-3)
+
+    # roofline of the dominant kernel
+    dom = max(kmean, key=kmean.get)
+    if dom == "attention":
+        ach = wk["attn"] / (kmean[dom] * 1e-3) / 1e12
+        roof = {"kernel": "attn_fwd_tc", "bound": "tensor", "achieved": ach, "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16"],
+                "frac_of_sustained": ach / peaks["bf16_sustained"],
+                "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+                else "fallback 1.9 PFLOP/s"}
+        traffic_key = "attention"
+    elif dom == "project":
+        ach = wk["proj_folded"] / (kmean[dom] * 1e-3) / 1e12
+        roof = {"kernel": "proj_gemm_tc", "bound": "tensor", "achieved": ach, "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16"],
+                "frac_of_sustained": ach / peaks["bf16_sustained"], "peak_source": peaks["source"]}
+        traffic_key = "project"
+    else:
+        b = wk["bytes_contract"] if dom == "contract" else wk["bytes_fold"]
+        ach = b / (kmean[dom] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": ach / peaks["hbm"], "peak_source": peaks["source"]}
+        traffic_key = dom
+    roof["traffic"] = traffic_per_launch(w.name, traffic_key)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": DATA,
+        "config": config_of(w, "flushed between steps (256 MiB write outside the timed events)"),
+        "tflops": {
+            "attention_exact_pairs": wk["attn"] / (kmean["attention"] * 1e-3) / 1e12,
+            "forward_algorithmic": wk["algorithmic"] / (mean_step * 1e-3) / 1e12,
+            "forward_executed_folded": wk["executed"] / (mean_step * 1e-3) / 1e12,
+            "projection_executed": wk["proj_folded"] / (kmean["project"] * 1e-3) / 1e12,
+        },
+        "kernel_ms": kmean,
+        "roofline": roof,
+        "gpu_launches": 4 * args.steps,
+        "wall_s_timed_region": t_wall,
+        "clocks": clk.summary(),
+    }
+
+    # end to end through the host-buffer entry point (pinned host inputs, copies in the timed region)
+    if rank == 0 or True:
+        hin = {k: v.contiguous().pin_memory() for k, v in host.items()}
+        hout = torch.empty(w.B, w.N, w.D, dtype=tdt).pin_memory()
+        nbytes = iha.iha_host_buffer_bytes(w.B, w.N, w.H, w.d, w.P, dt)
+        del QKV, Pbar, Wt
+        dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        h2d = sum(v.numel() * v.element_size() for v in hin.values())
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_call():
+            rc = iha.iha_forward_host(hin["X"], hin["W_Q"], hin["W_K"], hin["W_V"], hin["alpha_Q"], hin["alpha_K"],
+                                      hin["alpha_V"], hin["R"], w.B, w.N, w.H, w.d, w.P, w.mask_mode, w.window,
+                                      hout, dt, stream, dbuf, nbytes)
+            iha.check(rc, "iha_forward_host")
+
+        for _ in range(max(1, args.warmup)):
+            e2e_call()
+        n_e2e = max(3, min(args.steps, 50))
+        t = []
+        for _ in range(n_e2e):
+            flush.fill_(0)
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            e2e_call()
+            t.append(time.perf_counter() - t0)
+        e2e_s = max_over_ranks(sum(t) / len(t), dist, dev)
+        line["e2e"] = {"value": world * wk["pseudo_tokens"] / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
+                       "call": "iha_forward_host (pinned host buffers, preallocated device buffer)"}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        f = gi.as_f64(host)
+        v, secs, n = time_oracle(w, f, args.cpu_tokens)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+                                "sample": oracle_sample_desc(w, n), "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def traffic_per_launch(workload, kernel):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, if one
+    matches this workload and kernel; None otherwise."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        t = json.load(f)
+    return t.get(workload, {}).get(kernel)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=gi.WORKLOAD_ORDER)
+    ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=16, help="oracle sample size per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = gi.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -13,8 +13,8 @@ from conftest import ROOT
 
 @pytest.fixture(scope="module")
 def iha():
-    from transformer_attention_variant_gb300 import build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import transformer_attention_variant_gb300 as m
     return m
 
