@@ -360,7 +360,7 @@ def run_gpu(args, w):
     }
 
     # end to end through the host-buffer entry point (pinned host inputs, copies in the timed region)
-    if rank == 0 or True:
+    if not args.no_e2e:
         hin = {k: v.contiguous().pin_memory() for k, v in host.items()}
         hout = torch.empty(w.B, w.N, w.D, dtype=tdt).pin_memory()
         nbytes = iha.iha_host_buffer_bytes(w.B, w.N, w.H, w.d, w.P, dt)
@@ -424,10 +424,17 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=16, help="oracle sample size per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
+    ap.add_argument("--N", type=int, default=None,
+                    help="shrink the workload's sequence length (smaller cases for profiler captures); "
+                         "the window stays N/(2P) for windowed workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = gi.WORKLOADS[args.workload]
+    if args.N is not None:
+        w = w.with_(N=args.N, name=f"{w.name}@N={args.N}",
+                    window=args.N // (2 * w.P) if w.mask_mode == gi.MASK_WINDOW else w.window)
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -63,6 +63,7 @@ static int validate_shape(int B, int N, int H, int d, int P, int dtype) {
         3LL * H * P * d > INT_MAX / 2)
         return IHA_ERR_UNSUPPORTED;
     if (dtype == IHA_DTYPE_BF16 && d != 64 && d != 128) return IHA_ERR_UNSUPPORTED;
+    if (H > 64) return IHA_ERR_UNSUPPORTED;   // the weight fold keeps one W column per head in registers
     if (dtype == IHA_DTYPE_F32 && d > 256) return IHA_ERR_UNSUPPORTED;
     return IHA_OK;
 }

@@ -28,12 +28,15 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
 // ---------------------------------------------------------------------------------------
-// fold: block = (32 k) x (16 c) tile of one s; loops over every (h, j).
-// smem: Ws[m][kk][cc] (padded) and alpha_s.
+// fold: block = one s, FOLD_CB consecutive c, FOLD_KB consecutive k.  The W slab
+// W_s[k0..k0+KB)[m][c0..c0+CB) for all m is staged in shared memory as [m][cc][kk]
+// (so a warp's 32 consecutive k read consecutive words); alpha_s sits in shared memory
+// too.  Thread (group g, kk) produces, for its k, the output rows (h, j, c) of its
+// group; a row's KB values are written by KB consecutive threads (coalesced).
 // ---------------------------------------------------------------------------------------
-constexpr int FOLD_TK = 32, FOLD_TC = 16, FOLD_THREADS = 256;
+constexpr int FOLD_KB = 128, FOLD_CB = 16, FOLD_THREADS = 256, FOLD_GROUPS = FOLD_THREADS / FOLD_KB;
 
-template <typename T>
+template <typename T, int MAXH>
 __global__ void __launch_bounds__(FOLD_THREADS)
 fold_kernel(const T *__restrict__ WQ, const T *__restrict__ WK, const T *__restrict__ WV,
             const float *__restrict__ aQ, const float *__restrict__ aK, const float *__restrict__ aV,
@@ -42,69 +45,83 @@ fold_kernel(const T *__restrict__ WQ, const T *__restrict__ WK, const T *__restr
     const int s = blockIdx.z;
     const T *W = s == 0 ? WQ : (s == 1 ? WK : WV);
     const float *alpha = s == 0 ? aQ : (s == 1 ? aK : aV);
-    const long long D = (long long)H * d, Hd = D;
-    const int k0 = blockIdx.x * FOLD_TK, c0 = blockIdx.y * FOLD_TC;
-    float *Ws = fsm;                                   // [H][FOLD_TK][FOLD_TC + 1]
-    float *as = fsm + (size_t)H * FOLD_TK * (FOLD_TC + 1);   // [H][H][P]
-    const int tile = FOLD_TK * FOLD_TC;
-    for (int idx = threadIdx.x; idx < H * tile; idx += blockDim.x) {
-        const int m = idx / tile, rem = idx % tile, kk = rem / FOLD_TC, cc = rem % FOLD_TC;
+    const long long D = (long long)H * d;
+    const int k0 = blockIdx.x * FOLD_KB, c0 = blockIdx.y * FOLD_CB;
+    float *Ws = fsm;                                          // [H][FOLD_CB][FOLD_KB]
+    float *as = fsm + (size_t)H * FOLD_CB * FOLD_KB;          // [H][H][P]
+    const int slab = FOLD_CB * FOLD_KB;
+    // load: consecutive threads take consecutive c of one (k, m) row segment
+    for (int idx = threadIdx.x; idx < H * slab; idx += blockDim.x) {
+        const int cc = idx % FOLD_CB, rest = idx / FOLD_CB, kk = rest % FOLD_KB, m = rest / FOLD_KB;
         const long long k = k0 + kk;
         const int c = c0 + cc;
-        Ws[((size_t)m * FOLD_TK + kk) * (FOLD_TC + 1) + cc] = (k < D && c < d) ? ld_f(W + k * Hd + (long long)m * d + c) : 0.f;
+        Ws[((size_t)m * FOLD_CB + cc) * FOLD_KB + kk] = (k < D && c < d) ? ld_f(W + k * D + (long long)m * d + c) : 0.f;
     }
     for (int idx = threadIdx.x; idx < H * H * P; idx += blockDim.x) as[idx] = alpha[idx];
     __syncthreads();
+    const int kk = threadIdx.x % FOLD_KB, g = threadIdx.x / FOLD_KB;
+    const long long k = k0 + kk;
+    if (k >= D) return;
     const long long HPd = (long long)H * P * d, Pd = (long long)P * d;
-    for (int pair = 0; pair < H * P; ++pair) {
-        const int h = pair / P, j = pair % P;
-        for (int e = threadIdx.x; e < tile; e += blockDim.x) {
-            const int kk = e % FOLD_TK, cc = e / FOLD_TK;
+    const int ccmax = d - c0 < FOLD_CB ? d - c0 : FOLD_CB;
+    for (int cc = 0; cc < ccmax; ++cc) {
+        float w[MAXH];   // W_s[k][m][c0 + cc], m < H <= MAXH (registers: the loops are unrolled)
+#pragma unroll
+        for (int m = 0; m < MAXH; ++m) w[m] = m < H ? Ws[((size_t)m * FOLD_CB + cc) * FOLD_KB + kk] : 0.f;
+        for (int pair = g; pair < H * P; pair += FOLD_GROUPS) {
+            const int h = pair / P, j = pair % P;
             float acc = 0.f;
-            for (int m = 0; m < H; ++m)
-                acc = fmaf(as[((size_t)m * H + h) * P + j], Ws[((size_t)m * FOLD_TK + kk) * (FOLD_TC + 1) + cc], acc);
-            const long long k = k0 + kk;
-            const int c = c0 + cc;
-            if (k < D && c < d) Wt[(s * HPd + h * Pd + (long long)j * d + c) * D + k] = from_f<T>(acc);
+#pragma unroll
+            for (int m = 0; m < MAXH; ++m)
+                if (m < H) acc = fmaf(as[((size_t)m * H + h) * P + j], w[m], acc);
+            Wt[(s * HPd + h * Pd + (long long)j * d + c0 + cc) * D + k] = from_f<T>(acc);
         }
     }
 }
 
-cudaError_t launch_fold(const void *WQ, const void *WK, const void *WV, const float *aQ, const float *aK,
-                        const float *aV, const Shape &sh, int dtype, void *Wt, cudaStream_t st) {
+template <typename T, int MAXH>
+static cudaError_t launch_fold_t(const void *WQ, const void *WK, const void *WV, const float *aQ, const float *aK,
+                                 const float *aV, const Shape &sh, void *Wt, cudaStream_t st) {
     const long long D = sh.D();
-    dim3 grid((unsigned)((D + FOLD_TK - 1) / FOLD_TK), (unsigned)((sh.d + FOLD_TC - 1) / FOLD_TC), 3);
-    const size_t smem = sizeof(float) * ((size_t)sh.H * FOLD_TK * (FOLD_TC + 1) + (size_t)sh.H * sh.H * sh.P);
-    cudaError_t e;
-    if (dtype == 1) {
-        e = cudaFuncSetAttribute(fold_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        fold_kernel<__nv_bfloat16><<<grid, FOLD_THREADS, smem, st>>>(
-            (const __nv_bfloat16 *)WQ, (const __nv_bfloat16 *)WK, (const __nv_bfloat16 *)WV, aQ, aK, aV,
-            (__nv_bfloat16 *)Wt, sh.H, sh.d, sh.P);
-    } else {
-        e = cudaFuncSetAttribute(fold_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        fold_kernel<float><<<grid, FOLD_THREADS, smem, st>>>((const float *)WQ, (const float *)WK,
-                                                             (const float *)WV, aQ, aK, aV, (float *)Wt, sh.H,
-                                                             sh.d, sh.P);
-    }
+    dim3 grid((unsigned)((D + FOLD_KB - 1) / FOLD_KB), (unsigned)((sh.d + FOLD_CB - 1) / FOLD_CB), 3);
+    const size_t smem = sizeof(float) * ((size_t)sh.H * FOLD_CB * FOLD_KB + (size_t)sh.H * sh.H * sh.P);
+    cudaError_t e = cudaFuncSetAttribute(fold_kernel<T, MAXH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    fold_kernel<T, MAXH><<<grid, FOLD_THREADS, smem, st>>>((const T *)WQ, (const T *)WK, (const T *)WV, aQ, aK, aV,
+                                                           (T *)Wt, sh.H, sh.d, sh.P);
     return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t launch_fold_h(const void *WQ, const void *WK, const void *WV, const float *aQ, const float *aK,
+                                 const float *aV, const Shape &sh, void *Wt, cudaStream_t st) {
+    if (sh.H <= 16) return launch_fold_t<T, 16>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
+    if (sh.H <= 32) return launch_fold_t<T, 32>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
+    if (sh.H <= 64) return launch_fold_t<T, 64>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fold(const void *WQ, const void *WK, const void *WV, const float *aQ, const float *aK,
+                        const float *aV, const Shape &sh, int dtype, void *Wt, cudaStream_t st) {
+    if (dtype == 1) return launch_fold_h<__nv_bfloat16>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
+    return launch_fold_h<float>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
+}
+
 // ---------------------------------------------------------------------------------------
-// contract: one thread = (token row bt, VEC-wide chunk of the head dim), all H output
-// heads in groups of HB.  R lives in shared memory.  Reads of one pseudo-head row by the
-// d/VEC threads of a token are contiguous.
+// contract: thread = (token, group of CON_HG output heads, VEC-wide chunk of the head dim).
+// For each pseudo-head row i it loads VEC values of Pbar[token][i][:] (the d/VEC threads
+// of one (token, group) read one contiguous row) and adds R[h][i] times them into its
+// CON_HG x VEC accumulators; R is in shared memory and read as a warp-wide broadcast.
+// The CON_HG-fold re-reads of a row hit L1, so DRAM sees Pbar once.
 // ---------------------------------------------------------------------------------------
-constexpr int CON_HB = 16, CON_THREADS = 256;
+constexpr int CON_HG = 4, CON_THREADS = 256;
 
 template <typename T, int VEC>
 struct VecLoad;
 template <>
 struct VecLoad<__nv_bfloat16, 8> {
     __device__ static void load(const __nv_bfloat16 *p, float (&v)[8]) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
         const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -124,7 +141,7 @@ struct VecLoad<__nv_bfloat16, 8> {
 template <>
 struct VecLoad<float, 4> {
     __device__ static void load(const float *p, float (&v)[4]) {
-        const float4 u = *reinterpret_cast<const float4 *>(p);
+        const float4 u = __ldg(reinterpret_cast<const float4 *>(p));
         v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
     }
     __device__ static void store(float *p, const float (&v)[4]) {
@@ -133,7 +150,7 @@ struct VecLoad<float, 4> {
 };
 template <>
 struct VecLoad<float, 1> {
-    __device__ static void load(const float *p, float (&v)[1]) { v[0] = *p; }
+    __device__ static void load(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
     __device__ static void store(float *p, const float (&v)[1]) { *p = v[0]; }
 };
 
@@ -145,61 +162,55 @@ contract_kernel(const T *__restrict__ pbar, const float *__restrict__ R, T *__re
     const int HP = H * P;
     for (int i = threadIdx.x; i < H * HP; i += blockDim.x) Rs[i] = R[i];
     __syncthreads();
-    const int cpr = d / VEC;   // chunks per row
+    const int cpr = d / VEC;                         // chunks per row
+    const int ngroups = (H + CON_HG - 1) / CON_HG;
     const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (item >= BN * cpr) return;
-    const long long bt = item / cpr;
+    if (item >= BN * ngroups * cpr) return;
     const int cc = (int)(item % cpr);
+    const long long rest = item / cpr;
+    const int hg = (int)(rest % ngroups) * CON_HG;
+    const long long bt = rest / ngroups;
     const T *src = pbar + bt * HP * (long long)d + (long long)cc * VEC;
     T *dst = out + bt * (long long)H * d + (long long)cc * VEC;
-    for (int hg = 0; hg < H; hg += CON_HB) {
-        float acc[CON_HB][VEC];
+    float acc[CON_HG][VEC];
 #pragma unroll
-        for (int a = 0; a < CON_HB; ++a)
+    for (int a = 0; a < CON_HG; ++a)
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[a][e] = 0.f;
-        for (int i = 0; i < HP; ++i) {
-            float v[VEC];
-            VecLoad<T, VEC>::load(src + (long long)i * d, v);
+        for (int e = 0; e < VEC; ++e) acc[a][e] = 0.f;
+    const float *Rg = Rs + (size_t)hg * HP;
+#pragma unroll 4
+    for (int i = 0; i < HP; ++i) {
+        float v[VEC];
+        VecLoad<T, VEC>::load(src + (long long)i * d, v);
 #pragma unroll
-            for (int a = 0; a < CON_HB; ++a) {
-                const int h = hg + a;
-                const float r = h < H ? Rs[h * HP + i] : 0.f;
+        for (int a = 0; a < CON_HG; ++a) {
+            const float r = (hg + a < H) ? Rg[a * HP + i] : 0.f;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) acc[a][e] = fmaf(r, v[e], acc[a][e]);
-            }
+            for (int e = 0; e < VEC; ++e) acc[a][e] = fmaf(r, v[e], acc[a][e]);
         }
-#pragma unroll
-        for (int a = 0; a < CON_HB; ++a)
-            if (hg + a < H) VecLoad<T, VEC>::store(dst + (long long)(hg + a) * d, acc[a]);
     }
+#pragma unroll
+    for (int a = 0; a < CON_HG; ++a)
+        if (hg + a < H) VecLoad<T, VEC>::store(dst + (long long)(hg + a) * d, acc[a]);
+}
+
+template <typename T, int VEC>
+static cudaError_t launch_contract_t(const void *Pbar, const float *R, const Shape &sh, void *out, cudaStream_t st) {
+    const long long BN = (long long)sh.B * sh.N;
+    const size_t smem = sizeof(float) * (size_t)sh.H * sh.H * sh.P;
+    const long long items = BN * ((sh.H + CON_HG - 1) / CON_HG) * (sh.d / VEC);
+    cudaError_t e = cudaFuncSetAttribute(contract_kernel<T, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    contract_kernel<T, VEC><<<(unsigned)((items + CON_THREADS - 1) / CON_THREADS), CON_THREADS, smem, st>>>(
+        (const T *)Pbar, R, (T *)out, BN, sh.H, sh.P, sh.d);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_contract(const void *Pbar, const float *R, const Shape &sh, int dtype, void *out,
                             cudaStream_t st) {
-    const long long BN = (long long)sh.B * sh.N;
-    const size_t smem = sizeof(float) * (size_t)sh.H * sh.H * sh.P;
-    cudaError_t e;
-    if (dtype == 1) {
-        const long long items = BN * (sh.d / 8);
-        e = cudaFuncSetAttribute(contract_kernel<__nv_bfloat16, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        contract_kernel<__nv_bfloat16, 8><<<(unsigned)((items + CON_THREADS - 1) / CON_THREADS), CON_THREADS, smem, st>>>(
-            (const __nv_bfloat16 *)Pbar, R, (__nv_bfloat16 *)out, BN, sh.H, sh.P, sh.d);
-    } else if (sh.d % 4 == 0) {
-        const long long items = BN * (sh.d / 4);
-        e = cudaFuncSetAttribute(contract_kernel<float, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        contract_kernel<float, 4><<<(unsigned)((items + CON_THREADS - 1) / CON_THREADS), CON_THREADS, smem, st>>>(
-            (const float *)Pbar, R, (float *)out, BN, sh.H, sh.P, sh.d);
-    } else {
-        const long long items = BN * sh.d;
-        e = cudaFuncSetAttribute(contract_kernel<float, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        contract_kernel<float, 1><<<(unsigned)((items + CON_THREADS - 1) / CON_THREADS), CON_THREADS, smem, st>>>(
-            (const float *)Pbar, R, (float *)out, BN, sh.H, sh.P, sh.d);
-    }
-    return cudaGetLastError();
+    if (dtype == 1) return launch_contract_t<__nv_bfloat16, 8>(Pbar, R, sh, out, st);
+    if (sh.d % 4 == 0) return launch_contract_t<float, 4>(Pbar, R, sh, out, st);
+    return launch_contract_t<float, 1>(Pbar, R, sh, out, st);
 }
 
 }  // namespace iha
