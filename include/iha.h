@@ -143,6 +143,9 @@ IHA_API int iha_selftest_wait_timeout(void *stream, int limit_ms);
  *   Wt   [3*H*P*d][D]   folded, transposed weights: row s*H*P*d + h*P*d + j*d + c
  *                       holds  sum_m alpha_s[m,h,j] W_s[:, m*d + c]   (s = Q, K, V)
  *   Qbar, Kbar, Vbar [B][H][N*P][d]   stacked pseudo-tokens of head h; row t*P + j
+ *                       (for IHA_DTYPE_BF16: Qbar, Kbar bfloat16, Vbar float16 -- the
+ *                       softmax weights and Vbar meet in an f16 x f16 product; for
+ *                       IHA_DTYPE_F32 all three float32)
  *                       is pseudo-token (j, t) (t-major interleaving; with a mask
  *                       on t only this ordering gives the same output as the row
  *                       concatenation j*N + t, "注意力机制" eq. (5.41))

@@ -15,9 +15,10 @@
 //     the tensor cores work on one tile while the softmax warps work on the other;
 //   - warp 8: TMA producer (Q once; K and V tiles through a 2-stage ring, 128B swizzle);
 //   - warp 9: MMA issuer: S_i = Q_i K^T (SS, M=128 N=128) into TMEM, then O_i += P_i V
-//     with P_i read from TMEM (TS form, M=128 N=d) -- P never touches shared memory;
+//     with P_i read from TMEM (TS form, M=128 N=d, f16 P and f16 V) -- P never touches
+//     shared memory;
 //   - warps 0-3 / 4-7: softmax of Q0 / Q1, one thread per row (32x32b TMEM loads): row
-//     max, exp2, row sum, bf16 P written back over its S columns.  The running max is only
+//     max, exp2 (two per MUFU op in f16x2), row sum, f16 P written back over its S columns.  The running max is only
 //     raised when a tile's max exceeds it by more than 8 (log2 units), so O (in TMEM) is
 //     rarely rescaled; values stay <= 2^8 before normalisation;
 //   - epilogue: O / l -> bf16 -> Pbar[b][t][h][j][:].
@@ -32,7 +33,12 @@ namespace iha {
 
 constexpr int AT_BM = 128;         // query rows per tile
 constexpr int AT_BN = 128;         // key rows per tile
-constexpr int AT_THREADS = 320;    // 8 softmax warps + producer + MMA
+constexpr int AT_THREADS = 384;    // 2 softmax warpgroups + 1 warpgroup (producer, MMA, 2 idle)
+// Register split (setmaxnreg): the kernel is compiled to exactly AT_LAUNCH_REGS per thread
+// (384 x 168 = 64512 registers allocated at launch); the producer/MMA warpgroup gives
+// registers back, the softmax warpgroups take them: 128 x 56 + 256 x 224 = 64512.
+constexpr int AT_LAUNCH_REGS = 168, AT_REGS_SOFTMAX = 224, AT_REGS_CONTROL = 56;
+static_assert(128 * AT_REGS_CONTROL + 256 * AT_REGS_SOFTMAX <= AT_THREADS * AT_LAUNCH_REGS, "register split");
 constexpr float AT_RESCALE_THRESHOLD = 8.0f;
 
 template <int DH>
@@ -40,8 +46,11 @@ struct AttnCfg {
     static constexpr int CHUNKS = DH / 64;               // 64-column (128-byte) swizzle chunks
     static constexpr int Q_BYTES = AT_BM * DH * 2;
     static constexpr int KV_BYTES = AT_BN * DH * 2;
-    static constexpr int STAGES = 2;
-    static constexpr int SMEM = 2 * Q_BYTES + 2 * STAGES * KV_BYTES + 256 + 1024;
+    // K tiles are freed as soon as the second S-MMA has read them, V tiles only after the
+    // second PV-MMA: K gets the deeper ring so the next K is resident before it is needed.
+    static constexpr int KSTAGES = DH == 128 ? 3 : 4;
+    static constexpr int VSTAGES = DH == 128 ? 2 : 4;
+    static constexpr int SMEM = 2 * Q_BYTES + (KSTAGES + VSTAGES) * KV_BYTES + 256 + 1024;
     __device__ static constexpr uint32_t s_col(int i) { return uint32_t(i) * 128u; }
     __device__ static constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * DH; }
 };
@@ -84,14 +93,15 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = smem;                                  // 2 tiles
-    uint8_t *sK = sQ + 2 * C::Q_BYTES;                   // STAGES tiles
-    uint8_t *sV = sK + C::STAGES * C::KV_BYTES;          // STAGES tiles
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sV + C::STAGES * C::KV_BYTES);
+    uint8_t *sK = sQ + 2 * C::Q_BYTES;                   // KSTAGES tiles
+    uint8_t *sV = sK + C::KSTAGES * C::KV_BYTES;         // VSTAGES tiles
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sV + C::VSTAGES * C::KV_BYTES);
     uint64_t *q_full = bars;
-    uint64_t *k_full = bars + 1;              // [STAGES]
-    uint64_t *v_full = k_full + C::STAGES;    // [STAGES]
-    uint64_t *kv_empty = v_full + C::STAGES;  // [STAGES]
-    uint64_t *s_full = kv_empty + C::STAGES;  // [2]
+    uint64_t *k_full = bars + 1;               // [KSTAGES]
+    uint64_t *k_empty = k_full + C::KSTAGES;   // [KSTAGES]
+    uint64_t *v_full = k_empty + C::KSTAGES;   // [VSTAGES]
+    uint64_t *v_empty = v_full + C::VSTAGES;   // [VSTAGES]
+    uint64_t *s_full = v_empty + C::VSTAGES;   // [2]
     uint64_t *p_full = s_full + 2;            // [2]
     uint64_t *o_full = p_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_full + 1);
@@ -113,14 +123,17 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < C::KSTAGES; ++s) {
             mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < C::VSTAGES; ++s) {
             mbar_init(&v_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 128);
+            mbar_init(&p_full[i], 4);   // one arrive per softmax warp
         }
         mbar_init(o_full, 1);
         *abort_flag = 0;
@@ -139,8 +152,10 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    if (warp == 8) {
+    if (warp >= 8) {
+      // control warpgroup: gives registers back, then warp 8 = TMA, warp 9 = MMA
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(AT_REGS_CONTROL));
+      if (warp == 8) {
         // ------------------------------- TMA producer -------------------------------
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
@@ -148,24 +163,33 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 for (int c = 0; c < C::CHUNKS; ++c)
                     tma_load_3d(&tmQ, q_full, sQ + i * C::Q_BYTES + c * (AT_BM * 128), c * 64,
                                 (int)(r0 + i * AT_BM), bh);
-            for (int k = 0; k < nkv; ++k) {
-                const int st = k % C::STAGES;
-                const uint32_t ph = (k / C::STAGES) & 1;
-                if (!mbar_wait(&kv_empty[st], ph ^ 1, p.status, kSiteAttnProducer, abort_flag)) break;
-                const int krow = (kv_begin + k) * AT_BN;
-                mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    tma_load_3d(&tmK, &k_full[st], sK + st * C::KV_BYTES + c * (AT_BN * 128), c * 64, krow, bh);
-                mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    tma_load_3d(&tmV, &v_full[st], sV + st * C::KV_BYTES + c * (AT_BN * 128), c * 64, krow, bh);
+            // K runs one tile ahead of V: K(k) is issued before V(k-1)
+            for (int k = 0; k <= nkv; ++k) {
+                if (k < nkv) {
+                    const int st = k % C::KSTAGES;
+                    if (!mbar_wait_lazy(&k_empty[st], ((k / C::KSTAGES) & 1) ^ 1, p.status, kSiteAttnProducer, abort_flag))
+                        break;
+                    mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tma_load_3d(&tmK, &k_full[st], sK + st * C::KV_BYTES + c * (AT_BN * 128), c * 64,
+                                    (kv_begin + k) * AT_BN, bh);
+                }
+                if (k >= 1) {
+                    const int kv = k - 1, st = kv % C::VSTAGES;
+                    if (!mbar_wait_lazy(&v_empty[st], ((kv / C::VSTAGES) & 1) ^ 1, p.status, kSiteAttnProducer, abort_flag))
+                        break;
+                    mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tma_load_3d(&tmV, &v_full[st], sV + st * C::KV_BYTES + c * (AT_BN * 128), c * 64,
+                                    (kv_begin + kv) * AT_BN, bh);
+                }
             }
         }
-    } else if (warp == 9) {
+      } else if (warp == 9) {
         // ------------------------------- MMA issuer ---------------------------------
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(AT_BM, AT_BN, 0, 0);   // Q K^T: both K-major
-            constexpr uint32_t idesc_o = idesc_bf16_f32(AT_BM, DH, 0, 1);      // P V: V is MN-major
+            constexpr uint32_t idesc_o = idesc_f16_f32(AT_BM, DH, 0, 1);       // P V (f16): V is MN-major
             const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
             auto issue_s = [&](int i, int st) {
                 const uint32_t d = tmem + C::s_col(i);
@@ -195,41 +219,43 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 mma_commit(&s_full[0]);
                 issue_s(1, 0);
                 mma_commit(&s_full[1]);
+                mma_commit(&k_empty[0]);
             }
             for (int k = 0; ok && k < nkv; ++k) {
-                const int st = k % C::STAGES;
-                const uint32_t ph = (k / C::STAGES) & 1;
-                const int st2 = (k + 1) % C::STAGES;
-                const uint32_t ph2 = ((k + 1) / C::STAGES) & 1;
+                const int vst = k % C::VSTAGES;
+                const int kst2 = (k + 1) % C::KSTAGES;
                 const bool more = k + 1 < nkv;
                 // tile 0: O0 += P0 V(k), then S0(k+1)
                 ok = mbar_wait(&p_full[0], k & 1, p.status, kSiteAttnMmaP, abort_flag) &&
-                     mbar_wait(&v_full[st], ph, p.status, kSiteAttnMmaV, abort_flag);
+                     mbar_wait(&v_full[vst], (k / C::VSTAGES) & 1, p.status, kSiteAttnMmaV, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(0, st, k > 0);
+                issue_pv(0, vst, k > 0);
                 if (more) {
-                    ok = mbar_wait(&k_full[st2], ph2, p.status, kSiteAttnMmaK, abort_flag);
+                    ok = mbar_wait(&k_full[kst2], ((k + 1) / C::KSTAGES) & 1, p.status, kSiteAttnMmaK, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(0, st2);
+                    issue_s(0, kst2);
                     mma_commit(&s_full[0]);
                 }
-                // tile 1: O1 += P1 V(k), release stage k, then S1(k+1)
+                // tile 1: O1 += P1 V(k) (then V(k) is free), S1(k+1) (then K(k+1) is free)
                 ok = mbar_wait(&p_full[1], k & 1, p.status, kSiteAttnMmaP, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(1, st, k > 0);
-                mma_commit(&kv_empty[st]);
+                issue_pv(1, vst, k > 0);
+                mma_commit(&v_empty[vst]);
                 if (more) {
-                    issue_s(1, st2);
+                    issue_s(1, kst2);
                     mma_commit(&s_full[1]);
+                    mma_commit(&k_empty[kst2]);
                 }
             }
             mma_commit(o_full);
         }
+      }
     } else {
         // ------------------------------- softmax warps ------------------------------
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(AT_REGS_SOFTMAX));
         const int tile = warp >> 2;           // 0: rows [r0, r0+128), 1: [r0+128, r0+256)
         const int q = warp & 3;               // TMEM lane quarter
         const int row = q * 32 + lane;
@@ -258,17 +284,25 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             }
             tmem_ld_wait();
             // mask columns outside [lo, hi] (only when some row of the warp needs it)
-            const long long kr0 = (long long)(kv_begin + k) * AT_BN;
-            const bool need_mask = (kr0 < lo) || (kr0 + AT_BN - 1 > hi);
-            if (__any_sync(0xffffffffu, need_mask)) {
-                const long long a = lo - kr0, b = hi - kr0;
+            {
+                const long long kr0 = (long long)(kv_begin + k) * AT_BN;
+                const bool need_mask = (kr0 < lo) || (kr0 + AT_BN - 1 > hi);
+                if (__any_sync(0xffffffffu, need_mask)) {
+                    const long long a = lo - kr0, b = hi - kr0;
 #pragma unroll
-                for (int c = 0; c < AT_BN; ++c)
-                    if (c < a || c > b) s[c] = -INFINITY;
+                    for (int c = 0; c < AT_BN; ++c)
+                        if (c < a || c > b) s[c] = -INFINITY;
+                }
             }
-            float mt = s[0];
+            // row max: 8 independent chains of 3-input max, then a tree (max is exact)
+            float mx[8];
 #pragma unroll
-            for (int c = 1; c < AT_BN; ++c) mt = fmaxf(mt, s[c]);
+            for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+            for (int c = 8; c < AT_BN; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+            const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
             const float m_cand = mt * sl2;
             const bool raise = m_cand > m_run + AT_RESCALE_THRESHOLD;
             float factor = 1.f;
@@ -290,23 +324,43 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 }
             }
             const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-            float rs = 0.f;
+            // p = 2^(s * log2(e)/sqrt(d) - m): the exponent by a packed fp32x2 FMA, rounded to
+            // f16x2, then one ex2.f16x2 per pair.  P goes to TMEM as f16 (the PV product is f16).
+            uint32_t pk[AT_BN / 64][32];
 #pragma unroll
             for (int c = 0; c < AT_BN / 64; ++c) {
-                uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = fast_exp2(fmaf(s[c * 64 + 2 * i], sl2, -mu));
-                    const float p1 = fast_exp2(fmaf(s[c * 64 + 2 * i + 1], sl2, -mu));
-                    rs += p0 + p1;
-                    pk[i] = pack_bf16x2(p0, p1);
+                    float x0, x1;
+                    ffma2(x0, x1, s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1], sl2, sl2, -mu, -mu);
+                    pk[c][i] = ex2_f16x2(pack_f16x2(x0, x1));
                 }
-                tmem_st32(s_col + c * 32, pk);
+                tmem_st32(s_col + c * 32, pk[c]);
             }
-            l_run += rs;
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[tile]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[tile]);
+            // row sum off the critical path (the MMA warp already has P).  Each p <= 2^8
+            // (threshold rule), so an f16 partial over 16 values stays below 2^12.
+            uint32_t hs[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(pk[0][i], pk[0][i + 8]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(hs[i], hadd2_f16(pk[0][i + 16], pk[0][i + 24]));
+            float lsum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) lsum += f16x2_sum_to_f32(hs[i]);
+#pragma unroll
+            for (int c = 1; c < AT_BN / 64; ++c) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(pk[c][i], pk[c][i + 8]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(hs[i], hadd2_f16(pk[c][i + 16], pk[c][i + 24]));
+#pragma unroll
+                for (int i = 0; i < 8; ++i) lsum += f16x2_sum_to_f32(hs[i]);
+            }
+            l_run += lsum;
         }
         // ------------------------------- epilogue -----------------------------------
         if (ok && mbar_wait(o_full, 0, p.status, kSiteAttnEpilogue, abort_flag)) {
@@ -357,7 +411,8 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
         const uint64_t dims[3] = {(uint64_t)DH, (uint64_t)L, (uint64_t)BH};
         const uint64_t strides[2] = {(uint64_t)DH * 2, (uint64_t)L * DH * 2};
         const uint32_t box[3] = {64, AT_BM, 1};
-        if (!make_tmap_bf16(&tm[s], base + s * sstride, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_tmap_bf16(&tm[s], base + s * sstride, 3, dims, strides, box, /*f16=*/s == 2))
+            return cudaErrorInvalidValue;
     }
     AttnParams p;
     p.pbar = (__nv_bfloat16 *)Pbar;
@@ -372,6 +427,11 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     p.status = status;
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    // the register split above is only valid for exactly AT_LAUNCH_REGS registers per thread
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attn_fwd_tc<DH>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != AT_LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)BH, (unsigned)p.num_qblocks);
     attn_fwd_tc<DH><<<grid, AT_THREADS, C::SMEM, st>>>(tm[0], tm[1], tm[2], p);
     return cudaGetLastError();

@@ -28,15 +28,15 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
 // ---------------------------------------------------------------------------------------
-// fold: block = one s, FOLD_CB consecutive c, FOLD_KB consecutive k.  The W slab
-// W_s[k0..k0+KB)[m][c0..c0+CB) for all m is staged in shared memory as [m][cc][kk]
-// (so a warp's 32 consecutive k read consecutive words); alpha_s sits in shared memory
-// too.  Thread (group g, kk) produces, for its k, the output rows (h, j, c) of its
-// group; a row's KB values are written by KB consecutive threads (coalesced).
+// fold: block = one s, FOLD_K consecutive k (the 32 lanes of a warp) and FOLD_C
+// consecutive c.  The W slab W_s[k][m][c] of the block (all m) is staged in shared memory
+// as [m][c][k] (padded); each warp owns FOLD_PP output pseudo-head pairs (h, j) at a time
+// with their alpha_s[:, h, j] in registers, so one shared-memory read of W feeds FOLD_PP
+// FMAs, and each output row segment (32 consecutive k) is one coalesced 64/128-byte store.
 // ---------------------------------------------------------------------------------------
-constexpr int FOLD_KB = 128, FOLD_CB = 16, FOLD_THREADS = 256, FOLD_GROUPS = FOLD_THREADS / FOLD_KB;
+constexpr int FOLD_K = 32, FOLD_C = 32, FOLD_THREADS = 256, FOLD_WARPS = FOLD_THREADS / 32;
 
-template <typename T, int MAXH>
+template <typename T, int MAXH, int FOLD_PP>
 __global__ void __launch_bounds__(FOLD_THREADS)
 fold_kernel(const T *__restrict__ WQ, const T *__restrict__ WK, const T *__restrict__ WV,
             const float *__restrict__ aQ, const float *__restrict__ aK, const float *__restrict__ aV,
@@ -46,58 +46,70 @@ fold_kernel(const T *__restrict__ WQ, const T *__restrict__ WK, const T *__restr
     const T *W = s == 0 ? WQ : (s == 1 ? WK : WV);
     const float *alpha = s == 0 ? aQ : (s == 1 ? aK : aV);
     const long long D = (long long)H * d;
-    const int k0 = blockIdx.x * FOLD_KB, c0 = blockIdx.y * FOLD_CB;
-    float *Ws = fsm;                                          // [H][FOLD_CB][FOLD_KB]
-    float *as = fsm + (size_t)H * FOLD_CB * FOLD_KB;          // [H][H][P]
-    const int slab = FOLD_CB * FOLD_KB;
-    // load: consecutive threads take consecutive c of one (k, m) row segment
-    for (int idx = threadIdx.x; idx < H * slab; idx += blockDim.x) {
-        const int cc = idx % FOLD_CB, rest = idx / FOLD_CB, kk = rest % FOLD_KB, m = rest / FOLD_KB;
+    const int k0 = blockIdx.x * FOLD_K, c0 = blockIdx.y * FOLD_C;
+    constexpr int KP = FOLD_K + 1;                            // padded row (no bank conflicts)
+    float *Ws = fsm;                                          // [H][FOLD_C][KP]
+    float *as = fsm + (size_t)H * FOLD_C * KP;                // [H][H][P]
+    for (int idx = threadIdx.x; idx < H * FOLD_C * FOLD_K; idx += blockDim.x) {
+        const int cc = idx % FOLD_C, rest = idx / FOLD_C, kk = rest % FOLD_K, m = rest / FOLD_K;
         const long long k = k0 + kk;
         const int c = c0 + cc;
-        Ws[((size_t)m * FOLD_CB + cc) * FOLD_KB + kk] = (k < D && c < d) ? ld_f(W + k * D + (long long)m * d + c) : 0.f;
+        Ws[((size_t)m * FOLD_C + cc) * KP + kk] = (k < D && c < d) ? ld_f(W + k * D + (long long)m * d + c) : 0.f;
     }
     for (int idx = threadIdx.x; idx < H * H * P; idx += blockDim.x) as[idx] = alpha[idx];
     __syncthreads();
-    const int kk = threadIdx.x % FOLD_KB, g = threadIdx.x / FOLD_KB;
+    const int kk = threadIdx.x % 32, warp = threadIdx.x / 32;
     const long long k = k0 + kk;
-    if (k >= D) return;
-    const long long HPd = (long long)H * P * d, Pd = (long long)P * d;
-    const int ccmax = d - c0 < FOLD_CB ? d - c0 : FOLD_CB;
-    for (int cc = 0; cc < ccmax; ++cc) {
-        float w[MAXH];   // W_s[k][m][c0 + cc], m < H <= MAXH (registers: the loops are unrolled)
+    const int HP = H * P;
+    const int ccmax = d - c0 < FOLD_C ? d - c0 : FOLD_C;
+    for (int p0 = warp * FOLD_PP; p0 < HP; p0 += FOLD_WARPS * FOLD_PP) {
+        float a[FOLD_PP][MAXH];
 #pragma unroll
-        for (int m = 0; m < MAXH; ++m) w[m] = m < H ? Ws[((size_t)m * FOLD_CB + cc) * FOLD_KB + kk] : 0.f;
-        for (int pair = g; pair < H * P; pair += FOLD_GROUPS) {
-            const int h = pair / P, j = pair % P;
-            float acc = 0.f;
+        for (int q = 0; q < FOLD_PP; ++q)
 #pragma unroll
             for (int m = 0; m < MAXH; ++m)
-                if (m < H) acc = fmaf(as[((size_t)m * H + h) * P + j], w[m], acc);
-            Wt[(s * HPd + h * Pd + (long long)j * d + c0 + cc) * D + k] = from_f<T>(acc);
+                a[q][m] = (m < H && p0 + q < HP) ? as[(size_t)m * HP + p0 + q] : 0.f;   // alpha[m][h][j], pair = h*P + j
+        for (int cc = 0; cc < ccmax; ++cc) {
+            float acc[FOLD_PP] = {};
+#pragma unroll
+            for (int m = 0; m < MAXH; ++m) {
+                if (m < H) {
+                    const float wv = Ws[((size_t)m * FOLD_C + cc) * KP + kk];
+#pragma unroll
+                    for (int q = 0; q < FOLD_PP; ++q) acc[q] = fmaf(a[q][m], wv, acc[q]);
+                }
+            }
+            if (k < D) {
+#pragma unroll
+                for (int q = 0; q < FOLD_PP; ++q)
+                    if (p0 + q < HP)   // row (s, h, j, c) = s*H*P*d + (h*P + j)*d + c
+                        Wt[((long long)s * HP * d + (long long)(p0 + q) * d + c0 + cc) * D + k] = from_f<T>(acc[q]);
+            }
         }
     }
 }
 
-template <typename T, int MAXH>
+template <typename T, int MAXH, int PP>
 static cudaError_t launch_fold_t(const void *WQ, const void *WK, const void *WV, const float *aQ, const float *aK,
                                  const float *aV, const Shape &sh, void *Wt, cudaStream_t st) {
     const long long D = sh.D();
-    dim3 grid((unsigned)((D + FOLD_KB - 1) / FOLD_KB), (unsigned)((sh.d + FOLD_CB - 1) / FOLD_CB), 3);
-    const size_t smem = sizeof(float) * ((size_t)sh.H * FOLD_CB * FOLD_KB + (size_t)sh.H * sh.H * sh.P);
-    cudaError_t e = cudaFuncSetAttribute(fold_kernel<T, MAXH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    dim3 grid((unsigned)((D + FOLD_K - 1) / FOLD_K), (unsigned)((sh.d + FOLD_C - 1) / FOLD_C), 3);
+    const size_t smem = sizeof(float) * ((size_t)sh.H * FOLD_C * (FOLD_K + 1) + (size_t)sh.H * sh.H * sh.P);
+    cudaError_t e =
+        cudaFuncSetAttribute(fold_kernel<T, MAXH, PP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    fold_kernel<T, MAXH><<<grid, FOLD_THREADS, smem, st>>>((const T *)WQ, (const T *)WK, (const T *)WV, aQ, aK, aV,
-                                                           (T *)Wt, sh.H, sh.d, sh.P);
+    fold_kernel<T, MAXH, PP><<<grid, FOLD_THREADS, smem, st>>>((const T *)WQ, (const T *)WK, (const T *)WV, aQ, aK,
+                                                               aV, (T *)Wt, sh.H, sh.d, sh.P);
     return cudaGetLastError();
 }
 
 template <typename T>
 static cudaError_t launch_fold_h(const void *WQ, const void *WK, const void *WV, const float *aQ, const float *aK,
                                  const float *aV, const Shape &sh, void *Wt, cudaStream_t st) {
-    if (sh.H <= 16) return launch_fold_t<T, 16>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
-    if (sh.H <= 32) return launch_fold_t<T, 32>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
-    if (sh.H <= 64) return launch_fold_t<T, 64>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
+    if (sh.H <= 8) return launch_fold_t<T, 8, 4>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
+    if (sh.H <= 16) return launch_fold_t<T, 16, 4>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
+    if (sh.H <= 32) return launch_fold_t<T, 32, 2>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
+    if (sh.H <= 64) return launch_fold_t<T, 64, 1>(WQ, WK, WV, aQ, aK, aV, sh, Wt, st);
     return cudaErrorInvalidValue;
 }
 

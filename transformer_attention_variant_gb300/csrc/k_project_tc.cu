@@ -9,7 +9,8 @@
 // Design (sm_103a): persistent CTAs, one per SM; warp 0 = TMA producer (128B-swizzled
 // A and B tiles, 4-stage ring), warp 1 = MMA issuer (tcgen05.mma kind::f16, M=128 N=256
 // K=16, fp32 accumulators in TMEM, double-buffered so the epilogue of one tile overlaps
-// the main loop of the next), warps 2-5 = epilogue (tcgen05.ld -> bf16 -> global).
+// the main loop of the next), warps 2-5 = epilogue (tcgen05.ld -> bf16 -> global; the
+// Vbar third is written as f16, the type the attention kernel's P V product uses).
 #include <cuda_bf16.h>
 
 #include "iha_internal.h"
@@ -154,9 +155,15 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     __nv_bfloat16 *dst = p.qkv + s * p.s_stride + ((b * p.H + h) * p.N_tok + t) * Pd + jc;
                     uint4 v[4];
                     uint32_t *vw = reinterpret_cast<uint32_t *>(v);
+                    if (s == 2) {   // Vbar is stored as f16 (the P V product runs in f16)
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        vw[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                        for (int i = 0; i < 16; ++i)
+                            vw[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            vw[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    }
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) d4[i] = v[i];

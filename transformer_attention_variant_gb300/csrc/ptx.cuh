@@ -63,20 +63,55 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait until the barrier's phase with the given parity has completed.  Returns false
-// (after recording `site`) if that takes longer than kWaitLimitNs, or immediately if
-// another thread of the CTA already gave up (*abort set).
+// One potentially blocking probe: the thread may be suspended (without using issue slots)
+// until the phase completes or about `hint_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the barrier's phase with the given parity has completed.  The waiting warp
+// sleeps inside try_wait (it does not spin on issue slots that the warps sharing its
+// scheduler need).  Returns false (after recording `site`) if that takes longer than
+// limit_ns, or as soon as another thread of the CTA gave up (*abort set).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status, int site,
                                           volatile int *abort, uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            record_timeout(status, site);
+            if (abort) *abort = 1;
+            return false;
+        }
+    }
+}
+
+// The same for a waiter whose latency does not matter (a producer running ahead): after a
+// few polls it sleeps between polls so that it leaves issue slots to the warps it shares
+// a scheduler with.
+__device__ __forceinline__ bool mbar_wait_lazy(uint64_t *bar, uint32_t parity, int *status, int site,
+                                               volatile int *abort) {
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (true) {
+        __nanosleep(64);
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
             record_timeout(status, site);
             if (abort) *abort = 1;
             return false;
@@ -168,6 +203,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
     return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
            (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
+// The same with f16 A and B (format code 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) |
+           (uint32_t(M >> 4) << 24);
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle:
 //   [0,14) start >> 4, [16,30) leading-dimension byte offset >> 4,
@@ -222,6 +262,51 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);   // .x = lo (low half), .y = hi
     return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;   // cvt places its first source in the upper half
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// 2^x for both halves of an f16x2 (one MUFU operation for two values)
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+    uint32_t r;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+__device__ __forceinline__ uint32_t hadd2_f16(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ float f16x2_sum_to_f32(uint32_t x) {
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(x));
+    return lo + hi;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Packed two-wide fp32 arithmetic (sm_100+): d = a * b + c and d = a + b, lane-wise.
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+    uint64_t A, B, Cc, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(Cc) : "f"(c0), "f"(c1));
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(R) : "l"(A), "l"(B), "l"(Cc));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(R));
+}
+__device__ __forceinline__ void fadd2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    uint64_t A, B, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(R) : "l"(A), "l"(B));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(R));
 }
 
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }

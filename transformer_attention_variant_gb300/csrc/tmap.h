@@ -28,10 +28,11 @@ inline EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// A rank-`rank` bf16 tensor map: dims[0] is the contiguous dimension; strides_bytes[i]
-// is the byte stride of dimension i+1.  Out-of-bounds elements of a load read as zero.
+// A rank-`rank` 16-bit tensor map (bf16, or f16 when f16 is true): dims[0] is the
+// contiguous dimension; strides_bytes[i] is the byte stride of dimension i+1.
+// Out-of-bounds elements of a load read as zero.
 inline bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                           const uint64_t *strides_bytes, const uint32_t *box) {
+                           const uint64_t *strides_bytes, const uint32_t *box, bool f16 = false) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     cuuint64_t gdim[5], gstride[4];
@@ -42,7 +43,7 @@ inline bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const u
         estride[i] = 1;
         if (i + 1 < rank) gstride[i] = strides_bytes[i];
     }
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), gdim,
+    CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), gdim,
                     gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
