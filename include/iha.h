@@ -137,6 +137,33 @@ IHA_API size_t iha_host_buffer_bytes(int B, int N, int H, int d, int P, int dtyp
  */
 IHA_API int iha_selftest_wait_timeout(void *stream, int limit_ms);
 
+/*
+ * iha_forward_noalloc -- iha_forward_ex for callers that cannot allocate device
+ * memory: processes whose device memory is already reserved in full by another
+ * framework's pool, or code paths where an allocation may not happen (it could
+ * fail, block, or synchronise).  The pass's workspace is a fixed array of
+ * IHA_NOALLOC_SCRATCH_BYTES compiled into the library (every GPU that loads
+ * the library holds one until exit); the call itself allocates nothing.  The
+ * method has no counterpart to this entry point: it is about where the
+ * workspace lives.
+ *   - Arguments, layouts and dtypes as iha_forward_ex (device pointers, the
+ *     caller's stream); same kernels, so the same results.
+ *   - Problems with iha_workspace_bytes(...) > IHA_NOALLOC_SCRATCH_BYTES are
+ *     refused with IHA_ERR_WORKSPACE before anything runs.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.  A failed lookup returns IHA_ERR_CUDA.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind.  No part of it needs to start at zero (each step overwrites what
+ *     the next reads), but calls that overlap on the GPU (other streams, other
+ *     threads) race on it: serialise them.
+ */
+#define IHA_NOALLOC_SCRATCH_BYTES (64u << 20)
+IHA_API int iha_forward_noalloc(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                                const float *alpha_Q, const float *alpha_K, const float *alpha_V,
+                                const float *R, int B, int N, int H, int d, int P,
+                                int mask_mode, int window, void *out, int dtype, void *stream);
+
 /* ---------------------------------------------------------------------------
  * The four steps as separate entry points (same validation, same kernels as
  * iha_forward_ex; asynchronous on the stream).  Intermediate layouts:

@@ -32,7 +32,9 @@ IHA_MASK_WINDOW = 2
 EXPORTED = ("iha_forward", "iha_forward_ex", "iha_workspace_bytes", "iha_error_string",
             "iha_check_device_status", "iha_forward_host", "iha_host_buffer_bytes",
             "iha_selftest_wait_timeout", "iha_fold_weights", "iha_project", "iha_attention",
-            "iha_contract")
+            "iha_contract", "iha_forward_noalloc")
+
+IHA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class IHAError(RuntimeError):
@@ -73,6 +75,8 @@ def _load():
     lib.iha_attention.restype = i
     lib.iha_contract.argtypes = [vp, fp] + shape + [i, vp, vp]
     lib.iha_contract.restype = i
+    lib.iha_forward_noalloc.argtypes = [vp] * 4 + [fp] * 4 + shape + [i, i, vp, i, vp]
+    lib.iha_forward_noalloc.restype = i
     return lib
 
 
@@ -153,6 +157,14 @@ def iha_attention(QKV, B, N, H, d, P, mask_mode, window, dtype, Pbar, stream=Non
 
 def iha_contract(Pbar, R, B, N, H, d, P, dtype, out, stream=None) -> int:
     return _lib.iha_contract(_p(Pbar), _p(R), B, N, H, d, P, dtype, _p(out), _s(stream))
+
+
+def iha_forward_noalloc(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, out,
+                        dtype, stream=None) -> int:
+    """The forward pass with its workspace in the library's fixed scratch array (no
+    allocation).  For callers that cannot allocate device memory."""
+    return _lib.iha_forward_noalloc(_p(X), _p(W_Q), _p(W_K), _p(W_V), _p(alpha_Q), _p(alpha_K), _p(alpha_V),
+                                    _p(R), B, N, H, d, P, mask_mode, window, _p(out), dtype, _s(stream))
 
 
 def check(status: int, what: str = "") -> None:

@@ -115,6 +115,26 @@ static int run_forward(const void *X, const void *WQ, const void *WK, const void
     return cuda_status(e);
 }
 
+// Entry points outside this file reuse the checks and the launch sequence of
+// iha_forward_ex through these two functions.
+int check_forward_args(const void *X, const void *WQ, const void *WK, const void *WV, const float *aQ,
+                       const float *aK, const float *aV, const float *R, int B, int N, int H, int d, int P,
+                       int mask_mode, int window, const void *out, int dtype) {
+    if (!X || !WQ || !WK || !WV || !aQ || !aK || !aV || !R || !out) return IHA_ERR_INVALID_ARG;
+    int rc = validate_shape(B, N, H, d, P, dtype);
+    if (rc == IHA_OK) rc = validate_mask(mask_mode, window);
+    return rc;
+}
+
+int forward_in_workspace(const void *X, const void *WQ, const void *WK, const void *WV, const float *aQ,
+                         const float *aK, const float *aV, const float *R, const Shape &sh, int mask_mode,
+                         int window, void *out, int dtype, cudaStream_t st, void *workspace,
+                         size_t workspace_bytes) {
+    if (!workspace) return IHA_ERR_WORKSPACE;
+    return run_forward(X, WQ, WK, WV, aQ, aK, aV, R, sh, mask_mode, window, out, dtype, st, workspace,
+                       workspace_bytes);
+}
+
 }  // namespace iha
 
 using namespace iha;

@@ -51,6 +51,18 @@ cudaError_t launch_contract(const void *Pbar, const float *R, const Shape &sh, i
 // record kSiteSelfTest in the status word (exercises the failure path of every wait).
 cudaError_t launch_wait_selftest(int *status, unsigned long long limit_ns, cudaStream_t st);
 
+// The argument checks of iha_forward_ex (IHA_OK or the status it would return).
+int check_forward_args(const void *X, const void *WQ, const void *WK, const void *WV, const float *aQ,
+                       const float *aK, const float *aV, const float *R, int B, int N, int H, int d, int P,
+                       int mask_mode, int window, const void *out, int dtype);
+
+// The launch sequence of iha_forward_ex in a caller-given device workspace (never NULL;
+// nothing is allocated).
+int forward_in_workspace(const void *X, const void *WQ, const void *WK, const void *WV, const float *aQ,
+                         const float *aK, const float *aV, const float *R, const Shape &sh, int mask_mode,
+                         int window, void *out, int dtype, cudaStream_t st, void *workspace,
+                         size_t workspace_bytes);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
