@@ -59,9 +59,11 @@ static int validate_shape(int B, int N, int H, int d, int P, int dtype) {
     if (dtype != IHA_DTYPE_F32 && dtype != IHA_DTYPE_BF16) return IHA_ERR_INVALID_ARG;
     const long long L = (long long)N * P, D = (long long)H * d;
     // index ranges the kernels use: int for rows/columns, grid dims < 2^31 / 65536
-    if (L > 65535LL * 256 || D > (1LL << 20) || (long long)B * N > INT_MAX / 2 || (long long)B * H > INT_MAX / 2 ||
+    if (L > (1LL << 24) || D > (1LL << 20) || (long long)B * N > INT_MAX / 2 || (long long)B * H > INT_MAX / 2 ||
         3LL * H * P * d > INT_MAX / 2)
         return IHA_ERR_UNSUPPORTED;
+    // attention grids: one CTA per (b, h, 256 stacked rows) (bf16), one warp per row (fp32)
+    if ((long long)B * H * ((L + 255) / 256) > INT_MAX || (long long)B * H * L > (1LL << 34)) return IHA_ERR_UNSUPPORTED;
     if (dtype == IHA_DTYPE_BF16 && d != 64 && d != 128) return IHA_ERR_UNSUPPORTED;
     if (H > 64) return IHA_ERR_UNSUPPORTED;   // the weight fold keeps one W column per head in registers
     if (dtype == IHA_DTYPE_F32 && d > 256) return IHA_ERR_UNSUPPORTED;

@@ -61,6 +61,8 @@ struct AttnParams {
     int mask_mode, window;
     float scale_log2;      // log2(e) / sqrt(d)
     int num_qblocks;
+    int num_heads;         // B * H
+    int head_group;        // heads per scheduling group
     int *status;
 };
 
@@ -108,8 +110,20 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = warp_id(), lane = lane_id();
-    const int bh = blockIdx.x;
-    const int qb = p.num_qblocks - 1 - (int)blockIdx.y;   // heavy (late) blocks first
+    // Work order: heads in groups of p.head_group (chosen so a group's K and V fit in L2);
+    // within a group, query blocks heaviest (latest) first across the group's heads.  The
+    // CTAs resident at one time then share one group's K/V in L2, and the light blocks of
+    // each group fill the tail of its wave.
+    int bh, qb;
+    {
+        const long long i = blockIdx.x;
+        const long long per_group = (long long)p.head_group * p.num_qblocks;
+        const int g = (int)(i / per_group);
+        const int j = (int)(i % per_group);
+        const int g_heads = min(p.head_group, p.num_heads - g * p.head_group);
+        bh = g * p.head_group + j % g_heads;
+        qb = p.num_qblocks - 1 - j / g_heads;
+    }
     const long long r0 = (long long)qb * 2 * AT_BM;
 
     // KV tiles this CTA needs: union of the readable intervals of its rows
@@ -432,7 +446,13 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     e = cudaFuncGetAttributes(&fa, attn_fwd_tc<DH>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != AT_LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-    dim3 grid((unsigned)BH, (unsigned)p.num_qblocks);
+    p.num_heads = (int)BH;
+    {
+        const long long kv_bytes_per_head = 2LL * L * DH * 2;   // K and V of one (b, h)
+        long long g = (48LL << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
+        p.head_group = (int)(g < 1 ? 1 : (g > BH ? BH : g));
+    }
+    const unsigned grid = (unsigned)(BH * p.num_qblocks);
     attn_fwd_tc<DH><<<grid, AT_THREADS, C::SMEM, st>>>(tm[0], tm[1], tm[2], p);
     return cudaGetLastError();
 }
