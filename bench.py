@@ -193,6 +193,12 @@ def max_over_ranks(x: float, dist, device):
     return float(t.item())
 
 
+def job_value(world: int, pseudo_tokens_per_rank: int, step_ms: float) -> float:
+    """Whole-job throughput: every rank processes its own replica of the workload, so the
+    job handles world x pseudo_tokens_per_rank per step of step_ms (max over ranks)."""
+    return world * pseudo_tokens_per_rank / (step_ms * 1e-3)
+
+
 def barrier(dist):
     if dist is not None:
         dist.barrier()
@@ -315,7 +321,7 @@ def run_gpu(args, w):
     mean_step = sum(step_ms) / len(step_ms)
     mean_step = max_over_ranks(mean_step, dist, dev)
     kmean = {n: sum(v) / len(v) for n, v in k_ms.items()}
-    value = world * wk["pseudo_tokens"] / (mean_step * 1e-3)
+    value = job_value(world, wk["pseudo_tokens"], mean_step)
 
     # roofline of the dominant kernel
     dom = max(kmean, key=kmean.get)
@@ -386,7 +392,7 @@ def run_gpu(args, w):
             e2e_call()
             t.append(time.perf_counter() - t0)
         e2e_s = max_over_ranks(sum(t) / len(t), dist, dev)
-        line["e2e"] = {"value": world * wk["pseudo_tokens"] / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        line["e2e"] = {"value": job_value(world, wk["pseudo_tokens"], e2e_s * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
                        "call": "iha_forward_host (pinned host buffers, preallocated device buffer)"}
 
@@ -404,14 +410,23 @@ def run_gpu(args, w):
 
 
 def traffic_per_launch(workload, kernel):
-    """DRAM bytes (read + write) per launch from the committed ncu summary, if one
-    matches this workload and kernel; None otherwise."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes (read + write) per launch recorded from ncu in profiles/dram_traffic.txt,
+    provided the kernel's source is unchanged since that capture; None otherwise."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    with open(p) as f:
-        t = json.load(f)
-    return t.get(workload, {}).get(kernel)
+    for line in open(p):
+        f = line.split()
+        if len(f) < 6 or f[0].startswith("#") or f[0] != workload or f[1] != kernel:
+            continue
+        src = os.path.join(ROOT, "transformer_attention_variant_gb300", "csrc", f[2])
+        if not os.path.exists(src):
+            return None
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != f[3]:
+            return None
+        return int(f[4]) + int(f[5])
+    return None
 
 
 def main():
@@ -422,7 +437,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=gi.WORKLOAD_ORDER)
     ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
-    ap.add_argument("--ref-tokens", type=int, default=16, help="oracle sample size per reference-arm step")
+    ap.add_argument("--ref-tokens", type=int, default=48, help="oracle sample size per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
     ap.add_argument("--N", type=int, default=None,
