@@ -3,8 +3,9 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-fold (alpha into W) -> projection GEMM into the stacked layout -> attention over
-the stacked sequence -> R contraction, launched through the library's step
+projection + pseudo-head mixing into the stacked layout (the library's route for the
+shape: project all heads then mix, or fold alpha into W then project) -> attention
+over the stacked sequence -> R contraction, launched through the library's step
 entry points on one stream, each kernel bracketed by CUDA events on that stream.
 L2 is flushed (256 MiB write) between steps, outside the timed events.
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
@@ -78,9 +79,11 @@ def work(w):
     es = 2
     bytes_contract = es * (B * N * H * P * d + B * N * D)
     bytes_fold = es * (3 * D * D + 3 * H * P * d * D)
-    return dict(pairs=pairs, attn=attn, proj_folded=proj_folded, algorithmic=proj_heads + mixing + attn + contract,
-                executed=proj_folded + attn + contract, bytes_contract=bytes_contract, bytes_fold=bytes_fold,
-                pseudo_tokens=B * P * N)
+    bytes_mix = es * (B * N * 3 * D + 3 * B * H * N * P * d)   # read Y, write Qbar/Kbar/Vbar
+    return dict(pairs=pairs, attn=attn, proj_folded=proj_folded, proj_heads=proj_heads,
+                algorithmic=proj_heads + mixing + attn + contract,
+                executed_folded=proj_folded + attn + contract, executed_unfolded=proj_heads + mixing + attn + contract,
+                bytes_contract=bytes_contract, bytes_fold=bytes_fold, bytes_mix=bytes_mix, pseudo_tokens=B * P * N)
 
 
 # ---------------------------------------------------------------------------
@@ -263,7 +266,12 @@ def run_gpu(args, w):
 
     host = gi.make_inputs(w)
     d = {k: v.to(dev).contiguous() for k, v in host.items()}
-    Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=tdt, device=dev)
+    # steps 1+2 take the same route as iha_forward_ex: fold + project, or project heads + mix
+    route = iha.iha_projection_route(w.H, w.d, w.P, dt)
+    if route == 1:
+        Wt = torch.empty(w.B * w.N, 3 * w.D, dtype=tdt, device=dev)        # head projections Y
+    else:
+        Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=tdt, device=dev)  # folded weights
     QKV = torch.empty(3, w.B, w.H, w.N * w.P, w.d, dtype=tdt, device=dev)
     Pbar = torch.empty(w.B, w.N, w.H, w.P, w.d, dtype=tdt, device=dev)
     out = torch.empty(w.B, w.N, w.D, dtype=tdt, device=dev)
@@ -274,11 +282,19 @@ def run_gpu(args, w):
         s = stream
         if ev is not None:
             ev[0].record(s)
-        iha.check(iha.iha_fold_weights(d["W_Q"], d["W_K"], d["W_V"], d["alpha_Q"], d["alpha_K"], d["alpha_V"],
-                                       w.H, w.d, w.P, dt, Wt, s), "fold")
+        if route == 1:
+            iha.check(iha.iha_project_heads(d["X"], d["W_Q"], d["W_K"], d["W_V"], w.B, w.N, w.H, w.d, dt, Wt, s),
+                      "project_heads")
+        else:
+            iha.check(iha.iha_fold_weights(d["W_Q"], d["W_K"], d["W_V"], d["alpha_Q"], d["alpha_K"], d["alpha_V"],
+                                           w.H, w.d, w.P, dt, Wt, s), "fold")
         if ev is not None:
             ev[1].record(s)
-        iha.check(iha.iha_project(d["X"], Wt, w.B, w.N, w.H, w.d, w.P, dt, QKV, s), "project")
+        if route == 1:
+            iha.check(iha.iha_mix_heads(Wt, d["alpha_Q"], d["alpha_K"], d["alpha_V"], w.B, w.N, w.H, w.d, w.P, dt,
+                                        QKV, s), "mix")
+        else:
+            iha.check(iha.iha_project(d["X"], Wt, w.B, w.N, w.H, w.d, w.P, dt, QKV, s), "project")
         if ev is not None:
             ev[2].record(s)
         iha.check(iha.iha_attention(QKV, w.B, w.N, w.H, w.d, w.P, w.mask_mode, w.window, dt, Pbar, s), "attention")
@@ -311,7 +327,8 @@ def run_gpu(args, w):
     rc, code = iha.iha_check_device_status(stream)
     iha.check(rc, f"device status after timed steps ({code:#x})")
 
-    names = ["fold", "project", "attention", "contract"]
+    names = ["project_heads", "mix", "attention", "contract"] if route == 1 else ["fold", "project", "attention",
+                                                                                 "contract"]
     k_ms = {n: [] for n in names}
     step_ms = []
     for ev in events:
@@ -333,14 +350,14 @@ def run_gpu(args, w):
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
                 else "fallback 1.9 PFLOP/s"}
         traffic_key = "attention"
-    elif dom == "project":
-        ach = wk["proj_folded"] / (kmean[dom] * 1e-3) / 1e12
+    elif dom in ("project", "project_heads"):
+        ach = (wk["proj_folded"] if dom == "project" else wk["proj_heads"]) / (kmean[dom] * 1e-3) / 1e12
         roof = {"kernel": "proj_gemm_tc", "bound": "tensor", "achieved": ach, "peak": peaks["bf16"],
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16"],
                 "frac_of_sustained": ach / peaks["bf16_sustained"], "peak_source": peaks["source"]}
         traffic_key = "project"
     else:
-        b = wk["bytes_contract"] if dom == "contract" else wk["bytes_fold"]
+        b = {"contract": wk["bytes_contract"], "fold": wk["bytes_fold"], "mix": wk["bytes_mix"]}[dom]
         ach = b / (kmean[dom] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": ach / peaks["hbm"], "peak_source": peaks["source"]}
@@ -355,10 +372,13 @@ def run_gpu(args, w):
         "tflops": {
             "attention_exact_pairs": wk["attn"] / (kmean["attention"] * 1e-3) / 1e12,
             "forward_algorithmic": wk["algorithmic"] / (mean_step * 1e-3) / 1e12,
-            "forward_executed_folded": wk["executed"] / (mean_step * 1e-3) / 1e12,
-            "projection_executed": wk["proj_folded"] / (kmean["project"] * 1e-3) / 1e12,
+            "forward_executed": (wk["executed_unfolded"] if route == 1 else wk["executed_folded"])
+            / (mean_step * 1e-3) / 1e12,
+            "projection_gemm": (wk["proj_heads"] / (kmean["project_heads"] * 1e-3) if route == 1
+                                else wk["proj_folded"] / (kmean["project"] * 1e-3)) / 1e12,
         },
         "kernel_ms": kmean,
+        "projection_route": "project heads + mix" if route == 1 else "fold alpha into W + project",
         "roofline": roof,
         "gpu_launches": 4 * args.steps,
         "wall_s_timed_region": t_wall,

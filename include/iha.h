@@ -94,8 +94,9 @@ IHA_API int iha_forward_ex(const void *X, const void *W_Q, const void *W_K, cons
                    int mask_mode, int window, void *out,
                    int dtype, void *stream, void *workspace, size_t workspace_bytes);
 
-/* Bytes of device workspace one call needs (0 if the sizes are invalid):
- * folded weights + stacked Qbar, Kbar, Vbar + Pbar, each 256-byte aligned. */
+/* Bytes of device workspace one call needs (0 if the sizes are invalid): the folded
+ * weights (or, on the unfolded route, the head projections Y) + stacked Qbar, Kbar, Vbar
+ * + Pbar, each 256-byte aligned. */
 IHA_API size_t iha_workspace_bytes(int B, int N, int H, int d, int P, int dtype);
 
 /* A static, human-readable name for a status code (never NULL). */
@@ -189,6 +190,24 @@ IHA_API int iha_fold_weights(const void *W_Q, const void *W_K, const void *W_V,
  * layout.  QKV points to 3 consecutive arrays of B*H*N*P*d elements. */
 IHA_API int iha_project(const void *X, const void *Wt, int B, int N, int H, int d, int P,
                 int dtype, void *QKV, void *stream);
+
+/* Which way steps 1+2 run for this shape (what iha_forward_ex does):
+ *   1 = unfolded: iha_project_heads then iha_mix_heads (bf16 with P >= 2 and H <= 16 --
+ *       the projection GEMM then does 1/P of the folded GEMM's work);
+ *   0 = folded:   iha_fold_weights then iha_project;
+ *  -1 = invalid sizes or dtype. */
+IHA_API int iha_projection_route(int H, int d, int P, int dtype);
+
+/* Steps 1+2, first half, without the fold (bf16 only): the per-head projections of all
+ * heads, Y = X [W_Q | W_K | W_V], Y [B*N][3][H*d] bfloat16 row-major (block s, column
+ * m*d + c holds (X W_s^(m))[t][c]).  The weights are read as stored. */
+IHA_API int iha_project_heads(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                              int B, int N, int H, int d, int dtype, void *Y, void *stream);
+
+/* Steps 1+2, second half, and the stacking (bf16 only, H <= 16): the pseudo-head mixing
+ * S~_{h,j} = sum_m alpha_s[m,h,j] (X W_s^(m)) of Y into QKV (layout as for iha_project). */
+IHA_API int iha_mix_heads(const void *Y, const float *alpha_Q, const float *alpha_K, const float *alpha_V,
+                          int B, int N, int H, int d, int P, int dtype, void *QKV, void *stream);
 
 /* Step 3: masked softmax attention over each head's stacked sequence.
  * QKV as written by iha_project; Pbar [B][N][H][P][d]. */

@@ -51,7 +51,9 @@ def test_workspace_bytes(iha):
     D = H * d
     al = lambda x: (x + 255) // 256 * 256
     for dtype, es in ((iha.IHA_DTYPE_BF16, 2), (iha.IHA_DTYPE_F32, 4)):
-        expect = al(3 * H * P * d * D * es) + al(3 * B * H * N * P * d * es) + al(B * N * H * P * d * es)
+        # first region: head projections Y on the unfolded route, folded weights otherwise
+        first = 3 * B * N * D * es if iha.iha_projection_route(H, d, P, dtype) == 1 else 3 * H * P * d * D * es
+        expect = al(first) + al(3 * B * H * N * P * d * es) + al(B * N * H * P * d * es)
         assert iha.iha_workspace_bytes(B, N, H, d, P, dtype) == expect
     assert iha.iha_workspace_bytes(0, N, H, d, P, 1) == 0
     assert iha.iha_workspace_bytes(B, N, H, 96, P, 1) == 0       # bf16 needs d in {64, 128}
@@ -84,7 +86,20 @@ def test_forward_rejects_bad_arguments(iha, kw, status):
     assert fwd(iha, **kw) == status
 
 
+def test_projection_route(iha):
+    assert iha.iha_projection_route(16, 128, 4, iha.IHA_DTYPE_BF16) == 1
+    assert iha.iha_projection_route(16, 64, 2, iha.IHA_DTYPE_BF16) == 1
+    assert iha.iha_projection_route(16, 128, 1, iha.IHA_DTYPE_BF16) == 0
+    assert iha.iha_projection_route(32, 64, 2, iha.IHA_DTYPE_BF16) == 0
+    assert iha.iha_projection_route(4, 32, 2, iha.IHA_DTYPE_F32) == 0
+    assert iha.iha_projection_route(4, 96, 2, iha.IHA_DTYPE_BF16) == -1
+
+
 def test_step_entry_points_reject_bad_arguments(iha):
+    assert iha.iha_project_heads(FAKE, None, FAKE, FAKE, 1, 8, 2, 64, 1, FAKE) == 1
+    assert iha.iha_project_heads(FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 64, 0, FAKE) == 2
+    assert iha.iha_mix_heads(FAKE, FAKE, FAKE, FAKE, 1, 8, 32, 64, 2, 1, FAKE) == 2
+    assert iha.iha_mix_heads(FAKE, FAKE, FAKE, None, 1, 8, 2, 64, 2, 1, FAKE) == 1
     assert iha.iha_fold_weights(None, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 64, 2, 1, FAKE) == 1
     assert iha.iha_project(FAKE, FAKE, 1, 8, 2, 64, 0, 1, FAKE) == 1
     assert iha.iha_attention(FAKE, 1, 8, 2, 64, 2, 2, 0, 1, FAKE) == 1

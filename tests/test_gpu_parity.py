@@ -205,30 +205,53 @@ def test_repeated_tokens_gpu(iha):
 # the other entry points give the same bits as iha_forward_ex
 # ---------------------------------------------------------------------------
 
-def test_step_entry_points_match_forward(iha):
-    w = W("steps", B=2, N=260, H=4, d=64, P=2, mask_mode=WN, window=40, dtype="bf16", seed=43)
+@pytest.mark.parametrize("P", [1, 2, 3])
+def test_step_entry_points_match_forward(iha, P):
+    """Both ways of computing steps 1+2 (fold alpha into W, or project the heads and mix)
+    match the oracle; the route iha_forward_ex takes gives its bits exactly."""
+    w = W("steps", B=2, N=260, H=4, d=64, P=P, mask_mode=WN, window=40, dtype="bf16", seed=43)
     inp = gi.make_inputs(w)
     dinp = to_dev(inp)
     ref = run_gpu(iha, w, dinp=dinp)
     dt = iha.IHA_DTYPE_BF16
-    Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=torch.bfloat16, device="cuda:0")
-    QKV = torch.empty(3, w.B, w.H, w.N * w.P, w.d, dtype=torch.bfloat16, device="cuda:0")
-    Pbar = torch.empty(w.B, w.N, w.H, w.P, w.d, dtype=torch.bfloat16, device="cuda:0")
-    out = torch.empty_like(ref)
+    route = iha.iha_projection_route(w.H, w.d, w.P, dt)
+    assert route == (1 if P >= 2 else 0)
     s = torch.cuda.current_stream()
-    iha.check(iha.iha_fold_weights(dinp["W_Q"], dinp["W_K"], dinp["W_V"], dinp["alpha_Q"], dinp["alpha_K"],
-                                   dinp["alpha_V"], w.H, w.d, w.P, dt, Wt, s))
-    iha.check(iha.iha_project(dinp["X"], Wt, w.B, w.N, w.H, w.d, w.P, dt, QKV, s))
-    iha.check(iha.iha_attention(QKV, w.B, w.N, w.H, w.d, w.P, w.mask_mode, w.window, dt, Pbar, s))
-    iha.check(iha.iha_contract(Pbar, dinp["R"], w.B, w.N, w.H, w.d, w.P, dt, out, s))
-    torch.cuda.synchronize()
-    assert torch.equal(out, ref)
-    # the folded weights are the mixing sum (checked in float64 on a slice)
-    f = gi.as_f64(inp)
-    h, j, c = 1, 1, 5
-    col = sum(f["alpha_K"][m, h, j] * f["W_K"][:, m * w.d + c] for m in range(w.H))
-    row = Wt[1 * w.H * w.P * w.d + h * w.P * w.d + j * w.d + c].double().cpu().numpy()
-    np.testing.assert_allclose(row, col, rtol=1e-2, atol=1e-2 * np.abs(col).max())
+    ora = oracle_rows(w, inp)
+    for r in (0, 1):
+        QKV = torch.empty(3, w.B, w.H, w.N * w.P, w.d, dtype=torch.bfloat16, device="cuda:0")
+        Pbar = torch.empty(w.B, w.N, w.H, w.P, w.d, dtype=torch.bfloat16, device="cuda:0")
+        out = torch.empty_like(ref)
+        if r == 0:
+            Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=torch.bfloat16, device="cuda:0")
+            iha.check(iha.iha_fold_weights(dinp["W_Q"], dinp["W_K"], dinp["W_V"], dinp["alpha_Q"],
+                                           dinp["alpha_K"], dinp["alpha_V"], w.H, w.d, w.P, dt, Wt, s))
+            iha.check(iha.iha_project(dinp["X"], Wt, w.B, w.N, w.H, w.d, w.P, dt, QKV, s))
+        else:
+            Y = torch.empty(w.B * w.N, 3 * w.D, dtype=torch.bfloat16, device="cuda:0")
+            iha.check(iha.iha_project_heads(dinp["X"], dinp["W_Q"], dinp["W_K"], dinp["W_V"], w.B, w.N, w.H,
+                                            w.d, dt, Y, s))
+            iha.check(iha.iha_mix_heads(Y, dinp["alpha_Q"], dinp["alpha_K"], dinp["alpha_V"], w.B, w.N, w.H,
+                                        w.d, w.P, dt, QKV, s))
+            # the head projections themselves: X W_s^(m), checked in float64 on a slice
+            f = gi.as_f64(inp)
+            sl = slice(0, 7)
+            yref = f["X"].reshape(-1, w.D)[sl] @ f["W_V"]
+            ygot = Y[sl, 2 * w.D:3 * w.D].double().cpu().numpy()
+            np.testing.assert_allclose(ygot, yref, rtol=2e-2, atol=2e-2 * np.abs(yref).max())
+        iha.check(iha.iha_attention(QKV, w.B, w.N, w.H, w.d, w.P, w.mask_mode, w.window, dt, Pbar, s))
+        iha.check(iha.iha_contract(Pbar, dinp["R"], w.B, w.N, w.H, w.d, w.P, dt, out, s))
+        torch.cuda.synchronize()
+        assert_parity(w, out.double().cpu().numpy(), ora)
+        if r == route:
+            assert torch.equal(out, ref)
+        if r == 0:
+            # the folded weights are the mixing sum (checked in float64 on a slice)
+            f = gi.as_f64(inp)
+            h, j, c = 1, P - 1, 5
+            col = sum(f["alpha_K"][m, h, j] * f["W_K"][:, m * w.d + c] for m in range(w.H))
+            row = Wt[1 * w.H * w.P * w.d + h * w.P * w.d + j * w.d + c].double().cpu().numpy()
+            np.testing.assert_allclose(row, col, rtol=1e-2, atol=1e-2 * np.abs(col).max())
 
 
 def test_caller_workspace_and_default_stream_entry(iha):

@@ -32,7 +32,8 @@ IHA_MASK_WINDOW = 2
 EXPORTED = ("iha_forward", "iha_forward_ex", "iha_workspace_bytes", "iha_error_string",
             "iha_check_device_status", "iha_forward_host", "iha_host_buffer_bytes",
             "iha_selftest_wait_timeout", "iha_fold_weights", "iha_project", "iha_attention",
-            "iha_contract", "iha_forward_noalloc")
+            "iha_contract", "iha_forward_noalloc", "iha_projection_route", "iha_project_heads",
+            "iha_mix_heads")
 
 IHA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -75,6 +76,12 @@ def _load():
     lib.iha_attention.restype = i
     lib.iha_contract.argtypes = [vp, fp] + shape + [i, vp, vp]
     lib.iha_contract.restype = i
+    lib.iha_projection_route.argtypes = [i, i, i, i]
+    lib.iha_projection_route.restype = i
+    lib.iha_project_heads.argtypes = [vp] * 4 + [i] * 5 + [vp, vp]
+    lib.iha_project_heads.restype = i
+    lib.iha_mix_heads.argtypes = [vp] + [fp] * 3 + [i] * 6 + [vp, vp]
+    lib.iha_mix_heads.restype = i
     lib.iha_forward_noalloc.argtypes = [vp] * 4 + [fp] * 4 + shape + [i, i, vp, i, vp]
     lib.iha_forward_noalloc.restype = i
     return lib
@@ -149,6 +156,19 @@ def iha_fold_weights(W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, H, d, P, dtype, W
 
 def iha_project(X, Wt, B, N, H, d, P, dtype, QKV, stream=None) -> int:
     return _lib.iha_project(_p(X), _p(Wt), B, N, H, d, P, dtype, _p(QKV), _s(stream))
+
+
+def iha_projection_route(H, d, P, dtype) -> int:
+    return int(_lib.iha_projection_route(H, d, P, dtype))
+
+
+def iha_project_heads(X, W_Q, W_K, W_V, B, N, H, d, dtype, Y, stream=None) -> int:
+    return _lib.iha_project_heads(_p(X), _p(W_Q), _p(W_K), _p(W_V), B, N, H, d, dtype, _p(Y), _s(stream))
+
+
+def iha_mix_heads(Y, alpha_Q, alpha_K, alpha_V, B, N, H, d, P, dtype, QKV, stream=None) -> int:
+    return _lib.iha_mix_heads(_p(Y), _p(alpha_Q), _p(alpha_K), _p(alpha_V), B, N, H, d, P, dtype, _p(QKV),
+                              _s(stream))
 
 
 def iha_attention(QKV, B, N, H, d, P, mask_mode, window, dtype, Pbar, stream=None) -> int:

@@ -83,8 +83,10 @@ struct WsLayout {
 static WsLayout ws_layout(const Shape &sh, int dtype) {
     const size_t es = elem_size(dtype);
     WsLayout w;
-    w.wt = 0;
-    w.qkv = align256((size_t)sh.wt_rows() * (size_t)sh.D() * es);
+    w.wt = 0;   // folded weights Wt, or the head projections Y on the unfolded route
+    const size_t first = unfolded_route(sh, dtype) ? (size_t)sh.B * sh.N * 3 * (size_t)sh.D() * es
+                                                   : (size_t)sh.wt_rows() * (size_t)sh.D() * es;
+    w.qkv = align256(first);
     w.pbar = w.qkv + align256(3 * (size_t)sh.qkv_elems() * es);
     w.total = w.pbar + align256((size_t)sh.B * sh.N * sh.H * sh.P * sh.d * es);
     return w;
@@ -106,10 +108,16 @@ static int run_forward(const void *X, const void *WQ, const void *WK, const void
     int *status = status_ptr();
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     void *Wt = ws + lay.wt, *QKV = ws + lay.qkv, *Pbar = ws + lay.pbar;
-    cudaError_t e = launch_fold(WQ, WK, WV, aQ, aK, aV, sh, dtype, Wt, st);
-    if (e == cudaSuccess) e = launch_project(X, Wt, sh, dtype, QKV, st, status);
+    cudaError_t e;
+    if (unfolded_route(sh, dtype)) {
+        e = launch_project_heads(X, WQ, WK, WV, sh, Wt, st, status);   // Y in the first region
+        if (e == cudaSuccess) e = launch_mix(Wt, aQ, aK, aV, sh, QKV, st, status);
+    } else {
+        e = launch_fold(WQ, WK, WV, aQ, aK, aV, sh, dtype, Wt, st);
+        if (e == cudaSuccess) e = launch_project(X, Wt, sh, dtype, QKV, st, status);
+    }
     if (e == cudaSuccess) e = launch_attention(QKV, sh, mask_mode, window, dtype, Pbar, st, status);
-    if (e == cudaSuccess) e = launch_contract(Pbar, R, sh, dtype, out, st);
+    if (e == cudaSuccess) e = launch_contract(Pbar, R, sh, dtype, out, st, status);
     if (own) {
         const cudaError_t e2 = cudaFreeAsync(workspace, st);
         if (e == cudaSuccess) e = e2;
@@ -276,6 +284,31 @@ int iha_project(const void *X, const void *Wt, int B, int N, int H, int d, int P
         launch_project(X, Wt, Shape{B, N, H, d, P}, dtype, QKV, static_cast<cudaStream_t>(stream), status_ptr()));
 }
 
+int iha_projection_route(int H, int d, int P, int dtype) {
+    if (validate_shape(1, 1, H, d, P, dtype) != IHA_OK) return -1;
+    return unfolded_route(Shape{1, 1, H, d, P}, dtype) ? 1 : 0;
+}
+
+int iha_project_heads(const void *X, const void *W_Q, const void *W_K, const void *W_V, int B, int N, int H, int d,
+                      int dtype, void *Y, void *stream) {
+    if (!X || !W_Q || !W_K || !W_V || !Y) return IHA_ERR_INVALID_ARG;
+    const int rc = validate_shape(B, N, H, d, 1, dtype);
+    if (rc != IHA_OK) return rc;
+    if (dtype != IHA_DTYPE_BF16) return IHA_ERR_UNSUPPORTED;
+    return cuda_status(launch_project_heads(X, W_Q, W_K, W_V, Shape{B, N, H, d, 1}, Y,
+                                            static_cast<cudaStream_t>(stream), status_ptr()));
+}
+
+int iha_mix_heads(const void *Y, const float *alpha_Q, const float *alpha_K, const float *alpha_V, int B, int N, int H,
+                  int d, int P, int dtype, void *QKV, void *stream) {
+    if (!Y || !alpha_Q || !alpha_K || !alpha_V || !QKV) return IHA_ERR_INVALID_ARG;
+    const int rc = validate_shape(B, N, H, d, P, dtype);
+    if (rc != IHA_OK) return rc;
+    if (dtype != IHA_DTYPE_BF16 || H > 16) return IHA_ERR_UNSUPPORTED;
+    return cuda_status(launch_mix(Y, alpha_Q, alpha_K, alpha_V, Shape{B, N, H, d, P}, QKV,
+                                  static_cast<cudaStream_t>(stream), status_ptr()));
+}
+
 int iha_attention(const void *QKV, int B, int N, int H, int d, int P, int mask_mode, int window, int dtype,
                   void *Pbar, void *stream) {
     if (!QKV || !Pbar) return IHA_ERR_INVALID_ARG;
@@ -291,7 +324,8 @@ int iha_contract(const void *Pbar, const float *R, int B, int N, int H, int d, i
     if (!Pbar || !R || !out) return IHA_ERR_INVALID_ARG;
     const int rc = validate_shape(B, N, H, d, P, dtype);
     if (rc != IHA_OK) return rc;
-    return cuda_status(launch_contract(Pbar, R, Shape{B, N, H, d, P}, dtype, out, static_cast<cudaStream_t>(stream)));
+    return cuda_status(
+        launch_contract(Pbar, R, Shape{B, N, H, d, P}, dtype, out, static_cast<cudaStream_t>(stream), status_ptr()));
 }
 
 }  // extern "C"

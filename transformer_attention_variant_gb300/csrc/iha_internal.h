@@ -20,6 +20,7 @@ enum WaitSite {
     kSiteAttnMmaV = 20,
     kSiteAttnSoftmax = 21,
     kSiteAttnEpilogue = 22,
+    kSiteRowMix = 30,
     kSiteSelfTest = 99,
 };
 
@@ -39,13 +40,31 @@ cudaError_t launch_fold(const void *WQ, const void *WK, const void *WV, const fl
 cudaError_t launch_project(const void *X, const void *Wt, const Shape &sh, int dtype, void *QKV,
                            cudaStream_t st, int *status);
 
+// Steps 1+2 without the fold (bf16): Y = X [W_Q | W_K | W_V], Y [B*N][3][H*d] row-major.
+cudaError_t launch_project_heads(const void *X, const void *WQ, const void *WK, const void *WV, const Shape &sh,
+                                 void *Y, cudaStream_t st, int *status);
+
+// The pseudo-head mixing of Y into the stacked QKV layout (bf16 Qbar/Kbar, f16 Vbar).
+cudaError_t launch_mix(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh, void *QKV,
+                       cudaStream_t st, int *status);
+
+// Which way the library computes steps 1+2: true = project the heads then mix (bf16,
+// P >= 2, H <= 16: 1/P of the folded GEMM's work), false = fold alpha into W first.
+inline bool unfolded_route(const Shape &sh, int dtype) { return dtype == 1 && sh.P >= 2 && sh.H <= 16; }
+
 // Step 3: masked softmax attention per head over the stacked sequence -> Pbar [B][N][H][P][d].
 cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
                              void *Pbar, cudaStream_t st, int *status);
 
 // Step 4: out[b][t][h][:] = sum_i R[h][i] Pbar[b][t][i][:], i = h'*P + j.
 cudaError_t launch_contract(const void *Pbar, const float *R, const Shape &sh, int dtype, void *out,
-                            cudaStream_t st);
+                            cudaStream_t st, int *status);
+
+// The bf16 contraction (TMA-fed row mixing) when its 3-stage ring fits in shared memory;
+// otherwise, and for fp32, a SIMT kernel.
+bool contract_rowmix_fits(const Shape &sh);
+cudaError_t launch_contract_rowmix(const void *Pbar, const float *R, const Shape &sh, void *out, cudaStream_t st,
+                                   int *status);
 
 // A kernel whose only wait can never be satisfied: it must give up after limit_ns and
 // record kSiteSelfTest in the status word (exercises the failure path of every wait).

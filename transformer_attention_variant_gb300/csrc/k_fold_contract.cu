@@ -8,6 +8,7 @@
 //  * contract: the unstack-and-contract step of Algorithm 1 ("反堆疊與收縮"),
 //    O_h[t] = sum_{h'} sum_j R[h, h'P + j] P_{h',j}[t], heads concatenated.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "iha_internal.h"
 
@@ -219,8 +220,11 @@ static cudaError_t launch_contract_t(const void *Pbar, const float *R, const Sha
 }
 
 cudaError_t launch_contract(const void *Pbar, const float *R, const Shape &sh, int dtype, void *out,
-                            cudaStream_t st) {
-    if (dtype == 1) return launch_contract_t<__nv_bfloat16, 8>(Pbar, R, sh, out, st);
+                            cudaStream_t st, int *status) {
+    if (dtype == 1) {
+        if (contract_rowmix_fits(sh)) return launch_contract_rowmix(Pbar, R, sh, out, st, status);
+        return launch_contract_t<__nv_bfloat16, 8>(Pbar, R, sh, out, st);
+    }
     if (sh.d % 4 == 0) return launch_contract_t<float, 4>(Pbar, R, sh, out, st);
     return launch_contract_t<float, 1>(Pbar, R, sh, out, st);
 }

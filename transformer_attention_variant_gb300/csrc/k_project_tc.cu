@@ -6,6 +6,12 @@
 // K = D, N = 3*H*P*d columns).  The epilogue writes each column block straight into the
 // stacked layout QKV[s][b][h][t*P + j][c], so no separate stacking pass exists.
 //
+// A second mode (PLAIN) is the same GEMM without the fold: Y = X [W_Q | W_K | W_V], the
+// per-head projections X W_s^(m) of all heads, with the weights read as they are stored
+// ([D][H*d], N contiguous: an MN-major B operand) and Y written row-major [B*N][3*H*d]; the
+// pseudo-head mixing then runs as a separate pass (mix_kernel).  For P >= 2 this does 1/P of
+// the folded GEMM's tensor work.
+//
 // Design (sm_103a): persistent CTAs, one per SM; warp 0 = TMA producer (128B-swizzled
 // A and B tiles, 4-stage ring), warp 1 = MMA issuer (tcgen05.mma kind::f16, M=128 N=256
 // K=16, fp32 accumulators in TMEM, double-buffered so the epilogue of one tile overlaps
@@ -26,7 +32,10 @@ constexpr int PG_THREADS = 192;
 constexpr int PG_SMEM = PG_STAGES * (PG_A_BYTES + PG_B_BYTES) + 256 + 1024;
 
 struct ProjParams {
-    __nv_bfloat16 *qkv;
+    __nv_bfloat16 *qkv;   // folded mode: stacked output
+    __nv_bfloat16 *y;     // plain mode: [M][3 * hd] output
+    int hd;               // plain mode: H*d columns per projection
+    int ntps;             // plain mode: N tiles per projection
     long long s_stride;   // elements of one of Qbar/Kbar/Vbar
     int M, Ncols, K;
     int N_tok, H, P, d;
@@ -34,8 +43,10 @@ struct ProjParams {
     int *status;
 };
 
+template <bool PLAIN>
 __global__ void __launch_bounds__(PG_THREADS, 1)
-proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const ProjParams p) {
+proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, const ProjParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
@@ -63,6 +74,10 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (PLAIN) {
+            tma_prefetch_desc(&tmB1);
+            tma_prefetch_desc(&tmB2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -84,7 +99,17 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.status, kSiteProjProducer, abort_flag)) goto producer_done;
                     mbar_arrive_expect_tx(&full[stage], PG_A_BYTES + PG_B_BYTES);
                     tma_load_2d(&tmA, &full[stage], sA + stage * PG_A_BYTES, kb * PG_K, mt * PG_M);
-                    tma_load_2d(&tmB, &full[stage], sB + stage * PG_B_BYTES, kb * PG_K, nt * PG_N);
+                    if (PLAIN) {
+                        // B tile = 4 boxes of [64 k][64 n] of W_s (n contiguous): MN-major chunks
+                        const int s = nt / p.ntps, n0 = (nt % p.ntps) * PG_N;
+                        const CUtensorMap *mb = s == 0 ? &tmB : (s == 1 ? &tmB1 : &tmB2);
+#pragma unroll
+                        for (int i = 0; i < PG_N / 64; ++i)
+                            tma_load_2d(mb, &full[stage], sB + stage * PG_B_BYTES + i * (64 * PG_K * 2), n0 + 64 * i,
+                                        kb * PG_K);
+                    } else {
+                        tma_load_2d(&tmB, &full[stage], sB + stage * PG_B_BYTES, kb * PG_K, nt * PG_N);
+                    }
                     if (++stage == PG_STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -95,7 +120,7 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(PG_M, PG_N, 0, 0);
+            constexpr uint32_t idesc = idesc_bf16_f32(PG_M, PG_N, 0, PLAIN ? 1 : 0);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -115,9 +140,13 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     const uint32_t a0 = smem_u32(sA + stage * PG_A_BYTES);
                     const uint32_t b0 = smem_u32(sB + stage * PG_B_BYTES);
 #pragma unroll
-                    for (int k = 0; k < PG_K / 16; ++k)
-                        mma_ss(dt, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(b0 + k * 32, 16, 1024), idesc,
-                               (kb | k) != 0);
+                    for (int k = 0; k < PG_K / 16; ++k) {
+                        // K-major B: the next 16 k are 32 bytes along the row; MN-major B: 16 rows of
+                        // 128 bytes further, 64-column chunks 8 KB apart (leading byte offset)
+                        const uint64_t bdesc = PLAIN ? sdesc_sw128(b0 + k * 2048, 64 * PG_K * 2, 1024)
+                                                     : sdesc_sw128(b0 + k * 32, 16, 1024);
+                        mma_ss(dt, sdesc_sw128(a0 + k * 32, 16, 1024), bdesc, idesc, (kb | k) != 0);
+                    }
                     mma_commit(&empty[stage]);
                     if (++stage == PG_STAGES) {
                         stage = 0;
@@ -148,6 +177,21 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 uint32_t r[32];
                 tmem_ld32(tmem_base + acc * PG_N + c0 + (uint32_t(q * 32) << 16), r);
                 tmem_ld_wait();
+                if (PLAIN) {
+                    const int s = nt / p.ntps;
+                    const long long n = (long long)(nt % p.ntps) * PG_N + c0;
+                    if (row_ok && n < p.hd) {
+                        uint4 v[4];
+                        uint32_t *vw = reinterpret_cast<uint32_t *>(v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            vw[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                        uint4 *d4 = reinterpret_cast<uint4 *>(p.y + m * (3LL * p.hd) + (long long)s * p.hd + n);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) d4[i] = v[i];
+                    }
+                    continue;
+                }
                 const long long n = (long long)nt * PG_N + c0;
                 if (row_ok && n < p.Ncols) {
                     // columns n..n+31 lie in one (s, h) block because P*d is a multiple of 32
@@ -200,7 +244,7 @@ cudaError_t launch_project(const void *X, const void *Wt, const Shape &sh, int d
         const uint32_t box[2] = {PG_K, PG_N};
         if (!make_tmap_bf16(&tmB, Wt, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    ProjParams p;
+    ProjParams p{};
     p.qkv = (__nv_bfloat16 *)QKV;
     p.s_stride = sh.qkv_elems();
     p.M = (int)M;
@@ -214,10 +258,48 @@ cudaError_t launch_project(const void *X, const void *Wt, const Shape &sh, int d
     const int num_n_tiles = (int)((Ncols + PG_N - 1) / PG_N);
     p.num_tiles = p.num_m_tiles * num_n_tiles;
     p.status = status;
-    cudaError_t e = cudaFuncSetAttribute(proj_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(proj_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < device_sm_count() ? p.num_tiles : device_sm_count();
-    proj_gemm_tc<<<grid, PG_THREADS, PG_SMEM, st>>>(tmA, tmB, p);
+    proj_gemm_tc<false><<<grid, PG_THREADS, PG_SMEM, st>>>(tmA, tmB, tmB, tmB, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_project_heads(const void *X, const void *WQ, const void *WK, const void *WV, const Shape &sh,
+                                 void *Y, cudaStream_t st, int *status) {
+    const long long M = (long long)sh.B * sh.N, K = sh.D(), hd = (long long)sh.H * sh.d;
+    if (hd % 64 != 0) return cudaErrorInvalidValue;
+    CUtensorMap tmA, tmW[3];
+    {
+        const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+        const uint64_t strides[1] = {(uint64_t)K * 2};
+        const uint32_t box[2] = {PG_K, PG_M};
+        if (!make_tmap_bf16(&tmA, X, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    const void *W[3] = {WQ, WK, WV};
+    for (int s = 0; s < 3; ++s) {
+        const uint64_t dims[2] = {(uint64_t)hd, (uint64_t)K};   // n (contiguous), k
+        const uint64_t strides[1] = {(uint64_t)hd * 2};
+        const uint32_t box[2] = {64, PG_K};
+        if (!make_tmap_bf16(&tmW[s], W[s], 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    ProjParams p{};
+    p.y = (__nv_bfloat16 *)Y;
+    p.hd = (int)hd;
+    p.ntps = (int)((hd + PG_N - 1) / PG_N);
+    p.M = (int)M;
+    p.K = (int)K;
+    p.N_tok = sh.N;
+    p.H = sh.H;
+    p.P = sh.P;
+    p.d = sh.d;
+    p.num_m_tiles = (int)((M + PG_M - 1) / PG_M);
+    p.num_tiles = p.num_m_tiles * 3 * p.ntps;
+    p.status = status;
+    cudaError_t e = cudaFuncSetAttribute(proj_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
+    if (e != cudaSuccess) return e;
+    const int grid = p.num_tiles < device_sm_count() ? p.num_tiles : device_sm_count();
+    proj_gemm_tc<true><<<grid, PG_THREADS, PG_SMEM, st>>>(tmA, tmW[0], tmW[1], tmW[2], p);
     return cudaGetLastError();
 }
 
