@@ -192,7 +192,7 @@ IHA_API int iha_project(const void *X, const void *Wt, int B, int N, int H, int 
                 int dtype, void *QKV, void *stream);
 
 /* Which way steps 1+2 run for this shape (what iha_forward_ex does):
- *   1 = unfolded: iha_project_heads then iha_mix_heads (bf16 with P >= 2 and H <= 16 --
+ *   1 = unfolded: iha_project_heads then iha_mix_heads (bf16, P >= 2, H <= 16, H*P <= 128 --
  *       the projection GEMM then does 1/P of the folded GEMM's work);
  *   0 = folded:   iha_fold_weights then iha_project;
  *  -1 = invalid sizes or dtype. */
@@ -204,8 +204,9 @@ IHA_API int iha_projection_route(int H, int d, int P, int dtype);
 IHA_API int iha_project_heads(const void *X, const void *W_Q, const void *W_K, const void *W_V,
                               int B, int N, int H, int d, int dtype, void *Y, void *stream);
 
-/* Steps 1+2, second half, and the stacking (bf16 only, H <= 16): the pseudo-head mixing
- * S~_{h,j} = sum_m alpha_s[m,h,j] (X W_s^(m)) of Y into QKV (layout as for iha_project). */
+/* Steps 1+2, second half, and the stacking (bf16 only, H <= 16, H*P <= 128): the mixing
+ * S~_{h,j} = sum_m alpha_s[m,h,j] (X W_s^(m)) of Y into QKV (layout as for iha_project).
+ * Y and QKV must be 16-byte aligned (IHA_ERR_INVALID_ARG otherwise). */
 IHA_API int iha_mix_heads(const void *Y, const float *alpha_Q, const float *alpha_K, const float *alpha_V,
                           int B, int N, int H, int d, int P, int dtype, void *QKV, void *stream);
 

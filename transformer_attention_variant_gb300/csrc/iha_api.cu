@@ -304,7 +304,8 @@ int iha_mix_heads(const void *Y, const float *alpha_Q, const float *alpha_K, con
     if (!Y || !alpha_Q || !alpha_K || !alpha_V || !QKV) return IHA_ERR_INVALID_ARG;
     const int rc = validate_shape(B, N, H, d, P, dtype);
     if (rc != IHA_OK) return rc;
-    if (dtype != IHA_DTYPE_BF16 || H > 16) return IHA_ERR_UNSUPPORTED;
+    if (dtype != IHA_DTYPE_BF16 || H > 16 || H * P > 128) return IHA_ERR_UNSUPPORTED;
+    if (((reinterpret_cast<uintptr_t>(Y) | reinterpret_cast<uintptr_t>(QKV)) & 15) != 0) return IHA_ERR_INVALID_ARG;
     return cuda_status(launch_mix(Y, alpha_Q, alpha_K, alpha_V, Shape{B, N, H, d, P}, QKV,
                                   static_cast<cudaStream_t>(stream), status_ptr()));
 }

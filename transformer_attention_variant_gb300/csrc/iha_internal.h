@@ -21,6 +21,9 @@ enum WaitSite {
     kSiteAttnSoftmax = 21,
     kSiteAttnEpilogue = 22,
     kSiteRowMix = 30,
+    kSiteMixProducer = 31,
+    kSiteMixMma = 32,
+    kSiteMixEpilogue = 33,
     kSiteSelfTest = 99,
 };
 
@@ -49,8 +52,10 @@ cudaError_t launch_mix(const void *Y, const float *aQ, const float *aK, const fl
                        cudaStream_t st, int *status);
 
 // Which way the library computes steps 1+2: true = project the heads then mix (bf16,
-// P >= 2, H <= 16: 1/P of the folded GEMM's work), false = fold alpha into W first.
-inline bool unfolded_route(const Shape &sh, int dtype) { return dtype == 1 && sh.P >= 2 && sh.H <= 16; }
+// P >= 2, H <= 16, H*P <= 128: 1/P of the folded GEMM's work), false = fold alpha into W.
+inline bool unfolded_route(const Shape &sh, int dtype) {
+    return dtype == 1 && sh.P >= 2 && sh.H <= 16 && sh.H * sh.P <= 128;
+}
 
 // Step 3: masked softmax attention per head over the stacked sequence -> Pbar [B][N][H][P][d].
 cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,

@@ -1,14 +1,10 @@
-// k_rowmix.cu -- the two per-token "row mixing" steps of Algorithm 1 ("Interleaved Head
-// Attention" section 4), both of the form  out[t][r][:] = sum_k coef[k][r] * in[t][k][:]:
+// k_rowmix.cu -- a per-token "row mixing" kernel, out[t][r][:] = sum_k coef[k][r] in[t][k][:],
+// used for the unstack + contraction step of Algorithm 1 ("Interleaved Head Attention"
+// section 4, "反堆疊與收縮"): in = Pbar[t][h'*P + j][:] (k = h'P + j, H*P rows),
+// coef[k][h] = R[h][k], out = O[t][h][:] (heads concatenated).  (The kernel also supports a
+// mixing mode that writes the stacked pseudo-head layout.)
 //
-//  * pseudo-head mixing ("偽頭混合"), unfolded route: in = the head projections
-//    Y_s[t][m][:] = (X W_s^(m))[t] (k = m, H rows), coef = alpha_s[m][h*P + j], out = the
-//    pseudo-heads S~_{h,j}[t], written to the stacked layout QKV[s][b][h][t*P + j][:]
-//    (Qbar, Kbar bf16; Vbar f16);
-//  * unstack + contraction ("反堆疊與收縮"): in = Pbar[t][h'*P + j][:] (k = h'P + j, H*P
-//    rows), coef[k][h] = R[h][k], out = O[t][h][:] (heads concatenated).
-//
-// Both are HBM-bound streams with little arithmetic per byte.  Design: persistent CTAs
+// An HBM-bound stream with little arithmetic per byte.  Design: persistent CTAs
 // (two per SM); a tile is a few whole tokens whose input rows (contiguous d-element rows)
 // arrive by cp.async.bulk into a 3-stage shared-memory ring, so the next tiles' bytes are
 // in flight while the current one is computed.  A thread computes a register tile of R
@@ -219,26 +215,6 @@ static cudaError_t launch_rowmix(const float *c0, const float *c1, const float *
     const unsigned grid = (unsigned)(p.num_tiles < maxgrid ? p.num_tiles : maxgrid);
     rowmix_kernel<MIX, R><<<grid, RM_THREADS, smem, st>>>(c0, c1, c2, p);
     return cudaGetLastError();
-}
-
-cudaError_t launch_mix(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh, void *QKV,
-                       cudaStream_t st, int *status) {
-    if (sh.d % 8 != 0) return cudaErrorInvalidValue;
-    RowMixParams p{};
-    p.in = (const __nv_bfloat16 *)Y;
-    p.out = (__nv_bfloat16 *)QKV;
-    p.ntok = (long long)sh.B * sh.N;
-    p.N_tok = sh.N;
-    p.H = sh.H;
-    p.P = sh.P;
-    p.d = sh.d;
-    p.K = sh.H;
-    p.NR = sh.H * sh.P;
-    p.in_tok_stride = 3LL * sh.H * sh.d;
-    p.s_stride = sh.qkv_elems();
-    p.nsets = 3;
-    p.status = status;
-    return launch_rowmix<true, 8>(aQ, aK, aV, p, st);
 }
 
 cudaError_t launch_contract_rowmix(const void *Pbar, const float *R, const Shape &sh, void *out, cudaStream_t st,

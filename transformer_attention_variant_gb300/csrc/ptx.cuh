@@ -141,6 +141,39 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Bulk (untiled) store shared -> global, tracked by this thread's bulk groups.  Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// All but the newest `pending` (0..2) of this thread's committed bulk groups have
+// finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read(int pending) {
+    if (pending >= 2)
+        asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+    else if (pending == 1)
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    else
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// All of this thread's committed bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Named barrier `id` over `nthreads` threads that also ORs a predicate across them: every
+// participant gets the same result.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q, o;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred o, %2, %3, q;\n\tselp.u32 %0, 1, 0, o;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void tma_load_2d(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
