@@ -20,6 +20,9 @@ enum WaitSite {
     kSiteAttnMmaV = 20,
     kSiteAttnSoftmax = 21,
     kSiteAttnEpilogue = 22,
+    kSiteAttnMmaO = 23,
+    kSiteAttnProducerQ = 24,
+    kSiteAttnItem = 25,
     kSiteRowMix = 30,
     kSiteMixProducer = 31,
     kSiteMixMma = 32,

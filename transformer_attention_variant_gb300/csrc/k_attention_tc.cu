@@ -10,20 +10,36 @@
 // outside the union of intervals of a CTA's rows are skipped and tiles inside every row's
 // interval run without any mask arithmetic.
 //
-// Design (sm_103a, one CTA per SM):
-//   - a CTA owns 256 query rows of one (b, h): two 128-row tiles Q0, Q1 that ping-pong so
+// Design (sm_103a): a persistent kernel, one CTA per SM, looping over work items.
+//   - an item is 256 query rows of one (b, h): two 128-row tiles Q0, Q1 that ping-pong so
 //     the tensor cores work on one tile while the softmax warps work on the other;
-//   - warp 8: TMA producer (Q once; K and V tiles through a 2-stage ring, 128B swizzle);
+//   - items are drawn in a fixed order (head groups that fit in L2, heaviest query blocks
+//     first) from a per-launch counter as CTAs free up, so the items in flight stay a
+//     compact window of that order, as a non-persistent grid would start them;
+//   - warp 8: TMA producer -- draws the next item and hands it on through a small ring in
+//     shared memory, then loads its K(0), Q0, Q1 while the previous item is still being
+//     finished, and streams K and V tiles through separate rings (128B swizzle);
 //   - warp 9: MMA issuer: S_i = Q_i K^T (SS, M=128 N=128) into TMEM, then O_i += P_i V
 //     with P_i read from TMEM (TS form, M=128 N=d, f16 P and f16 V) -- P never touches
-//     shared memory;
+//     shared memory.  The next item's first S-MMAs run while the softmax warps are in the
+//     previous item's epilogue; its first PV-MMA waits until O_i has been read out;
+//   - warps 8 and 9 run their loops on the whole warp and issue from one elected lane:
+//     warp-uniform loop values stay in uniform registers, and the issue path is short
+//     (single-lane loops cost about 8% of tensor time here);
 //   - warps 0-3 / 4-7: softmax of Q0 / Q1, one thread per row (32x32b TMEM loads): row
-//     max, exp2 (two per MUFU op in f16x2), row sum, f16 P written back over its S columns.  The running max is only
-//     raised when a tile's max exceeds it by more than 8 (log2 units), so O (in TMEM) is
-//     rarely rescaled; values stay <= 2^8 before normalisation;
-//   - epilogue: O / l -> bf16 -> Pbar[b][t][h][j][:].
+//     max, exp2 (two per MUFU op in f16x2), row sum, f16 P written back over its S
+//     columns.  The running max is only raised when a tile's max exceeds it by more than 8
+//     (log2 units), so O (in TMEM) is rarely rescaled; values stay <= 2^8 before
+//     normalisation;
+//   - epilogue: O / l -> bf16 -> Pbar[b][t][h][j][:].  When P divides 128 a tile's rows are
+//     whole tokens: each thread writes its row into the (now idle) Q tile of its warpgroup
+//     in the 128B-swizzled layout and one thread sends the tile with TMA tensor stores
+//     (rank-5 map over [B][N][H][P][d]), then releases the Q tile for the next item.  One
+//     thread per row storing 16 bytes at a time touches a different line with every lane.
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d)  (512 columns allocated).
 #include <cuda_bf16.h>
+
+#include <atomic>
 
 #include "iha_internal.h"
 #include "ptx.cuh"
@@ -36,10 +52,12 @@ constexpr int AT_BN = 128;         // key rows per tile
 constexpr int AT_THREADS = 384;    // 2 softmax warpgroups + 1 warpgroup (producer, MMA, 2 idle)
 // Register split (setmaxnreg): the kernel is compiled to exactly AT_LAUNCH_REGS per thread
 // (384 x 168 = 64512 registers allocated at launch); the producer/MMA warpgroup gives
-// registers back, the softmax warpgroups take them: 128 x 56 + 256 x 224 = 64512.
-constexpr int AT_LAUNCH_REGS = 168, AT_REGS_SOFTMAX = 224, AT_REGS_CONTROL = 56;
+// registers back, the softmax warpgroups take them: 128 x 72 + 256 x 216 = 64512.
+constexpr int AT_LAUNCH_REGS = 168, AT_REGS_SOFTMAX = 216, AT_REGS_CONTROL = 72;
 static_assert(128 * AT_REGS_CONTROL + 256 * AT_REGS_SOFTMAX <= AT_THREADS * AT_LAUNCH_REGS, "register split");
 constexpr float AT_RESCALE_THRESHOLD = 8.0f;
+constexpr int AT_ITEM_SLOTS = 4;   // work items handed from the TMA warp to the other roles
+constexpr int AT_TICKETS = 1024;   // per-launch work counters (a ring; see launch_attn_tc)
 
 template <int DH>
 struct AttnCfg {
@@ -50,7 +68,10 @@ struct AttnCfg {
     // second PV-MMA: K gets the deeper ring so the next K is resident before it is needed.
     static constexpr int KSTAGES = DH == 128 ? 3 : 4;
     static constexpr int VSTAGES = DH == 128 ? 2 : 4;
-    static constexpr int SMEM = 2 * Q_BYTES + (KSTAGES + VSTAGES) * KV_BYTES + 256 + 1024;
+    static constexpr int NBARS = 12 + 2 * (KSTAGES + VSTAGES) + 2 * AT_ITEM_SLOTS;
+    static constexpr int CTRL_BYTES = 512;   // barriers, item slots, TMEM address, abort flag
+    static constexpr int SMEM = 2 * Q_BYTES + (KSTAGES + VSTAGES) * KV_BYTES + CTRL_BYTES + 1024;
+    static_assert(NBARS * 8 + AT_ITEM_SLOTS * 16 + 8 <= CTRL_BYTES, "control area");
     __device__ static constexpr uint32_t s_col(int i) { return uint32_t(i) * 128u; }
     __device__ static constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * DH; }
 };
@@ -63,6 +84,8 @@ struct AttnParams {
     int num_qblocks;
     int num_heads;         // B * H
     int head_group;        // heads per scheduling group
+    int stage_o;           // epilogue through shared memory and TMA (P divides 128)
+    unsigned int *ticket;  // this launch's work counter (0 at launch)
     int *status;
 };
 
@@ -72,25 +95,57 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// readable stacked key rows of query row r: [lo, hi]
-__device__ __forceinline__ void key_interval(const AttnParams &p, long long r, long long &lo, long long &hi) {
-    const long long t = r / p.P;
+// readable stacked key rows of query row r: [lo, hi] (stacked lengths are at most 2^24,
+// so 32-bit arithmetic holds every value here)
+__device__ __forceinline__ void key_interval(const AttnParams &p, int r, int &lo, int &hi) {
+    const int t = r / p.P;
     lo = 0;
     hi = p.L - 1;
-    if (p.mask_mode >= 1) {
-        const long long h2 = (t + 1) * p.P - 1;
-        if (h2 < hi) hi = h2;
-    }
-    if (p.mask_mode == 2) {
-        const long long l2 = (t - p.window + 1) * p.P;
-        if (l2 > lo) lo = l2;
-    }
+    if (p.mask_mode >= 1) hi = min(hi, (t + 1) * p.P - 1);
+    if (p.mask_mode == 2) lo = max(lo, (t - p.window + 1) * p.P);
+}
+
+// Work item i (0 <= i < B*H*num_qblocks) -> (bh, qb): heads in groups of p.head_group
+// (chosen so that a group's K and V fit in L2); within a group, query blocks heaviest
+// (latest) first across the group's heads.  The CTAs working at one time then share one
+// group's K/V in L2, and the light blocks of each group fill the tail of its round.
+__device__ __forceinline__ void item_coords(const AttnParams &p, long long i, int &bh, int &qb) {
+    const long long per_group = (long long)p.head_group * p.num_qblocks;
+    const int g = (int)(i / per_group);
+    const int j = (int)(i % per_group);
+    const int g_heads = min(p.head_group, p.num_heads - g * p.head_group);
+    bh = g * p.head_group + j % g_heads;
+    qb = p.num_qblocks - 1 - j / g_heads;
+}
+
+// Work counters: a launch takes one (reset to 0 on its stream before the kernel) and its
+// CTAs draw items from it in order, each CTA taking the next item when its TMA warp is
+// done loading the previous one -- the order in which a non-persistent grid would start
+// them, so the items in flight stay a compact window of the ordering above.
+__device__ unsigned int g_attn_tickets[AT_TICKETS];
+
+// A work item as the TMA warp hands it on: head bh, rows [qb*256, qb*256 + 256), and the
+// KV tiles [kv_begin, kv_begin + nkv) those rows need (the union of their readable
+// intervals).  bh < 0 ends the CTA's work.
+struct AttnItem {
+    int bh, qb, kv_begin, nkv;
+};
+__device__ __forceinline__ AttnItem make_item(const AttnParams &p, long long i) {
+    AttnItem it;
+    item_coords(p, i, it.bh, it.qb);
+    const int r0 = it.qb * 2 * AT_BM, r_last = min(r0 + 2 * AT_BM - 1, p.L - 1);
+    int lo_first, hi_first, lo_last, hi_last;
+    key_interval(p, r0, lo_first, hi_first);
+    key_interval(p, r_last, lo_last, hi_last);
+    it.kv_begin = lo_first / AT_BN;
+    it.nkv = hi_last / AT_BN - it.kv_begin + 1;
+    return it;
 }
 
 template <int DH>
 __global__ void __launch_bounds__(AT_THREADS, 1)
 attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-            const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const AttnParams p) {
     using C = AttnCfg<DH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -98,45 +153,34 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     uint8_t *sK = sQ + 2 * C::Q_BYTES;                   // KSTAGES tiles
     uint8_t *sV = sK + C::KSTAGES * C::KV_BYTES;         // VSTAGES tiles
     uint64_t *bars = reinterpret_cast<uint64_t *>(sV + C::VSTAGES * C::KV_BYTES);
-    uint64_t *q_full = bars;
-    uint64_t *k_full = bars + 1;               // [KSTAGES]
+    uint64_t *q_full = bars;                   // [2]
+    uint64_t *q_empty = q_full + 2;            // [2]
+    uint64_t *k_full = q_empty + 2;            // [KSTAGES]
     uint64_t *k_empty = k_full + C::KSTAGES;   // [KSTAGES]
     uint64_t *v_full = k_empty + C::KSTAGES;   // [VSTAGES]
     uint64_t *v_empty = v_full + C::VSTAGES;   // [VSTAGES]
     uint64_t *s_full = v_empty + C::VSTAGES;   // [2]
-    uint64_t *p_full = s_full + 2;            // [2]
-    uint64_t *o_full = p_full + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_full + 1);
+    uint64_t *p_full = s_full + 2;             // [2]
+    uint64_t *o_full = p_full + 2;             // [2]
+    uint64_t *o_empty = o_full + 2;            // [2]
+    uint64_t *item_full = o_empty + 2;                 // [AT_ITEM_SLOTS]
+    uint64_t *item_empty = item_full + AT_ITEM_SLOTS;  // [AT_ITEM_SLOTS]
+    AttnItem *item_slot = reinterpret_cast<AttnItem *>(item_empty + AT_ITEM_SLOTS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(item_slot + AT_ITEM_SLOTS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = warp_id(), lane = lane_id();
-    // Work order: heads in groups of p.head_group (chosen so a group's K and V fit in L2);
-    // within a group, query blocks heaviest (latest) first across the group's heads.  The
-    // CTAs resident at one time then share one group's K/V in L2, and the light blocks of
-    // each group fill the tail of its wave.
-    int bh, qb;
-    {
-        const long long i = blockIdx.x;
-        const long long per_group = (long long)p.head_group * p.num_qblocks;
-        const int g = (int)(i / per_group);
-        const int j = (int)(i % per_group);
-        const int g_heads = min(p.head_group, p.num_heads - g * p.head_group);
-        bh = g * p.head_group + j % g_heads;
-        qb = p.num_qblocks - 1 - j / g_heads;
-    }
-    const long long r0 = (long long)qb * 2 * AT_BM;
-
-    // KV tiles this CTA needs: union of the readable intervals of its rows
-    long long lo_first, hi_first, lo_last, hi_last;
-    const long long r_last = (r0 + 2 * AT_BM - 1 < p.L - 1) ? r0 + 2 * AT_BM - 1 : p.L - 1;
-    key_interval(p, r0, lo_first, hi_first);
-    key_interval(p, r_last, lo_last, hi_last);
-    const int kv_begin = (int)(lo_first / AT_BN);
-    const int kv_end = (int)(hi_last / AT_BN);
-    const int nkv = kv_end - kv_begin + 1;
+    const long long num_items = (long long)p.num_heads * p.num_qblocks;
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);     // one arrive per softmax warp
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 128);  // every thread of the tile's softmax warpgroup
+        }
         for (int s = 0; s < C::KSTAGES; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -145,11 +189,10 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 4);   // one arrive per softmax warp
+        for (int i = 0; i < AT_ITEM_SLOTS; ++i) {
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], 1 + 8);   // the MMA thread and lane 0 of each softmax warp
         }
-        mbar_init(o_full, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -157,6 +200,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        if (p.stage_o) tma_prefetch_desc(&tmO);
     }
     if (warp == 9) {
         tmem_alloc(tmem_slot, 512);
@@ -169,102 +213,192 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     if (warp >= 8) {
       // control warpgroup: gives registers back, then warp 8 = TMA, warp 9 = MMA
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(AT_REGS_CONTROL));
+      // Both roles run their loops on the whole warp (warp-uniform values) and issue from
+      // one elected lane; every wait is decided for the whole warp.
+      const bool leader = elect_one();
       if (warp == 8) {
         // ------------------------------- TMA producer -------------------------------
-        if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
-            for (int i = 0; i < 2; ++i)
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    tma_load_3d(&tmQ, q_full, sQ + i * C::Q_BYTES + c * (AT_BM * 128), c * 64,
-                                (int)(r0 + i * AT_BM), bh);
-            // K runs one tile ahead of V: K(k) is issued before V(k-1)
-            for (int k = 0; k <= nkv; ++k) {
-                if (k < nkv) {
-                    const int st = k % C::KSTAGES;
-                    if (!mbar_wait_lazy(&k_empty[st], ((k / C::KSTAGES) & 1) ^ 1, p.status, kSiteAttnProducer, abort_flag))
-                        break;
+        auto wait = [&](uint64_t *bar, uint32_t par, int site) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait_lazy(bar, par, p.status, site, abort_flag));
+        };
+        int kc = 0, vc = 0;   // K and V tiles loaded so far (ring positions)
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            // draw the next item and hand it to the MMA and softmax warps
+            const int slot = n % AT_ITEM_SLOTS;
+            ok = wait(&item_empty[slot], ((n / AT_ITEM_SLOTS) & 1) ^ 1, kSiteAttnItem);
+            if (!ok) break;
+            unsigned int ticket = 0;
+            if (leader) ticket = atomicAdd(p.ticket, 1u);
+            ticket = __shfl_sync(0xffffffffu, ticket, __ffs(__ballot_sync(0xffffffffu, leader)) - 1);
+            AttnItem it{-1, 0, 0, 0};
+            if (ticket < num_items) it = make_item(p, ticket);
+            if (leader) {
+                item_slot[slot] = it;
+                mbar_arrive(&item_full[slot]);   // release: the slot write is visible to the waiters
+            }
+            if (it.bh < 0) break;
+            const int bh = it.bh, kv_begin = it.kv_begin, nkv = it.nkv;
+            const int r0 = it.qb * 2 * AT_BM;
+            auto load_k = [&](int k) -> bool {
+                const int st = kc % C::KSTAGES;
+                if (!wait(&k_empty[st], ((kc / C::KSTAGES) & 1) ^ 1, kSiteAttnProducer)) return false;
+                if (leader) {
                     mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
                     for (int c = 0; c < C::CHUNKS; ++c)
                         tma_load_3d(&tmK, &k_full[st], sK + st * C::KV_BYTES + c * (AT_BN * 128), c * 64,
                                     (kv_begin + k) * AT_BN, bh);
                 }
-                if (k >= 1) {
-                    const int kv = k - 1, st = kv % C::VSTAGES;
-                    if (!mbar_wait_lazy(&v_empty[st], ((kv / C::VSTAGES) & 1) ^ 1, p.status, kSiteAttnProducer, abort_flag))
-                        break;
+                ++kc;
+                return true;
+            };
+            auto load_v = [&](int k) -> bool {
+                const int st = vc % C::VSTAGES;
+                if (!wait(&v_empty[st], ((vc / C::VSTAGES) & 1) ^ 1, kSiteAttnProducer)) return false;
+                if (leader) {
                     mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
                     for (int c = 0; c < C::CHUNKS; ++c)
                         tma_load_3d(&tmV, &v_full[st], sV + st * C::KV_BYTES + c * (AT_BN * 128), c * 64,
-                                    (kv_begin + kv) * AT_BN, bh);
+                                    (kv_begin + k) * AT_BN, bh);
                 }
+                ++vc;
+                return true;
+            };
+            // K(0) first (its slot frees early), then the Q tiles once the previous item no
+            // longer needs them; K runs one tile ahead of V.
+            ok = load_k(0);
+            for (int t = 0; ok && t < 2; ++t) {
+                ok = wait(&q_empty[t], (n & 1) ^ 1, kSiteAttnProducerQ);
+                if (!ok) break;
+                if (leader) {
+                    mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        tma_load_3d(&tmQ, &q_full[t], sQ + t * C::Q_BYTES + c * (AT_BM * 128), c * 64,
+                                    r0 + t * AT_BM, bh);
+                }
+            }
+            for (int k = 1; ok && k <= nkv; ++k) {
+                if (k < nkv) ok = load_k(k);
+                if (ok) ok = load_v(k - 1);
             }
         }
       } else if (warp == 9) {
         // ------------------------------- MMA issuer ---------------------------------
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(AT_BM, AT_BN, 0, 0);   // Q K^T: both K-major
-            constexpr uint32_t idesc_o = idesc_f16_f32(AT_BM, DH, 0, 1);       // P V (f16): V is MN-major
-            const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-            auto issue_s = [&](int i, int st) {
-                const uint32_t d = tmem + C::s_col(i);
+        auto wait = [&](uint64_t *bar, uint32_t par, int site) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, par, p.status, site, abort_flag));
+        };
+        constexpr uint32_t idesc_s = idesc_bf16_f32(AT_BM, AT_BN, 0, 0);   // Q K^T: both K-major
+        constexpr uint32_t idesc_o = idesc_f16_f32(AT_BM, DH, 0, 1);       // P V (f16): V is MN-major
+        // descriptors as 32-bit low words (start, leading offset) + one shared high word
+        const uint32_t hi = sdesc_sw128_hi(1024);                    // 8-row groups 1 KB apart
+        const uint32_t q_lo = sdesc_sw128_lo(smem_u32(sQ), 16);      // K-major: LBO unused
+        const uint32_t k_lo = sdesc_sw128_lo(smem_u32(sK), 16);
+        const uint32_t v_lo = sdesc_sw128_lo(smem_u32(sV), AT_BN * 128);   // MN-major: 64-col chunks
+        auto issue_s = [&](int i, int st) {
+            const uint32_t d = tmem + C::s_col(i);
+            const uint32_t a = q_lo + i * (C::Q_BYTES >> 4), b = k_lo + st * (C::KV_BYTES >> 4);
 #pragma unroll
-                for (int kk = 0; kk < DH / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * (AT_BM * 128) + (kk % 4) * 32;
-                    mma_ss(d, sdesc_sw128(q_addr + i * C::Q_BYTES + off, 16, 1024),
-                           sdesc_sw128(k_addr + st * C::KV_BYTES + off, 16, 1024), idesc_s, kk > 0);
-                }
-            };
-            auto issue_pv = [&](int i, int st, bool acc) {
-                const uint32_t d = tmem + C::o_col(i);
-#pragma unroll
-                for (int kk = 0; kk < AT_BN / 16; ++kk) {
-                    // A = P (bf16 pairs in TMEM, 8 columns per 16 keys); B = 16 keys x d of V:
-                    // leading (MN) byte offset = one 64-column chunk, stride = 8 keys.
-                    mma_ts(d, tmem + C::s_col(i) + kk * 8,
-                           sdesc_sw128(v_addr + st * C::KV_BYTES + kk * 16 * 128, AT_BN * 128, 1024), idesc_o,
-                           (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-            bool ok = mbar_wait(q_full, 0, p.status, kSiteAttnMmaQ, abort_flag) &&
-                      mbar_wait(&k_full[0], 0, p.status, kSiteAttnMmaK, abort_flag);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);
-                mma_commit(&s_full[0]);
-                issue_s(1, 0);
-                mma_commit(&s_full[1]);
-                mma_commit(&k_empty[0]);
+            for (int kk = 0; kk < DH / 16; ++kk) {
+                const uint32_t off = ((kk / 4) * (AT_BM * 128) + (kk % 4) * 32) >> 4;
+                mma_ss_w(d, a + off, b + off, hi, idesc_s, kk > 0);
             }
-            for (int k = 0; ok && k < nkv; ++k) {
-                const int vst = k % C::VSTAGES;
-                const int kst2 = (k + 1) % C::KSTAGES;
+        };
+        auto issue_pv = [&](int i, int st, bool acc) {
+            const uint32_t d = tmem + C::o_col(i);
+            const uint32_t b = v_lo + st * (C::KV_BYTES >> 4);
+#pragma unroll
+            for (int kk = 0; kk < AT_BN / 16; ++kk) {
+                // A = P (f16 pairs in TMEM, 8 columns per 16 keys); B = 16 keys x d of V:
+                // leading (MN) byte offset = one 64-column chunk, stride = 8 keys.
+                mma_ts_w(d, tmem + C::s_col(i) + kk * 8, b + ((kk * 16 * 128) >> 4), hi, idesc_o,
+                         (acc || kk > 0) ? 1u : 0u);
+            }
+        };
+        // After the last S-MMA of Q tile i the tile's shared memory may be refilled, unless
+        // the epilogue stages O there (then the epilogue releases it).
+        auto release_q = [&](int i) {
+            if (!p.stage_o) mma_commit(&q_empty[i]);
+        };
+        int kc = 0, vc = 0, sc = 0;   // K, V tiles consumed; S tiles per Q tile so far
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            const int slot = n % AT_ITEM_SLOTS;
+            ok = wait(&item_full[slot], (n / AT_ITEM_SLOTS) & 1, kSiteAttnItem);
+            if (!ok) break;
+            const int nkv = item_slot[slot].nkv;
+            const bool last = item_slot[slot].bh < 0;
+            __syncwarp();
+            if (leader) mbar_arrive(&item_empty[slot]);
+            if (last) break;
+            {
+                const int st = kc % C::KSTAGES;
+                ok = wait(&q_full[0], n & 1, kSiteAttnMmaQ) &&
+                     wait(&k_full[st], (kc / C::KSTAGES) & 1, kSiteAttnMmaK);
+                if (!ok) break;
+                tc_fence_after();
+                if (leader) {
+                    issue_s(0, st);
+                    mma_commit(&s_full[0]);
+                    if (nkv == 1) release_q(0);
+                }
+                ok = wait(&q_full[1], n & 1, kSiteAttnMmaQ);
+                if (!ok) break;
+                tc_fence_after();
+                if (leader) {
+                    issue_s(1, st);
+                    mma_commit(&s_full[1]);
+                    if (nkv == 1) release_q(1);
+                    mma_commit(&k_empty[st]);
+                }
+                ++kc;
+            }
+            for (int k = 0; k < nkv; ++k) {
+                const int vst = vc % C::VSTAGES;
+                const uint32_t vph = (vc / C::VSTAGES) & 1;
+                const int kst = kc % C::KSTAGES;
+                const uint32_t kph = (kc / C::KSTAGES) & 1;
+                const uint32_t pph = (sc + k) & 1;
                 const bool more = k + 1 < nkv;
                 // tile 0: O0 += P0 V(k), then S0(k+1)
-                ok = mbar_wait(&p_full[0], k & 1, p.status, kSiteAttnMmaP, abort_flag) &&
-                     mbar_wait(&v_full[vst], (k / C::VSTAGES) & 1, p.status, kSiteAttnMmaV, abort_flag);
+                ok = wait(&p_full[0], pph, kSiteAttnMmaP) && wait(&v_full[vst], vph, kSiteAttnMmaV);
+                if (ok && k == 0)   // the previous item's epilogue has read O0
+                    ok = wait(&o_empty[0], (n & 1) ^ 1, kSiteAttnMmaO);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(0, vst, k > 0);
+                if (leader) {
+                    issue_pv(0, vst, k > 0);
+                    if (!more) mma_commit(&o_full[0]);
+                }
                 if (more) {
-                    ok = mbar_wait(&k_full[kst2], ((k + 1) / C::KSTAGES) & 1, p.status, kSiteAttnMmaK, abort_flag);
+                    ok = wait(&k_full[kst], kph, kSiteAttnMmaK);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(0, kst2);
-                    mma_commit(&s_full[0]);
+                    if (leader) {
+                        issue_s(0, kst);
+                        mma_commit(&s_full[0]);
+                        if (k + 2 == nkv) release_q(0);
+                    }
                 }
                 // tile 1: O1 += P1 V(k) (then V(k) is free), S1(k+1) (then K(k+1) is free)
-                ok = mbar_wait(&p_full[1], k & 1, p.status, kSiteAttnMmaP, abort_flag);
+                ok = wait(&p_full[1], pph, kSiteAttnMmaP);
+                if (ok && k == 0) ok = wait(&o_empty[1], (n & 1) ^ 1, kSiteAttnMmaO);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(1, vst, k > 0);
-                mma_commit(&v_empty[vst]);
-                if (more) {
-                    issue_s(1, kst2);
-                    mma_commit(&s_full[1]);
-                    mma_commit(&k_empty[kst2]);
+                if (leader) {
+                    issue_pv(1, vst, k > 0);
+                    mma_commit(&v_empty[vst]);
+                    if (!more) mma_commit(&o_full[1]);
+                    if (more) {
+                        issue_s(1, kst);
+                        mma_commit(&s_full[1]);
+                        if (k + 2 == nkv) release_q(1);
+                        mma_commit(&k_empty[kst]);
+                    }
                 }
+                ++vc;
+                if (more) ++kc;
             }
-            mma_commit(o_full);
+            sc += nkv;
         }
       }
     } else {
@@ -273,134 +407,187 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const int tile = warp >> 2;           // 0: rows [r0, r0+128), 1: [r0+128, r0+256)
         const int q = warp & 3;               // TMEM lane quarter
         const int row = q * 32 + lane;
-        const long long r = r0 + tile * AT_BM + row;
         const uint32_t lane_addr = uint32_t(q * 32) << 16;
         const uint32_t s_col = tmem + lane_addr + C::s_col(tile);
         const uint32_t o_col = tmem + lane_addr + C::o_col(tile);
-        long long lo, hi;
-        key_interval(p, r, lo, hi);
         const float sl2 = p.scale_log2;
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int k = 0; k < nkv; ++k) {
-            if (!mbar_wait(&s_full[tile], k & 1, p.status, kSiteAttnSoftmax, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float s[AT_BN];
-#pragma unroll
-            for (int c = 0; c < AT_BN / 32; ++c) {
-                uint32_t u[32];
-                tmem_ld32(s_col + c * 32, u);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
-            }
-            tmem_ld_wait();
-            // mask columns outside [lo, hi] (only when some row of the warp needs it)
-            {
-                const long long kr0 = (long long)(kv_begin + k) * AT_BN;
-                const bool need_mask = (kr0 < lo) || (kr0 + AT_BN - 1 > hi);
-                if (__any_sync(0xffffffffu, need_mask)) {
-                    const long long a = lo - kr0, b = hi - kr0;
-#pragma unroll
-                    for (int c = 0; c < AT_BN; ++c)
-                        if (c < a || c > b) s[c] = -INFINITY;
+        const bool issuer = q == 0 && lane == 0;   // sends the staged tile
+        int sc = 0;
+        for (int n = 0;; ++n) {
+            const int slot = n % AT_ITEM_SLOTS;
+            const bool got = mbar_wait(&item_full[slot], (n / AT_ITEM_SLOTS) & 1, p.status, kSiteAttnItem, abort_flag);
+            AttnItem it{-1, 0, 0, 0};
+            if (got) it = item_slot[slot];
+            __syncwarp();
+            if (lane == 0 && got) mbar_arrive(&item_empty[slot]);
+            // leave together (the epilogue has a warpgroup barrier); all read the same slot
+            if (named_bar_or(1 + tile, 128, !got) || it.bh < 0) break;
+            const int nkv = it.nkv;
+            const int r = it.qb * 2 * AT_BM + tile * AT_BM + row;
+            // readable key rows of this thread's row, relative to the item's first KV tile
+            int lo_rel, hi_rel;
+            key_interval(p, r, lo_rel, hi_rel);
+            lo_rel -= it.kv_begin * AT_BN;
+            hi_rel -= it.kv_begin * AT_BN;
+            float m_run = -INFINITY, l_run = 0.f;
+            bool ok = true;
+            for (int k = 0; k < nkv; ++k) {
+                if (!mbar_wait(&s_full[tile], (sc + k) & 1, p.status, kSiteAttnSoftmax, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-            }
-            // row max: 8 independent chains of 3-input max, then a tree (max is exact)
-            float mx[8];
+                tc_fence_after();
+                float s[AT_BN];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = s[i];
+                for (int c = 0; c < AT_BN / 32; ++c) {
+                    uint32_t u[32];
+                    tmem_ld32(s_col + c * 32, u);
 #pragma unroll
-            for (int c = 8; c < AT_BN; c += 16)
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
+                }
+                tmem_ld_wait();
+                // mask columns outside [lo, hi] (only when some row of the warp needs it)
+                {
+                    const int a = lo_rel - k * AT_BN, b = hi_rel - k * AT_BN;
+                    const bool need_mask = a > 0 || b < AT_BN - 1;
+                    if (__any_sync(0xffffffffu, need_mask)) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
-            const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
-            const float m_cand = mt * sl2;
-            const bool raise = m_cand > m_run + AT_RESCALE_THRESHOLD;
-            float factor = 1.f;
-            if (raise) {
-                factor = fast_exp2(m_run - m_cand);   // m_run = -inf -> 0
-                l_run *= factor;
-                m_run = m_cand;
-            }
-            if (k > 0 && __any_sync(0xffffffffu, raise)) {
-                // O (previous tiles) is complete: S(k) was issued after PV(k-1)
+                        for (int c = 0; c < AT_BN; ++c)
+                            if (c < a || c > b) s[c] = -INFINITY;
+                    }
+                }
+                // row max: 8 independent chains of 3-input max, then a tree (max is exact)
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+                for (int c = 8; c < AT_BN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+                const float mt =
+                    fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+                const float m_cand = mt * sl2;
+                const bool raise = m_cand > m_run + AT_RESCALE_THRESHOLD;
+                float factor = 1.f;
+                if (raise) {
+                    factor = fast_exp2(m_run - m_cand);   // m_run = -inf -> 0
+                    l_run *= factor;
+                    m_run = m_cand;
+                }
+                const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+                // p = 2^(s * log2(e)/sqrt(d) - m): the exponent by a packed fp32x2 FMA, rounded
+                // to f16x2, then one ex2.f16x2 per pair.  P goes to TMEM as f16 (the PV
+                // product is f16).
+                uint32_t pk[AT_BN / 64][32];
+#pragma unroll
+                for (int c = 0; c < AT_BN / 64; ++c) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x0, x1;
+                        ffma2(x0, x1, s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1], sl2, sl2, -mu, -mu);
+                        pk[c][i] = ex2_f16x2(pack_f16x2(x0, x1));
+                    }
+                    tmem_st32(s_col + c * 32, pk[c]);
+                }
+                tmem_st_wait();
+                if (k > 0 && __any_sync(0xffffffffu, raise)) {
+                    // O (previous tiles) is complete: S(k) was issued after PV(k-1); PV(k)
+                    // waits for p_full.  Done here, after S is dead, to keep registers free.
 #pragma unroll 1
+                    for (int c = 0; c < DH / 32; ++c) {
+                        uint32_t u[32];
+                        tmem_ld32(o_col + c * 32, u);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * factor);
+                        tmem_st32(o_col + c * 32, u);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[tile]);
+                // row sum off the critical path (the MMA warp already has P).  Each p <= 2^8
+                // (threshold rule), so an f16 partial over 16 values stays below 2^12.
+                uint32_t hs[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(pk[0][i], pk[0][i + 8]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(hs[i], hadd2_f16(pk[0][i + 16], pk[0][i + 24]));
+                float lsum = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) lsum += f16x2_sum_to_f32(hs[i]);
+#pragma unroll
+                for (int c = 1; c < AT_BN / 64; ++c) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(pk[c][i], pk[c][i + 8]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(hs[i], hadd2_f16(pk[c][i + 16], pk[c][i + 24]));
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) lsum += f16x2_sum_to_f32(hs[i]);
+                }
+                l_run += lsum;
+            }
+            sc += nkv;
+            // ------------------------------- epilogue -------------------------------
+            // O / l -> packed bf16 in registers; then O_tile is free for the next item's first
+            // PV-MMA.
+            const bool have = ok && mbar_wait(&o_full[tile], n & 1, p.status, kSiteAttnEpilogue, abort_flag);
+            uint32_t ob[DH / 2];   // bf16 pairs of this row
+            if (have) {
+                tc_fence_after();
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
                 for (int c = 0; c < DH / 32; ++c) {
                     uint32_t u[32];
                     tmem_ld32(o_col + c * 32, u);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * factor);
-                    tmem_st32(o_col + c * 32, u);
-                }
-            }
-            const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-            // p = 2^(s * log2(e)/sqrt(d) - m): the exponent by a packed fp32x2 FMA, rounded to
-            // f16x2, then one ex2.f16x2 per pair.  P goes to TMEM as f16 (the PV product is f16).
-            uint32_t pk[AT_BN / 64][32];
-#pragma unroll
-            for (int c = 0; c < AT_BN / 64; ++c) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float x0, x1;
-                    ffma2(x0, x1, s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1], sl2, sl2, -mu, -mu);
-                    pk[c][i] = ex2_f16x2(pack_f16x2(x0, x1));
-                }
-                tmem_st32(s_col + c * 32, pk[c]);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[tile]);
-            // row sum off the critical path (the MMA warp already has P).  Each p <= 2^8
-            // (threshold rule), so an f16 partial over 16 values stays below 2^12.
-            uint32_t hs[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(pk[0][i], pk[0][i + 8]);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(hs[i], hadd2_f16(pk[0][i + 16], pk[0][i + 24]));
-            float lsum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) lsum += f16x2_sum_to_f32(hs[i]);
-#pragma unroll
-            for (int c = 1; c < AT_BN / 64; ++c) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(pk[c][i], pk[c][i + 8]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) hs[i] = hadd2_f16(hs[i], hadd2_f16(pk[c][i + 16], pk[c][i + 24]));
-#pragma unroll
-                for (int i = 0; i < 8; ++i) lsum += f16x2_sum_to_f32(hs[i]);
-            }
-            l_run += lsum;
-        }
-        // ------------------------------- epilogue -----------------------------------
-        if (ok && mbar_wait(o_full, 0, p.status, kSiteAttnEpilogue, abort_flag)) {
-            tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            const bool row_ok = r < p.L;
-            const long long t = r / p.P, j = r % p.P;
-            const long long b = bh / p.H, h = bh % p.H;
-            __nv_bfloat16 *dst = p.pbar + (((b * p.N + t) * p.H + h) * p.P + j) * DH;
-#pragma unroll 1
-            for (int c = 0; c < DH / 32; ++c) {
-                uint32_t u[32];
-                tmem_ld32(o_col + c * 32, u);
-                tmem_ld_wait();
-                if (row_ok) {
-                    uint4 v[4];
-                    uint32_t *vw = reinterpret_cast<uint32_t *>(v);
-#pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        vw[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+                        ob[c * 16 + i] = pack_bf16x2(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
+                }
+                tc_fence_before();
+                mbar_arrive(&o_empty[tile]);
+            }
+            const int b = it.bh / p.H, h = it.bh % p.H;
+            if (p.stage_o) {
+                // all S-MMAs of this item (the readers of Q_tile) completed before o_full, and
+                // the next Q_tile waits for q_empty: stage the tile there (128B swizzle)
+                uint8_t *stg = sQ + tile * C::Q_BYTES;
+                if (have) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) d4[i] = v[i];
+                    for (int unit = 0; unit < DH / 8; ++unit) {
+                        // 64-column chunk unit/8, 16-byte unit unit%8 of this row, swizzled
+                        *reinterpret_cast<uint4 *>(stg + (unit / 8) * (AT_BM * 128) + row * 128 +
+                                                   (((unit & 7) ^ (row & 7)) << 4)) =
+                            make_uint4(ob[4 * unit], ob[4 * unit + 1], ob[4 * unit + 2], ob[4 * unit + 3]);
+                    }
+                    fence_proxy_async_smem();   // the staging writes before the TMA store reads them
+                }
+                if (named_bar_or(1 + tile, 128, !have)) break;   // the warpgroup decides together
+                if (issuer) {
+                    const int rt0 = it.qb * 2 * AT_BM + tile * AT_BM;
+                    if (rt0 < p.L) {
+                        // rows rt0 .. rt0+127 = tokens rt0/P .. with all P pseudo-heads; tokens >= N clip
+                        for (int c = 0; c < C::CHUNKS; ++c)
+                            tma_store_5d(&tmO, stg + c * (AT_BM * 128), c * 64, 0, h, rt0 / p.P, b);
+                        bulk_commit();
+                        bulk_wait_read(0);
+                    }
+                    mbar_arrive(&q_empty[tile]);
+                }
+            } else {
+                if (!have) break;
+                if (r < p.L) {
+                    const long long t = r / p.P, j = r % p.P;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.pbar + ((((long long)b * p.N + t) * p.H + h) * p.P + j) * DH);
+#pragma unroll
+                    for (int unit = 0; unit < DH / 8; ++unit)
+                        dst[unit] = make_uint4(ob[4 * unit], ob[4 * unit + 1], ob[4 * unit + 2], ob[4 * unit + 3]);
                 }
             }
         }
+        if (p.stage_o && issuer) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -412,6 +599,18 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 
 cudaError_t launch_attention_f32(const void *QKV, const Shape &sh, int mask_mode, int window, void *Pbar,
                                  cudaStream_t st);
+
+// A work counter for one launch, set to 0 on the launch's stream.  Launches take the
+// AT_TICKETS counters in turn, so up to AT_TICKETS launches may run at once.
+static unsigned int *attn_ticket(cudaStream_t st, cudaError_t &e) {
+    static std::atomic<unsigned> next{0};
+    unsigned int *base = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void **>(&base), g_attn_tickets);
+    if (e != cudaSuccess) return nullptr;
+    unsigned int *t = base + next.fetch_add(1u) % AT_TICKETS;
+    e = cudaMemsetAsync(t, 0, sizeof(unsigned int), st);
+    return e == cudaSuccess ? t : nullptr;
+}
 
 template <int DH>
 static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mode, int window, void *Pbar,
@@ -428,6 +627,18 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
         if (!make_tmap_bf16(&tm[s], base + s * sstride, 3, dims, strides, box, /*f16=*/s == 2))
             return cudaErrorInvalidValue;
     }
+    // Pbar [B][N][H][P][d] as (c, j, h, t, b); a box = 128/P whole tokens of one head
+    CUtensorMap tmO;
+    bool stage_o = 128 % sh.P == 0 && (reinterpret_cast<uintptr_t>(Pbar) & 15) == 0;
+    if (stage_o) {
+        const uint64_t dims[5] = {(uint64_t)DH, (uint64_t)sh.P, (uint64_t)sh.H, (uint64_t)sh.N, (uint64_t)sh.B};
+        const uint64_t strides[4] = {(uint64_t)DH * 2, (uint64_t)sh.P * DH * 2, (uint64_t)sh.H * sh.P * DH * 2,
+                                     (uint64_t)sh.N * sh.H * sh.P * DH * 2};
+        const uint32_t box[5] = {64, (uint32_t)sh.P, 1, (uint32_t)(AT_BM / sh.P), 1};
+        if (!make_tmap_bf16(&tmO, Pbar, 5, dims, strides, box)) return cudaErrorInvalidValue;
+    } else {
+        tmO = tm[0];   // unused
+    }
     AttnParams p;
     p.pbar = (__nv_bfloat16 *)Pbar;
     p.N = sh.N;
@@ -438,6 +649,7 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     p.window = window;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
     p.num_qblocks = (int)((L + 2 * AT_BM - 1) / (2 * AT_BM));
+    p.stage_o = stage_o ? 1 : 0;
     p.status = status;
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
@@ -452,8 +664,12 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
         long long g = (48LL << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
         p.head_group = (int)(g < 1 ? 1 : (g > BH ? BH : g));
     }
-    const unsigned grid = (unsigned)(BH * p.num_qblocks);
-    attn_fwd_tc<DH><<<grid, AT_THREADS, C::SMEM, st>>>(tm[0], tm[1], tm[2], p);
+    // persistent: one CTA per SM, each looping over work items
+    const long long items = BH * p.num_qblocks;
+    const unsigned grid = (unsigned)(items < device_sm_count() ? items : device_sm_count());
+    p.ticket = attn_ticket(st, e);
+    if (!p.ticket) return e;
+    attn_fwd_tc<DH><<<grid, AT_THREADS, C::SMEM, st>>>(tm[0], tm[1], tm[2], tmO, p);
     return cudaGetLastError();
 }
 

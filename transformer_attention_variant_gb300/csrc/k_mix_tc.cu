@@ -1,6 +1,5 @@
 // k_mix_tc.cu -- pseudo-head mixing ("Interleaved Head Attention" section 4, Algorithm 1,
-// the pseudo-query/key/value step) on the unfolded route, as the small dense contraction
-// it is:
+// step "偽頭混合") on the unfolded route, as the small dense contraction it is:
 //
 //     S~_s[t][(h,j)][c] = sum_m alpha_s[m][h][j] * Y_s[t][m][c],   s in {Q, K, V},
 //
