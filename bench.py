@@ -456,7 +456,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=gi.WORKLOAD_ORDER)
-    ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=768, help="oracle sample size for cpu_baseline (about 10-15 s)")
     ap.add_argument("--ref-tokens", type=int, default=48, help="oracle sample size per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")

@@ -211,7 +211,10 @@ IHA_API int iha_mix_heads(const void *Y, const float *alpha_Q, const float *alph
                           int B, int N, int H, int d, int P, int dtype, void *QKV, void *stream);
 
 /* Step 3: masked softmax attention over each head's stacked sequence.
- * QKV as written by iha_project; Pbar [B][N][H][P][d]. */
+ * QKV as written by iha_project; Pbar [B][N][H][P][d].  For bf16 each call takes one of
+ * 1024 device work counters in turn (zeroed on `stream` before the kernel), so at most 1024
+ * calls may be executing or queued on different streams at once; calls on one stream are
+ * ordered and never collide. */
 IHA_API int iha_attention(const void *QKV, int B, int N, int H, int d, int P,
                   int mask_mode, int window, int dtype, void *Pbar, void *stream);
 
