@@ -27,6 +27,9 @@ enum WaitSite {
     kSiteMixProducer = 31,
     kSiteMixMma = 32,
     kSiteMixEpilogue = 33,
+    kSiteContractProducer = 34,
+    kSiteContractMma = 35,
+    kSiteContractEpilogue = 36,
     kSiteSelfTest = 99,
 };
 
@@ -68,8 +71,12 @@ cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, in
 cudaError_t launch_contract(const void *Pbar, const float *R, const Shape &sh, int dtype, void *out,
                             cudaStream_t st, int *status);
 
-// The bf16 contraction (TMA-fed row mixing) when its 3-stage ring fits in shared memory;
-// otherwise, and for fp32, a SIMT kernel.
+// The bf16 contraction on tensor cores (d in {64, 128}, H <= 16, H*P <= 128); else the
+// TMA-fed row mixing when its 3-stage ring fits in shared memory; otherwise, and for fp32,
+// a SIMT kernel.
+bool contract_tc_fits(const Shape &sh);
+cudaError_t launch_contract_tc(const void *Pbar, const float *R, const Shape &sh, void *out, cudaStream_t st,
+                               int *status);
 bool contract_rowmix_fits(const Shape &sh);
 cudaError_t launch_contract_rowmix(const void *Pbar, const float *R, const Shape &sh, void *out, cudaStream_t st,
                                    int *status);

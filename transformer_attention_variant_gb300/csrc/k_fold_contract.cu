@@ -222,6 +222,8 @@ static cudaError_t launch_contract_t(const void *Pbar, const float *R, const Sha
 cudaError_t launch_contract(const void *Pbar, const float *R, const Shape &sh, int dtype, void *out,
                             cudaStream_t st, int *status) {
     if (dtype == 1) {
+        if (contract_tc_fits(sh) && (reinterpret_cast<uintptr_t>(out) & 15) == 0)
+            return launch_contract_tc(Pbar, R, sh, out, st, status);
         if (contract_rowmix_fits(sh)) return launch_contract_rowmix(Pbar, R, sh, out, st, status);
         return launch_contract_t<__nv_bfloat16, 8>(Pbar, R, sh, out, st);
     }
