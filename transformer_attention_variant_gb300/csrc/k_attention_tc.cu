@@ -71,7 +71,7 @@ struct AttnCfg {
     static constexpr int NBARS = 12 + 2 * (KSTAGES + VSTAGES) + 2 * AT_ITEM_SLOTS;
     static constexpr int CTRL_BYTES = 512;   // barriers, item slots, TMEM address, abort flag
     static constexpr int SMEM = 2 * Q_BYTES + (KSTAGES + VSTAGES) * KV_BYTES + CTRL_BYTES + 1024;
-    static_assert(NBARS * 8 + AT_ITEM_SLOTS * 16 + 8 <= CTRL_BYTES, "control area");
+    static_assert(NBARS * 8 + AT_ITEM_SLOTS * 24 + 8 <= CTRL_BYTES, "control area");
     __device__ static constexpr uint32_t s_col(int i) { return uint32_t(i) * 128u; }
     __device__ static constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * DH; }
 };
@@ -126,19 +126,26 @@ __device__ unsigned int g_attn_tickets[AT_TICKETS];
 
 // A work item as the TMA warp hands it on: head bh, rows [qb*256, qb*256 + 256), and the
 // KV tiles [kv_begin, kv_begin + nkv) those rows need (the union of their readable
-// intervals).  bh < 0 ends the CTA's work.
+// intervals).  Relative to kv_begin, Q tile 0 needs tiles [0, e0] and Q tile 1 tiles
+// [b1, nkv - 1]; the two ranges overlap or touch (b1 <= e0 + 1), so every loaded tile has a
+// reader, and each Q tile skips the tiles where all of its rows are masked.  Rows past the
+// end of the sequence take the range of its last row.  bh < 0 ends the CTA's work.
 struct AttnItem {
-    int bh, qb, kv_begin, nkv;
+    int bh, qb, kv_begin, nkv, e0, b1;
 };
 __device__ __forceinline__ AttnItem make_item(const AttnParams &p, long long i) {
     AttnItem it;
     item_coords(p, i, it.bh, it.qb);
-    const int r0 = it.qb * 2 * AT_BM, r_last = min(r0 + 2 * AT_BM - 1, p.L - 1);
-    int lo_first, hi_first, lo_last, hi_last;
-    key_interval(p, r0, lo_first, hi_first);
-    key_interval(p, r_last, lo_last, hi_last);
-    it.kv_begin = lo_first / AT_BN;
-    it.nkv = hi_last / AT_BN - it.kv_begin + 1;
+    const int r0 = it.qb * 2 * AT_BM;
+    int lo_a, hi_a, lo_b, hi_b, lo_c, hi_c, lo_d, hi_d;
+    key_interval(p, min(r0, p.L - 1), lo_a, hi_a);
+    key_interval(p, min(r0 + AT_BM - 1, p.L - 1), lo_b, hi_b);
+    key_interval(p, min(r0 + AT_BM, p.L - 1), lo_c, hi_c);
+    key_interval(p, min(r0 + 2 * AT_BM - 1, p.L - 1), lo_d, hi_d);
+    it.kv_begin = lo_a / AT_BN;
+    it.nkv = hi_d / AT_BN - it.kv_begin + 1;
+    it.e0 = hi_b / AT_BN - it.kv_begin;
+    it.b1 = lo_c / AT_BN - it.kv_begin;
     return it;
 }
 
@@ -231,7 +238,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             unsigned int ticket = 0;
             if (leader) ticket = atomicAdd(p.ticket, 1u);
             ticket = __shfl_sync(0xffffffffu, ticket, __ffs(__ballot_sync(0xffffffffu, leader)) - 1);
-            AttnItem it{-1, 0, 0, 0};
+            AttnItem it{-1, 0, 0, 0, 0, 0};
             if (ticket < num_items) it = make_item(p, ticket);
             if (leader) {
                 item_slot[slot] = it;
@@ -319,17 +326,19 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         auto release_q = [&](int i) {
             if (!p.stage_o) mma_commit(&q_empty[i]);
         };
-        int kc = 0, vc = 0, sc = 0;   // K, V tiles consumed; S tiles per Q tile so far
+        int kc = 0, vc = 0;             // K and V tiles consumed (ring positions)
+        int sc0 = 0, sc1 = 0;           // S tiles issued so far for Q tile 0 / 1
         bool ok = true;
         for (int n = 0; ok; ++n) {
             const int slot = n % AT_ITEM_SLOTS;
             ok = wait(&item_full[slot], (n / AT_ITEM_SLOTS) & 1, kSiteAttnItem);
             if (!ok) break;
-            const int nkv = item_slot[slot].nkv;
+            const int nkv = item_slot[slot].nkv, e0 = item_slot[slot].e0, b1 = item_slot[slot].b1;
             const bool last = item_slot[slot].bh < 0;
             __syncwarp();
             if (leader) mbar_arrive(&item_empty[slot]);
             if (last) break;
+            // K(0): S0(0), and S1(0) when tile 1 starts there
             {
                 const int st = kc % C::KSTAGES;
                 ok = wait(&q_full[0], n & 1, kSiteAttnMmaQ) &&
@@ -339,66 +348,82 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 if (leader) {
                     issue_s(0, st);
                     mma_commit(&s_full[0]);
-                    if (nkv == 1) release_q(0);
+                    if (e0 == 0) release_q(0);
                 }
-                ok = wait(&q_full[1], n & 1, kSiteAttnMmaQ);
-                if (!ok) break;
-                tc_fence_after();
-                if (leader) {
-                    issue_s(1, st);
-                    mma_commit(&s_full[1]);
-                    if (nkv == 1) release_q(1);
-                    mma_commit(&k_empty[st]);
+                if (b1 == 0) {
+                    ok = wait(&q_full[1], n & 1, kSiteAttnMmaQ);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (leader) {
+                        issue_s(1, st);
+                        mma_commit(&s_full[1]);
+                        if (nkv == 1) release_q(1);
+                    }
                 }
+                if (leader) mma_commit(&k_empty[st]);
                 ++kc;
             }
+            // Iteration k: PV0(k), S0(k+1), PV1(k), S1(k+1), each only where the tile needs
+            // KV tile k (k+1); a ring slot is released after its last reader.
             for (int k = 0; k < nkv; ++k) {
                 const int vst = vc % C::VSTAGES;
                 const uint32_t vph = (vc / C::VSTAGES) & 1;
                 const int kst = kc % C::KSTAGES;
                 const uint32_t kph = (kc / C::KSTAGES) & 1;
-                const uint32_t pph = (sc + k) & 1;
-                const bool more = k + 1 < nkv;
-                // tile 0: O0 += P0 V(k), then S0(k+1)
-                ok = wait(&p_full[0], pph, kSiteAttnMmaP) && wait(&v_full[vst], vph, kSiteAttnMmaV);
-                if (ok && k == 0)   // the previous item's epilogue has read O0
-                    ok = wait(&o_empty[0], (n & 1) ^ 1, kSiteAttnMmaO);
-                if (!ok) break;
-                tc_fence_after();
-                if (leader) {
-                    issue_pv(0, vst, k > 0);
-                    if (!more) mma_commit(&o_full[0]);
+                const bool pv0 = k <= e0, pv1 = k >= b1;
+                const bool s0 = k + 1 <= e0, s1 = k + 1 < nkv && k + 1 >= b1;
+                if (pv0) {   // tile 0: O0 += P0 V(k)
+                    ok = wait(&p_full[0], (sc0 + k) & 1, kSiteAttnMmaP) && wait(&v_full[vst], vph, kSiteAttnMmaV);
+                    if (ok && k == 0)   // the previous item's epilogue has read O0
+                        ok = wait(&o_empty[0], (n & 1) ^ 1, kSiteAttnMmaO);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (leader) {
+                        issue_pv(0, vst, k > 0);
+                        if (k == e0) mma_commit(&o_full[0]);
+                        if (!pv1) mma_commit(&v_empty[vst]);
+                    }
                 }
-                if (more) {
+                if (s0) {    // S0(k+1)
                     ok = wait(&k_full[kst], kph, kSiteAttnMmaK);
                     if (!ok) break;
                     tc_fence_after();
                     if (leader) {
                         issue_s(0, kst);
                         mma_commit(&s_full[0]);
-                        if (k + 2 == nkv) release_q(0);
+                        if (k + 1 == e0) release_q(0);
+                        if (!s1) mma_commit(&k_empty[kst]);
                     }
                 }
-                // tile 1: O1 += P1 V(k) (then V(k) is free), S1(k+1) (then K(k+1) is free)
-                ok = wait(&p_full[1], pph, kSiteAttnMmaP);
-                if (ok && k == 0) ok = wait(&o_empty[1], (n & 1) ^ 1, kSiteAttnMmaO);
-                if (!ok) break;
-                tc_fence_after();
-                if (leader) {
-                    issue_pv(1, vst, k > 0);
-                    mma_commit(&v_empty[vst]);
-                    if (!more) mma_commit(&o_full[1]);
-                    if (more) {
-                        issue_s(1, kst);
-                        mma_commit(&s_full[1]);
-                        if (k + 2 == nkv) release_q(1);
-                        mma_commit(&k_empty[kst]);
+                if (pv1) {   // tile 1: O1 += P1 V(k)
+                    ok = wait(&p_full[1], (sc1 + k - b1) & 1, kSiteAttnMmaP);
+                    if (ok && !pv0) ok = wait(&v_full[vst], vph, kSiteAttnMmaV);
+                    if (ok && k == b1) ok = wait(&o_empty[1], (n & 1) ^ 1, kSiteAttnMmaO);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (leader) {
+                        issue_pv(1, vst, k > b1);
+                        mma_commit(&v_empty[vst]);
+                        if (k == nkv - 1) mma_commit(&o_full[1]);
                     }
                 }
                 ++vc;
-                if (more) ++kc;
+                if (s1) {    // S1(k+1)
+                    if (!s0) ok = wait(&k_full[kst], kph, kSiteAttnMmaK);
+                    if (ok && k + 1 == b1) ok = wait(&q_full[1], n & 1, kSiteAttnMmaQ);   // tile 1's first S
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (leader) {
+                        issue_s(1, kst);
+                        mma_commit(&s_full[1]);
+                        if (k + 1 == nkv - 1) release_q(1);
+                        mma_commit(&k_empty[kst]);
+                    }
+                }
+                if (s0 || s1) ++kc;
             }
-            sc += nkv;
+            sc0 += e0 + 1;
+            sc1 += nkv - b1;
         }
       }
     } else {
@@ -416,19 +441,21 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int n = 0;; ++n) {
             const int slot = n % AT_ITEM_SLOTS;
             const bool got = mbar_wait(&item_full[slot], (n / AT_ITEM_SLOTS) & 1, p.status, kSiteAttnItem, abort_flag);
-            AttnItem it{-1, 0, 0, 0};
+            AttnItem it{-1, 0, 0, 0, 0, 0};
             if (got) it = item_slot[slot];
             __syncwarp();
             if (lane == 0 && got) mbar_arrive(&item_empty[slot]);
             // leave together (the epilogue has a warpgroup barrier); all read the same slot
             if (named_bar_or(1 + tile, 128, !got) || it.bh < 0) break;
-            const int nkv = it.nkv;
+            // this Q tile's KV tiles: [kv_begin + base, kv_begin + base + nkv)
+            const int base = tile == 0 ? 0 : it.b1;
+            const int nkv = tile == 0 ? it.e0 + 1 : it.nkv - it.b1;
             const int r = it.qb * 2 * AT_BM + tile * AT_BM + row;
-            // readable key rows of this thread's row, relative to the item's first KV tile
+            // readable key rows of this thread's row, relative to the tile's first KV tile
             int lo_rel, hi_rel;
-            key_interval(p, r, lo_rel, hi_rel);
-            lo_rel -= it.kv_begin * AT_BN;
-            hi_rel -= it.kv_begin * AT_BN;
+            key_interval(p, min(r, p.L - 1), lo_rel, hi_rel);
+            lo_rel -= (it.kv_begin + base) * AT_BN;
+            hi_rel -= (it.kv_begin + base) * AT_BN;
             float m_run = -INFINITY, l_run = 0.f;
             bool ok = true;
             for (int k = 0; k < nkv; ++k) {
