@@ -688,7 +688,9 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     p.num_heads = (int)BH;
     {
         const long long kv_bytes_per_head = 2LL * L * DH * 2;   // K and V of one (b, h)
-        long long g = (48LL << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
+        // 64 MB of the 129 MB L2 per group: measured best of 24..128 MB on causal and windowed
+        // workloads (causal P=4: 2.90 ms at 64 MB, 2.99 ms at 48 MB)
+        long long g = (64LL << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
         p.head_group = (int)(g < 1 ? 1 : (g > BH ? BH : g));
     }
     // persistent: one CTA per SM, each looping over work items
