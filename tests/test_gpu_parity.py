@@ -101,6 +101,14 @@ EDGE = [
     W("h1_narrow_gemm", B=3, N=130, H=1, d=64, P=1, mask_mode=C, window=0, dtype="bf16", seed=30),
     W("multi_tile_window", B=1, N=1000, H=2, d=128, P=2, mask_mode=WN, window=300, dtype="bf16", seed=31),
     W("p4_causal_d64", B=2, N=200, H=4, d=64, P=4, mask_mode=C, window=0, dtype="bf16", seed=32),
+    # tile shapes of the mixing and contraction kernels: H*P = 128 (one token group per
+    # tile), 65..127 (padded K, one group, P not dividing 128), 64 with d = 64, H > 16 (folded
+    # route, row-mixing contraction; H = 20, d = 128 is the pages' model shape), ragged tokens
+    W("hp128_p8", B=1, N=160, H=16, d=128, P=8, mask_mode=C, window=0, dtype="bf16", seed=36),
+    W("hp80_p5_window", B=2, N=77, H=16, d=64, P=5, mask_mode=WN, window=9, dtype="bf16", seed=37),
+    W("h20_folded", B=1, N=96, H=20, d=128, P=2, mask_mode=C, window=0, dtype="bf16", seed=38),
+    W("h16_d64_p4", B=1, N=300, H=16, d=64, P=4, mask_mode=C, window=0, dtype="bf16", seed=39),
+    W("h12_ragged_window", B=3, N=111, H=12, d=128, P=2, mask_mode=WN, window=50, dtype="bf16", seed=40),
     W("f32_odd_d", B=2, N=37, H=3, d=17, P=3, mask_mode=C, window=0, dtype="f32", seed=33),
     W("f32_window", B=1, N=50, H=2, d=40, P=2, mask_mode=WN, window=4, dtype="f32", seed=34),
     W("f32_n1", B=1, N=1, H=1, d=8, P=1, mask_mode=NM, window=0, dtype="f32", seed=35),
