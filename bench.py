@@ -429,6 +429,74 @@ def run_gpu(args, w):
         dist.destroy_process_group()
 
 
+def run_stack(args, w):
+    """The layer stack of the pages' appendix C on workload w's shape: four sliding-window
+    IHA layers (P = w.P, window N/(2P^2) tokens) and one global layer (P = 1, causal), timed
+    through iha_forward_stack.  Its own JSON line; value = tokens through the stack / s."""
+    rank, world, local, dist = dist_setup(args.gpus)
+    import transformer_attention_variant_gb300 as iha
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    sched = gi.local_global_schedule(w.N, w.P)
+    host = gi.make_stack_inputs(w.B, w.N, w.H, w.d, w.dtype, w.seed, sched)
+    keys = ("W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")
+    layers = []
+    for L in host:
+        dl = {k: L[k].to(dev).contiguous() for k in keys}
+        dl.update(P=L["P"], mask_mode=L["mask_mode"], window=L["window"])
+        layers.append(dl)
+    X = host[0]["X"].to(dev).contiguous()
+    out = torch.empty_like(X)
+    dt = iha.IHA_DTYPE_BF16 if w.dtype == "bf16" else iha.IHA_DTYPE_F32
+    ws_bytes = iha.iha_stack_workspace_bytes([L["P"] for L in layers], w.B, w.N, w.H, w.d, dt)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flops = sum(work(L["workload"])["algorithmic"] for L in host)
+
+    def step():
+        iha.check(iha.iha_forward_stack(X, layers, w.B, w.N, w.H, w.d, dt, out, stream, ws, ws_bytes), "stack")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)          # evict L2 between steps (outside the events)
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status(stream)
+    iha.check(rc, f"device status after timed steps ({code:#x})")
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    ms = max_over_ranks(ms, dist, dev)
+    barrier(dist)
+    if rank == 0:
+        line = {
+            "metric": "IHA layer stack (4 sliding-window layers + 1 global layer) tokens/s, 1 GPU per replica",
+            "value": job_value(world, w.B * w.N, ms), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": DATA,
+            "config": {"workload": f"stack4x1_{w.name}", "B": w.B, "N": w.N, "H": w.H, "d": w.d,
+                       "layers": [{"P": L["P"], "mask": ["none", "causal", "causal+window"][L["mask_mode"]],
+                                   "window": L["window"] or None} for L in layers],
+                       "l2": "flushed between steps (256 MiB write outside the timed events)"},
+            "tflops_algorithmic": flops / (ms * 1e-3) / 1e12,
+            "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / peaks["bf16"],
+            "gpu_launches": 4 * len(layers) * args.steps, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def traffic_per_launch(workload, kernel):
     """DRAM bytes (read + write) per launch recorded from ncu in profiles/dram_traffic.txt,
     provided the kernel's source is unchanged since that capture; None otherwise."""
@@ -460,6 +528,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=48, help="oracle sample size per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
+    ap.add_argument("--stack", action="store_true",
+                    help="time the four-local + one-global layer stack on the workload's shape instead")
     ap.add_argument("--N", type=int, default=None,
                     help="shrink the workload's sequence length (smaller cases for profiler captures); "
                          "the window stays N/(2P) for windowed workloads")
@@ -472,6 +542,8 @@ def main():
                     window=args.N // (2 * w.P) if w.mask_mode == gi.MASK_WINDOW else w.window)
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.stack:
+        run_stack(args, w)
     else:
         run_gpu(args, w)
 

@@ -135,6 +135,29 @@ def make_inputs(w: Workload) -> dict:
     return inp
 
 
+def local_global_schedule(N: int, P_local: int, n_local: int = 4):
+    """Per-layer (P, mask_mode, window) of the hybrid local/global schedule of the pages'
+    appendix C: n_local sliding-window IHA layers with window N / (2 P^2) tokens, then one
+    global layer, taken as one pseudo-head per head (P = 1) over the causal mask -- the
+    layer the appendix's FLOP balance counts at plain-attention cost."""
+    w = max(1, N // (2 * P_local * P_local))
+    return [(P_local, MASK_WINDOW, w)] * n_local + [(1, MASK_CAUSAL, 0)]
+
+
+def make_stack_inputs(B: int, N: int, H: int, d: int, dtype: str, seed: int, schedule) -> list:
+    """CPU inputs of a layer stack: one dict per layer (the make_inputs tensors for that
+    layer's P, seeds seed, seed+1, ...) with its P, mask_mode and window; only layer 0's X
+    is the stack input."""
+    layers = []
+    for l, (P, mode, window) in enumerate(schedule):
+        w = Workload(f"stack_layer{l}", B=B, N=N, H=H, d=d, P=P, mask_mode=mode, window=window, dtype=dtype,
+                     seed=seed + l)
+        inp = make_inputs(w)
+        inp.update(P=P, mask_mode=mode, window=window, workload=w)
+        layers.append(inp)
+    return layers
+
+
 def identity_mixing(H: int, P: int) -> torch.Tensor:
     """alpha[m, h, j] = 1 if m == h else 0, for every j (each pseudo-head copies its own head)."""
     a = torch.zeros(H, H, P, dtype=torch.float32)

@@ -222,6 +222,28 @@ IHA_API int iha_attention(const void *QKV, int B, int N, int H, int d, int P,
 IHA_API int iha_contract(const void *Pbar, const float *R, int B, int N, int H, int d, int P,
                  int dtype, void *out, void *stream);
 
+/* A stack of IHA layers ("Interleaved Head Attention" appendix C, the hybrid local/global
+ * schedule, e.g. four sliding-window layers with window N/(2P^2) tokens and one global
+ * layer).  Layer l maps its input [B][N][H*d] to its output with its own weights and its
+ * own P[l], mask_mode[l], window[l]; layer 0 reads X, layer l+1 reads layer l's output and
+ * `out` receives the last layer's.  Nothing runs between layers (Algorithm 1 defines the
+ * attention layer alone: no residual, normalisation or MLP).
+ *   W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R: HOST arrays of num_layers DEVICE pointers,
+ *     each with the layout and dtype of the iha_forward_ex argument of that name;
+ *   P, mask_mode, window: host arrays of num_layers ints;
+ *   workspace: NULL (allocated and freed on `stream`) or at least
+ *     iha_stack_workspace_bytes(num_layers, P, B, N, H, d, dtype) bytes, 256-byte aligned.
+ * Every layer's arguments are checked (as by iha_forward_ex) before the first launch; the
+ * first failing check's status is returned and nothing runs. */
+IHA_API size_t iha_stack_workspace_bytes(int num_layers, const int *P, int B, int N, int H, int d, int dtype);
+IHA_API int iha_forward_stack(const void *X, int num_layers,
+                              const void *const *W_Q, const void *const *W_K, const void *const *W_V,
+                              const float *const *alpha_Q, const float *const *alpha_K,
+                              const float *const *alpha_V, const float *const *R,
+                              const int *P, const int *mask_mode, const int *window,
+                              int B, int N, int H, int d, int dtype, void *out, void *stream,
+                              void *workspace, size_t workspace_bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -123,3 +123,29 @@ def test_binding_fails_loudly_without_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import transformer_attention_variant_gb300"], cwd=tmp_path,
                        capture_output=True, text=True)
     assert r.returncode != 0 and "libiha.so is missing" in r.stderr
+
+
+def test_stack_workspace_and_validation(iha):
+    B, N, H, d = 1, 512, 4, 64
+    P = [2, 2, 2, 2, 1]
+    act = (B * N * H * d * 2 + 255) // 256 * 256
+    expect = 2 * act + max(iha.iha_workspace_bytes(B, N, H, d, p, 1) for p in P)
+    assert iha.iha_stack_workspace_bytes(P, B, N, H, d, 1) == expect
+    assert iha.iha_stack_workspace_bytes([], B, N, H, d, 1) == 0
+    assert iha.iha_stack_workspace_bytes([2, 0], B, N, H, d, 1) == 0          # a layer with P = 0
+    fake = 1 << 40                                                           # never dereferenced
+    layer = dict(W_Q=fake, W_K=fake, W_V=fake, alpha_Q=fake, alpha_K=fake, alpha_V=fake, R=fake,
+                 P=2, mask_mode=2, window=32)
+    ok = [dict(layer) for _ in range(5)]
+    bad_p = [dict(layer), dict(layer, P=0)]
+    bad_window = [dict(layer), dict(layer, window=0)]
+    null_w = [dict(layer), dict(layer, W_K=None)]
+    for layers, status in ((bad_p, iha.IHA_ERR_INVALID_ARG), (bad_window, iha.IHA_ERR_INVALID_ARG),
+                           (null_w, iha.IHA_ERR_INVALID_ARG)):
+        assert iha.iha_forward_stack(fake, layers, B, N, H, d, 1, fake) == status
+    assert iha.iha_forward_stack(fake, [], B, N, H, d, 1, fake) == iha.IHA_ERR_INVALID_ARG
+    assert iha.iha_forward_stack(None, ok, B, N, H, d, 1, fake) == iha.IHA_ERR_INVALID_ARG
+    assert iha.iha_forward_stack(fake, ok, B, N, H, 96, 1, fake) == iha.IHA_ERR_UNSUPPORTED
+    # a workspace that is too small is refused before anything runs
+    assert iha.iha_forward_stack(fake, ok, B, N, H, d, 1, fake, workspace=fake, workspace_bytes=256) == \
+        iha.IHA_ERR_WORKSPACE

@@ -309,3 +309,31 @@ def test_device_wait_timeout_is_reported(iha):
     w = W("after_timeout", B=1, N=64, H=2, d=64, P=2, mask_mode=C, window=0, dtype="bf16", seed=46)
     inp = gi.make_inputs(w)
     assert_parity(w, run_gpu(iha, w, inp).double().cpu().numpy(), oracle_rows(w, inp))
+
+
+# ---------------------------------------------------------------------------
+# layer stack (the hybrid local/global schedule): the stack entry point equals the chain of
+# single-layer calls bit for bit, and every layer matches the oracle on its own input
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("P_local,N", [(2, 300), (4, 257)])
+def test_layer_stack(iha, P_local, N):
+    B, H, d = 2, 4, 64
+    layers = gi.make_stack_inputs(B, N, H, d, "bf16", seed=60 + P_local, schedule=gi.local_global_schedule(N, P_local))
+    keys = ("W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")
+    dev = [{k: L[k].to("cuda:0").contiguous() for k in keys} for L in layers]
+    for dl, L in zip(dev, layers):
+        dl.update(P=L["P"], mask_mode=L["mask_mode"], window=L["window"])
+    X = layers[0]["X"].to("cuda:0").contiguous()
+    out = torch.empty_like(X)
+    iha.check(iha.iha_forward_stack(X, dev, B, N, H, d, iha.IHA_DTYPE_BF16, out), "iha_forward_stack")
+    torch.cuda.synchronize()
+    x = X
+    for l, (dl, L) in enumerate(zip(dev, layers)):
+        w = L["workload"]
+        y = run_gpu(iha, w, dinp=dict({k: dl[k] for k in keys}, X=x))
+        inp = {k: L[k] for k in keys}
+        inp["X"] = x.cpu()
+        assert_parity(w, y.double().cpu().numpy(), oracle_rows(w, inp))
+        x = y
+    assert torch.equal(out, x)

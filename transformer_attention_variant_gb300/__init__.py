@@ -33,7 +33,7 @@ EXPORTED = ("iha_forward", "iha_forward_ex", "iha_workspace_bytes", "iha_error_s
             "iha_check_device_status", "iha_forward_host", "iha_host_buffer_bytes",
             "iha_selftest_wait_timeout", "iha_fold_weights", "iha_project", "iha_attention",
             "iha_contract", "iha_forward_noalloc", "iha_projection_route", "iha_project_heads",
-            "iha_mix_heads")
+            "iha_mix_heads", "iha_stack_workspace_bytes", "iha_forward_stack")
 
 IHA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -84,6 +84,12 @@ def _load():
     lib.iha_mix_heads.restype = i
     lib.iha_forward_noalloc.argtypes = [vp] * 4 + [fp] * 4 + shape + [i, i, vp, i, vp]
     lib.iha_forward_noalloc.restype = i
+    ip = ctypes.POINTER(i)
+    pp = ctypes.POINTER(vp)
+    lib.iha_stack_workspace_bytes.argtypes = [i, ip, i, i, i, i, i]
+    lib.iha_stack_workspace_bytes.restype = sz
+    lib.iha_forward_stack.argtypes = [vp, i] + [pp] * 7 + [ip] * 3 + [i] * 5 + [vp, vp, vp, sz]
+    lib.iha_forward_stack.restype = i
     return lib
 
 
@@ -185,6 +191,35 @@ def iha_forward_noalloc(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H,
     allocation).  For callers that cannot allocate device memory."""
     return _lib.iha_forward_noalloc(_p(X), _p(W_Q), _p(W_K), _p(W_V), _p(alpha_Q), _p(alpha_K), _p(alpha_V),
                                     _p(R), B, N, H, d, P, mask_mode, window, _p(out), dtype, _s(stream))
+
+
+def _ptr_array(xs):
+    arr = (ctypes.c_void_p * len(xs))()
+    for k, x in enumerate(xs):
+        arr[k] = _p(x)
+    return arr
+
+
+def _int_array(xs):
+    arr = (ctypes.c_int * len(xs))()
+    for k, x in enumerate(xs):
+        arr[k] = int(x)
+    return arr
+
+
+def iha_stack_workspace_bytes(P, B, N, H, d, dtype) -> int:
+    """Workspace of iha_forward_stack for the per-layer pseudo-head counts P (a list)."""
+    return int(_lib.iha_stack_workspace_bytes(len(P), _int_array(P), B, N, H, d, dtype))
+
+
+def iha_forward_stack(X, layers, B, N, H, d, dtype, out, stream=None, workspace=None, workspace_bytes=0) -> int:
+    """layers: a list of dicts with W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R (device
+    tensors or addresses) and P, mask_mode, window (ints), one per layer in order."""
+    n = len(layers)
+    arrs = [_ptr_array([L[k] for L in layers]) for k in ("W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")]
+    ints = [_int_array([L[k] for L in layers]) for k in ("P", "mask_mode", "window")]
+    return _lib.iha_forward_stack(_p(X), n, *arrs, *ints, B, N, H, d, dtype, _p(out), _s(stream), _p(workspace),
+                                  workspace_bytes)
 
 
 def check(status: int, what: str = "") -> None:
