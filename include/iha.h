@@ -244,6 +244,34 @@ IHA_API int iha_forward_stack(const void *X, int num_layers,
                               int B, int N, int H, int d, int dtype, void *out, void *stream,
                               void *workspace, size_t workspace_bytes);
 
+/* Incremental decoding over a cache of pseudo-keys and pseudo-values (Algorithm 1 evaluated
+ * for the rows of one new token; the mask is by original position, so the P pseudo-queries
+ * of token t read the cached pseudo-tokens of positions t' <= t, and t - t' < window).
+ * bf16 only; d = 64 with P <= 8, or d = 128 with P <= 4 (IHA_ERR_UNSUPPORTED otherwise);
+ * mask_mode 1 or 2 (mode 0 would read future tokens: IHA_ERR_INVALID_ARG).
+ *   K_cache [B][H][cache_tokens*P][d] bfloat16, V_cache same shape float16: stacked row
+ *     t*P + j holds pseudo-key/value j of token t (the layout of Kbar/Vbar in iha_project).
+ *
+ * iha_prefill: iha_forward_ex over X [B][N][H*d] (the prompt) that also writes the prompt's
+ *   pseudo-keys/values into rows 0 .. N*P-1 of the caches (cache_tokens >= N). */
+IHA_API int iha_prefill(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                        const float *alpha_Q, const float *alpha_K, const float *alpha_V, const float *R,
+                        int B, int N, int H, int d, int P, int mask_mode, int window, void *out,
+                        void *K_cache, void *V_cache, int cache_tokens, int dtype, void *stream,
+                        void *workspace, size_t workspace_bytes);
+
+/* iha_decode_step: x [B][H*d] is token t of every sequence (t = the number of tokens
+ *   already cached, 0 <= t < cache_tokens).  Appends its pseudo-keys/values at rows
+ *   t*P .. t*P+P-1 of the caches and writes its output row out [B][H*d] (the row iha_forward
+ *   would give token t of the whole sequence).  workspace: NULL (allocated and freed on
+ *   `stream`) or iha_decode_workspace_bytes(B, H, d, P) bytes, 256-byte aligned. */
+IHA_API size_t iha_decode_workspace_bytes(int B, int H, int d, int P);
+IHA_API int iha_decode_step(const void *x, const void *W_Q, const void *W_K, const void *W_V,
+                            const float *alpha_Q, const float *alpha_K, const float *alpha_V, const float *R,
+                            int B, int H, int d, int P, int mask_mode, int window,
+                            void *K_cache, void *V_cache, int cache_tokens, int t, void *out,
+                            int dtype, void *stream, void *workspace, size_t workspace_bytes);
+
 #ifdef __cplusplus
 }
 #endif

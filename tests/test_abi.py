@@ -149,3 +149,30 @@ def test_stack_workspace_and_validation(iha):
     # a workspace that is too small is refused before anything runs
     assert iha.iha_forward_stack(fake, ok, B, N, H, d, 1, fake, workspace=fake, workspace_bytes=256) == \
         iha.IHA_ERR_WORKSPACE
+
+
+def test_decode_validation(iha):
+    fake = 1 << 40                                           # never dereferenced
+    B, H, d, P = 2, 4, 64, 2
+    assert iha.iha_decode_workspace_bytes(B, H, d, P) > 0
+    assert iha.iha_decode_workspace_bytes(B, H, 128, 8) == 0     # d = 128 takes P <= 4
+    assert iha.iha_decode_workspace_bytes(B, H, 96, 2) == 0
+    args = [fake] * 8
+    ok = dict(B=B, H=H, d=d, P=P, mask_mode=1, window=0, K_cache=fake, V_cache=fake, cache_tokens=100, t=5,
+              out=fake, dtype=1)
+
+    def step(**kw):
+        a = dict(ok, **kw)
+        return iha.iha_decode_step(*args, a["B"], a["H"], a["d"], a["P"], a["mask_mode"], a["window"],
+                                   a["K_cache"], a["V_cache"], a["cache_tokens"], a["t"], a["out"], a["dtype"])
+    assert step(t=100) == iha.IHA_ERR_INVALID_ARG            # no room in the cache
+    assert step(t=-1) == iha.IHA_ERR_INVALID_ARG
+    assert step(mask_mode=0) == iha.IHA_ERR_INVALID_ARG      # would read future tokens
+    assert step(K_cache=None) == iha.IHA_ERR_INVALID_ARG
+    assert step(dtype=0) == iha.IHA_ERR_UNSUPPORTED
+    assert step(d=128, P=8) == iha.IHA_ERR_UNSUPPORTED
+    assert iha.iha_decode_step(*args, B, H, d, P, 1, 0, fake, fake, 100, 5, fake, 1, None, fake, 16) == \
+        iha.IHA_ERR_WORKSPACE
+    # prefill: the cache must hold the prompt
+    assert iha.iha_prefill(*args, B, 50, H, d, P, 1, 0, fake, fake, fake, 49, 1) == iha.IHA_ERR_INVALID_ARG
+    assert iha.iha_prefill(*args, B, 50, H, d, P, 0, 0, fake, fake, fake, 60, 1) == iha.IHA_ERR_INVALID_ARG

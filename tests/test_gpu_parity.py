@@ -337,3 +337,59 @@ def test_layer_stack(iha, P_local, N):
         assert_parity(w, y.double().cpu().numpy(), oracle_rows(w, inp))
         x = y
     assert torch.equal(out, x)
+
+
+# ---------------------------------------------------------------------------
+# incremental decoding: prefill a prompt, then decode token by token; every decoded row
+# must be the row the forward pass gives that token of the whole sequence (the oracle)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,d,P,mode,window", [(4, 64, 2, C, 0), (4, 64, 8, WN, 5), (16, 128, 4, C, 0),
+                                                (3, 128, 3, WN, 20), (2, 128, 1, C, 0)])
+def test_decode_matches_oracle(iha, H, d, P, mode, window):
+    B, T, steps = 2, 37, 4
+    n_all = T + steps
+    w = gi.Workload("decode", B=B, N=n_all, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=70 + P)
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    D = w.D
+    cap = n_all + 3
+    Kc = torch.zeros(B, H, cap * P, d, dtype=torch.bfloat16, device="cuda:0")
+    Vc = torch.zeros(B, H, cap * P, d, dtype=torch.float16, device="cuda:0")
+    X = dinp["X"]
+    wts = [dinp[k] for k in ("W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")]
+    out_prompt = torch.empty(B, T, D, dtype=torch.bfloat16, device="cuda:0")
+    iha.check(iha.iha_prefill(X[:, :T].contiguous(), *wts, B, T, H, d, P, mode, window, out_prompt, Kc, Vc, cap,
+                              iha.IHA_DTYPE_BF16), "iha_prefill")
+    dec = []
+    for s in range(steps):
+        t = T + s
+        o = torch.empty(B, D, dtype=torch.bfloat16, device="cuda:0")
+        iha.check(iha.iha_decode_step(X[:, t].contiguous(), *wts, B, H, d, P, mode, window, Kc, Vc, cap, t, o,
+                                      iha.IHA_DTYPE_BF16), "iha_decode_step")
+        dec.append(o)
+    torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status()
+    assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
+    rows = [b * n_all + t for b in range(B) for t in range(T, n_all)]
+    got = torch.stack(dec, 1).reshape(B * steps, D).double().cpu().numpy()    # [b][step] = rows order
+    assert_parity(w, got, oracle_rows(w, inp, rows=rows))
+    # the prompt's rows come from the forward pass (rows of a prefix do not depend on later tokens)
+    rows_p = [b * n_all + t for b in range(B) for t in range(T)]
+    assert_parity(w, out_prompt.reshape(B * T, D).double().cpu().numpy(), oracle_rows(w, inp, rows=rows_p))
+
+
+def test_decode_from_empty_cache(iha):
+    """t = 0: the token reads only its own P pseudo-keys."""
+    B, H, d, P = 3, 4, 64, 2
+    w = gi.Workload("decode0", B=B, N=1, H=H, d=d, P=P, mask_mode=C, window=0, dtype="bf16", seed=77)
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    wts = [dinp[k] for k in ("W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")]
+    Kc = torch.zeros(B, H, 2 * P, d, dtype=torch.bfloat16, device="cuda:0")
+    Vc = torch.zeros(B, H, 2 * P, d, dtype=torch.float16, device="cuda:0")
+    o = torch.empty(B, w.D, dtype=torch.bfloat16, device="cuda:0")
+    iha.check(iha.iha_decode_step(dinp["X"][:, 0].contiguous(), *wts, B, H, d, P, C, 0, Kc, Vc, 2, 0, o,
+                                  iha.IHA_DTYPE_BF16))
+    torch.cuda.synchronize()
+    assert_parity(w, o.double().cpu().numpy(), oracle_rows(w, inp))

@@ -33,7 +33,8 @@ EXPORTED = ("iha_forward", "iha_forward_ex", "iha_workspace_bytes", "iha_error_s
             "iha_check_device_status", "iha_forward_host", "iha_host_buffer_bytes",
             "iha_selftest_wait_timeout", "iha_fold_weights", "iha_project", "iha_attention",
             "iha_contract", "iha_forward_noalloc", "iha_projection_route", "iha_project_heads",
-            "iha_mix_heads", "iha_stack_workspace_bytes", "iha_forward_stack")
+            "iha_mix_heads", "iha_stack_workspace_bytes", "iha_forward_stack", "iha_prefill",
+            "iha_decode_workspace_bytes", "iha_decode_step")
 
 IHA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -90,6 +91,12 @@ def _load():
     lib.iha_stack_workspace_bytes.restype = sz
     lib.iha_forward_stack.argtypes = [vp, i] + [pp] * 7 + [ip] * 3 + [i] * 5 + [vp, vp, vp, sz]
     lib.iha_forward_stack.restype = i
+    lib.iha_prefill.argtypes = [vp] * 4 + [fp] * 4 + shape + [i, i, vp, vp, vp, i, i, vp, vp, sz]
+    lib.iha_prefill.restype = i
+    lib.iha_decode_workspace_bytes.argtypes = [i, i, i, i]
+    lib.iha_decode_workspace_bytes.restype = sz
+    lib.iha_decode_step.argtypes = [vp] * 4 + [fp] * 4 + [i] * 6 + [vp, vp, i, i, vp, i, vp, vp, sz]
+    lib.iha_decode_step.restype = i
     return lib
 
 
@@ -220,6 +227,24 @@ def iha_forward_stack(X, layers, B, N, H, d, dtype, out, stream=None, workspace=
     ints = [_int_array([L[k] for L in layers]) for k in ("P", "mask_mode", "window")]
     return _lib.iha_forward_stack(_p(X), n, *arrs, *ints, B, N, H, d, dtype, _p(out), _s(stream), _p(workspace),
                                   workspace_bytes)
+
+
+def iha_prefill(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, out,
+                K_cache, V_cache, cache_tokens, dtype, stream=None, workspace=None, workspace_bytes=0) -> int:
+    return _lib.iha_prefill(_p(X), _p(W_Q), _p(W_K), _p(W_V), _p(alpha_Q), _p(alpha_K), _p(alpha_V), _p(R),
+                            B, N, H, d, P, mask_mode, window, _p(out), _p(K_cache), _p(V_cache), cache_tokens,
+                            dtype, _s(stream), _p(workspace), workspace_bytes)
+
+
+def iha_decode_workspace_bytes(B, H, d, P) -> int:
+    return int(_lib.iha_decode_workspace_bytes(B, H, d, P))
+
+
+def iha_decode_step(x, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, H, d, P, mask_mode, window, K_cache,
+                    V_cache, cache_tokens, t, out, dtype, stream=None, workspace=None, workspace_bytes=0) -> int:
+    return _lib.iha_decode_step(_p(x), _p(W_Q), _p(W_K), _p(W_V), _p(alpha_Q), _p(alpha_K), _p(alpha_V), _p(R),
+                                B, H, d, P, mask_mode, window, _p(K_cache), _p(V_cache), cache_tokens, t, _p(out),
+                                dtype, _s(stream), _p(workspace), workspace_bytes)
 
 
 def check(status: int, what: str = "") -> None:

@@ -180,6 +180,43 @@ int iha_forward_ex(const void *X, const void *W_Q, const void *W_K, const void *
                        dtype, static_cast<cudaStream_t>(stream), workspace, workspace_bytes);
 }
 
+int iha_prefill(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
+                const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
+                int mask_mode, int window, void *out, void *K_cache, void *V_cache, int cache_tokens, int dtype,
+                void *stream, void *workspace, size_t workspace_bytes) {
+    int rc = check_forward_args(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window,
+                                out, dtype);
+    if (rc != IHA_OK) return rc;
+    if (!K_cache || !V_cache || cache_tokens < N || mask_mode == IHA_MASK_NONE) return IHA_ERR_INVALID_ARG;
+    if (dtype != IHA_DTYPE_BF16 || !decode_supported(H, d, P)) return IHA_ERR_UNSUPPORTED;
+    const Shape sh{B, N, H, d, P};
+    const WsLayout lay = ws_layout(sh, dtype);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool own = false;
+    if (!workspace) {
+        if (cudaMallocAsync(&workspace, lay.total, st) != cudaSuccess) return IHA_ERR_CUDA;
+        own = true;
+        workspace_bytes = lay.total;
+    }
+    rc = run_forward(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, sh, mask_mode, window, out, dtype, st, workspace,
+                     workspace_bytes);
+    if (rc == IHA_OK) {
+        // Kbar, Vbar [B][H][N*P][d] -> the caches [B][H][cache_tokens*P][d]
+        const uint8_t *qkv = static_cast<const uint8_t *>(workspace) + lay.qkv;
+        const size_t blk = (size_t)N * P * d * 2, cap = (size_t)cache_tokens * P * d * 2;
+        const size_t third = (size_t)sh.qkv_elems() * 2;
+        cudaError_t e = cudaMemcpy2DAsync(K_cache, cap, qkv + third, blk, blk, (size_t)B * H, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(V_cache, cap, qkv + 2 * third, blk, blk, (size_t)B * H, cudaMemcpyDeviceToDevice, st);
+        rc = cuda_status(e);
+    }
+    if (own) {
+        const cudaError_t e = cudaFreeAsync(workspace, st);
+        if (rc == IHA_OK && e != cudaSuccess) rc = IHA_ERR_CUDA;
+    }
+    return rc;
+}
+
 int iha_forward(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
                 const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
                 int mask_mode, int window, void *out) {

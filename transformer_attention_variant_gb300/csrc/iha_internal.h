@@ -97,6 +97,14 @@ int forward_in_workspace(const void *X, const void *WQ, const void *WK, const vo
                          int window, void *out, int dtype, cudaStream_t st, void *workspace,
                          size_t workspace_bytes);
 
+// One decoding step over a pseudo-token cache (bf16; d = 64 with P <= 8, d = 128 with P <= 4).
+bool decode_supported(int H, int d, int P);
+size_t decode_workspace_bytes(int B, int H, int d, int P);
+cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const void *WV, const float *aQ,
+                          const float *aK, const float *aV, const float *R, int B, int H, int d, int P, int mask_mode,
+                          int window, void *Kc, void *Vc, long long cache_tokens, long long t, void *out, void *ws,
+                          cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
