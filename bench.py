@@ -497,6 +497,78 @@ def run_stack(args, w):
         dist.destroy_process_group()
 
 
+def run_decode(args, w):
+    """One decoding step at position N-1 over a full cache of workload w's shape (B
+    sequences, N cached tokens, P pseudo-heads): HBM-bound, so reported against the copy
+    bandwidth.  Algorithmic bytes per step: W_Q, W_K, W_V once (3 D^2 bf16) + the readable
+    cached pseudo-keys and values + the new token's rows; the cache holds random values."""
+    rank, world, local, dist = dist_setup(args.gpus)
+    import transformer_attention_variant_gb300 as iha
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    B, N, H, d, P = w.B, w.N, w.H, w.d, w.P
+    host = gi.make_inputs(w.with_(N=1, name=w.name + "@decode"))
+    dd = {k: v.to(dev).contiguous() for k, v in host.items()}
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    Kc = torch.randn(B, H, N * P, d, generator=g, device=dev).to(torch.bfloat16)
+    Vc = torch.randn(B, H, N * P, d, generator=g, device=dev).to(torch.float16)
+    x = dd["X"].reshape(B, w.D).contiguous()
+    out = torch.empty(B, w.D, dtype=torch.bfloat16, device=dev)
+    ws_bytes = iha.iha_decode_workspace_bytes(B, H, d, P)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    t = N - 1
+    lo = max(0, (t - w.window + 1) * P) if w.mask_mode == gi.MASK_WINDOW else 0
+    rows = (t + 1) * P - lo
+    nbytes = 3 * w.D * w.D * 2 + B * H * rows * d * 2 * 2 + B * w.D * 2 * 2
+
+    def step():
+        iha.check(iha.iha_decode_step(x, dd["W_Q"], dd["W_K"], dd["W_V"], dd["alpha_Q"], dd["alpha_K"], dd["alpha_V"],
+                                      dd["R"], B, H, d, P, w.mask_mode, w.window, Kc, Vc, N, t, out,
+                                      iha.IHA_DTYPE_BF16, stream, ws, ws_bytes), "decode")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status(stream)
+    iha.check(rc, f"device status after timed steps ({code:#x})")
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    ms = max_over_ranks(ms, dist, dev)
+    barrier(dist)
+    if rank == 0:
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        line = {
+            "metric": "IHA decode step tokens/s (one new token per sequence over a full pseudo-token cache)",
+            "value": job_value(world, B, ms), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": DATA + "; cache filled with N(0,1) values",
+            "config": {"workload": f"decode_{w.name}", "B": B, "cached_tokens": N, "H": H, "d": d, "P": P,
+                       "mask": ["none", "causal", "causal+window"][w.mask_mode], "window": w.window or None,
+                       "l2": "flushed between steps (256 MiB write outside the timed events)"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "bytes_per_step": nbytes, "traffic": None},
+            "gpu_launches": 4 * args.steps, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def traffic_per_launch(workload, kernel):
     """DRAM bytes (read + write) per launch recorded from ncu in profiles/dram_traffic.txt,
     provided the kernel's source is unchanged since that capture; None otherwise."""
@@ -530,6 +602,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
     ap.add_argument("--stack", action="store_true",
                     help="time the four-local + one-global layer stack on the workload's shape instead")
+    ap.add_argument("--decode", action="store_true",
+                    help="time one decoding step over a full cache of the workload's shape instead")
     ap.add_argument("--N", type=int, default=None,
                     help="shrink the workload's sequence length (smaller cases for profiler captures); "
                          "the window stays N/(2P) for windowed workloads")
@@ -544,6 +618,8 @@ def main():
         run_reference(args, w)
     elif args.stack:
         run_stack(args, w)
+    elif args.decode:
+        run_decode(args, w)
     else:
         run_gpu(args, w)
 

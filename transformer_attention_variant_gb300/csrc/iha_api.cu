@@ -39,6 +39,8 @@ static int *status_ptr() {
     return g_status_ptr[dev];
 }
 
+int *status_word_ptr() { return status_ptr(); }
+
 int device_sm_count() {
     static int counts[kMaxDevices];
     const int dev = current_device();

@@ -34,7 +34,7 @@ int iha_decode_step(const void *x, const void *W_Q, const void *W_K, const void 
         return IHA_ERR_WORKSPACE;
     }
     cudaError_t e = launch_decode(x, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, H, d, P, mask_mode, window,
-                                  K_cache, V_cache, cache_tokens, t, out, workspace, st);
+                                  K_cache, V_cache, cache_tokens, t, out, workspace, st, status_word_ptr());
     if (own) {
         const cudaError_t e2 = cudaFreeAsync(workspace, st);
         if (e == cudaSuccess) e = e2;

@@ -30,6 +30,8 @@ enum WaitSite {
     kSiteContractProducer = 34,
     kSiteContractMma = 35,
     kSiteContractEpilogue = 36,
+    kSiteDecodeProducer = 37,
+    kSiteDecodeConsumer = 38,
     kSiteSelfTest = 99,
 };
 
@@ -103,7 +105,10 @@ size_t decode_workspace_bytes(int B, int H, int d, int P);
 cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const void *WV, const float *aQ,
                           const float *aK, const float *aV, const float *R, int B, int H, int d, int P, int mask_mode,
                           int window, void *Kc, void *Vc, long long cache_tokens, long long t, void *out, void *ws,
-                          cudaStream_t st);
+                          cudaStream_t st, int *status);
+
+// The status word of the current device (bounded device waits record timeouts there).
+int *status_word_ptr();
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

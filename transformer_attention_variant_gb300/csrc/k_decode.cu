@@ -8,12 +8,13 @@
 //   2. decode_mix:     q~/k~/v~_{h,j}[b] = sum_m alpha_s[m,h,j] y_s[b][m]; k~ and v~ go into
 //                      the cache at stacked row t*P + j, q~ into the workspace.
 //   3. decode_attn:    split-KV attention: a CTA takes a chunk of the cached rows of one
-//                      (b, h); all P pseudo-queries share the chunk's K and V reads (eight
-//                      lanes hold one key row, 16 bytes of K and V per lane per row); online
-//                      softmax per query; the chunk's (max, sum, unnormalised output) go to
-//                      the workspace.
-//   4. decode_combine: merge the chunks of every (b, h, j), then the R contraction
-//                      out[b][h][c] = sum_{h',j} R[h][h'P + j] Pbar[b][h'][j][c].
+//                      (b, h); a producer warp streams the chunk's K and V rows into a
+//                      6-stage shared-memory ring with bulk copies (about 96 KB in flight per
+//                      CTA); all P pseudo-queries share each row (eight lanes hold one key
+//                      row); online softmax per query; the chunk's (max, sum, unnormalised
+//                      output) go to the workspace.
+//   4. decode_merge:   merge the chunks of every (b, h, j);
+//      decode_contract: the R contraction out[b][h][c] = sum_{h',j} R[h][h'P + j] Pbar[b][h'][j][c].
 // All four are HBM-bound: W (3 D^2 bf16) and the cached rows of K and V are the bytes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -23,10 +24,9 @@
 
 namespace iha {
 
-constexpr int DC_KS = 8;          // K splits of the projection GEMV
+constexpr int DC_KS = 16;         // K splits of the projection GEMV
 constexpr int DC_BMAX = 8;        // batch rows per pass of the GEMV
 constexpr int DC_NCH_MAX = 64;    // KV chunks per (b, h)
-constexpr int DC_ATT_THREADS = 128;
 
 // ---------------------------------------------------------------------------------------
 // 1. projection GEMV: Yp[ks][b][s][n] = sum_{k in split ks} x[b][k] W_s[k][n]
@@ -56,21 +56,33 @@ decode_proj(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[b][e] = 0.f;
         if (n < D) {
-            for (int k = warp; k < krows; k += 8) {
-                const uint4 wv = *reinterpret_cast<const uint4 *>(W + (size_t)(k0 + k) * D + n);
-                const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
-                float wf[8];
+            // rows warp, warp+8, ... of the split; eight rows' loads in flight per lane
+            for (int k8 = warp; k8 < krows; k8 += 64) {
+                uint4 wv[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    wf[2 * e] = __uint_as_float(w4[e] << 16);
-                    wf[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+                for (int u = 0; u < 8; ++u) {
+                    const int k = k8 + 8 * u;
+                    wv[u] = k < krows ? *reinterpret_cast<const uint4 *>(W + (size_t)(k0 + k) * D + n)
+                                      : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
-                for (int b = 0; b < DC_BMAX; ++b) {
-                    if (b < nb) {
-                        const float xv = xs[b * krows + k];
+                for (int u = 0; u < 8; ++u) {
+                    const int k = k8 + 8 * u;
+                    if (k >= krows) break;
+                    const uint32_t w4[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+                    float wf[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[b][e] = fmaf(xv, wf[e], acc[b][e]);
+                    for (int e = 0; e < 4; ++e) {
+                        wf[2 * e] = __uint_as_float(w4[e] << 16);
+                        wf[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+                    }
+#pragma unroll
+                    for (int b = 0; b < DC_BMAX; ++b) {
+                        if (b < nb) {
+                            const float xv = xs[b * krows + k];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[b][e] = fmaf(xv, wf[e], acc[b][e]);
+                        }
                     }
                 }
             }
@@ -78,8 +90,9 @@ decode_proj(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict
         // reduce over the 8 warps
 #pragma unroll
         for (int b = 0; b < DC_BMAX; ++b)
+            if (b < nb)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) red[(warp * DC_BMAX + b) * 256 + lane * 8 + e] = acc[b][e];
+                for (int e = 0; e < 8; ++e) red[(warp * DC_BMAX + b) * 256 + lane * 8 + e] = acc[b][e];
         __syncthreads();
         for (int i = threadIdx.x; i < nb * 256; i += blockDim.x) {
             const int b = i / 256, c = i % 256;
@@ -93,34 +106,52 @@ decode_proj(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict
 }
 
 // ---------------------------------------------------------------------------------------
-// 2. mixing + cache append, one CTA per (b, s, h), one thread per column c
+// 2. mixing + cache append, one CTA per (b, s): y_s[b] = sum of the K-split partials into
+//    shared memory (all loads of a thread in flight), alpha_s into shared memory, then every
+//    (h, j, c) output of the projection
 // ---------------------------------------------------------------------------------------
-__global__ void decode_mix(const float *__restrict__ Yp, const float *__restrict__ aQ, const float *__restrict__ aK,
-                           const float *__restrict__ aV, int B, int H, int d, int P, long long t, long long cache_rows,
-                           __nv_bfloat16 *__restrict__ qt, __nv_bfloat16 *__restrict__ Kc, __half *__restrict__ Vc) {
-    const int b = blockIdx.x, s = blockIdx.y, h = blockIdx.z, c = threadIdx.x;
-    const int D = H * d;
-    const float *al = s == 0 ? aQ : (s == 1 ? aK : aV);
-    float acc[16];
+__global__ void __launch_bounds__(256)
+decode_mix(const float *__restrict__ Yp, const float *__restrict__ aQ, const float *__restrict__ aK,
+           const float *__restrict__ aV, int B, int H, int d, int P, long long t, long long cache_rows,
+           __nv_bfloat16 *__restrict__ qt, __nv_bfloat16 *__restrict__ Kc, __half *__restrict__ Vc) {
+    extern __shared__ float msm[];
+    const int b = blockIdx.x, s = blockIdx.y, hg = blockIdx.z, nhg = gridDim.z;   // heads h = hg, hg + nhg, ...
+    const int D = H * d, HP = H * P;
+    float *y = msm;              // [H][d]
+    float *al = msm + D;         // alpha_s [H][H][P]
+    const float *alg = s == 0 ? aQ : (s == 1 ? aK : aV);
+    for (int i0 = threadIdx.x; i0 < D; i0 += 4 * blockDim.x) {
+        float v[4][DC_KS];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-    for (int m = 0; m < H; ++m) {
-        float y = 0.f;
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * blockDim.x;
 #pragma unroll
-        for (int ks = 0; ks < DC_KS; ++ks) y += Yp[(((size_t)ks * B + b) * 3 + s) * D + m * d + c];
+            for (int ks = 0; ks < DC_KS; ++ks) v[u][ks] = i < D ? Yp[(((size_t)ks * B + b) * 3 + s) * D + i] : 0.f;
+        }
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (j < P) acc[j] = fmaf(al[((size_t)m * H + h) * P + j], y, acc[j]);   // alpha_s[m][h][j]
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * blockDim.x;
+            float acc = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < DC_KS; ++ks) acc += v[u][ks];
+            if (i < D) y[i] = acc;
+        }
     }
-    for (int j = 0; j < P; ++j) {
+    for (int i = threadIdx.x; i < H * HP; i += blockDim.x) al[i] = alg[i];
+    __syncthreads();
+    const int nh = (H - hg + nhg - 1) / nhg;   // heads of this group
+    for (int i = threadIdx.x; i < nh * P * d; i += blockDim.x) {
+        const int hj = i / d, c = i % d, h = hg + (hj / P) * nhg, j = hj % P;
+        float acc = 0.f;
+        for (int m = 0; m < H; ++m) acc = fmaf(al[(m * H + h) * P + j], y[m * d + c], acc);   // alpha_s[m][h][j]
         if (s == 0) {
-            qt[(((size_t)b * H + h) * P + j) * d + c] = __float2bfloat16_rn(acc[j]);
+            qt[(((size_t)b * H + h) * P + j) * d + c] = __float2bfloat16_rn(acc);
         } else {
             const size_t row = ((size_t)b * H + h) * cache_rows + (size_t)t * P + j;   // stacked row t*P + j
             if (s == 1)
-                Kc[row * d + c] = __float2bfloat16_rn(acc[j]);
+                Kc[row * d + c] = __float2bfloat16_rn(acc);
             else
-                Vc[row * d + c] = __float2half_rn(acc[j]);
+                Vc[row * d + c] = __float2half_rn(acc);
         }
     }
 }
@@ -128,125 +159,191 @@ __global__ void decode_mix(const float *__restrict__ Yp, const float *__restrict
 // ---------------------------------------------------------------------------------------
 // 3. split-KV attention of the P pseudo-queries of token t
 // ---------------------------------------------------------------------------------------
-template <int DPL, int PMAX>   // DPL = d / 8 dims per lane; PMAX = largest P
-__global__ void __launch_bounds__(DC_ATT_THREADS)
+constexpr int DA_KT = 32;        // cached rows per ring stage
+constexpr int DA_STAGES = 5;
+constexpr int DA_CWARPS = 8;     // consumer warps; warp 8 is the producer
+constexpr int DA_THREADS = 32 * (DA_CWARPS + 1);
+
+template <int D>
+constexpr int da_smem_bytes() { return DA_STAGES * 2 * DA_KT * D * 2 + 2 * DA_STAGES * 8 + 16 + 128; }
+
+__device__ __forceinline__ float fast_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+
+// A group of LPR = d/8 lanes holds one cached row, 8 dims (16 bytes) per lane: the group
+// reads its row's 16*LPR contiguous bytes per load (no bank conflict).
+template <int LPR, int PMAX>   // LPR = d / 8 lanes per row; PMAX = largest P
+__global__ void __launch_bounds__(DA_THREADS, PMAX <= 4 ? 2 : 1)
 decode_attn(const __nv_bfloat16 *__restrict__ qt, const __nv_bfloat16 *__restrict__ Kc, const __half *__restrict__ Vc,
             int H, int P, long long cache_rows, long long lo, long long hi, int rows_per_chunk, float scale_log2,
-            float *__restrict__ part_ml, float *__restrict__ part_o) {
-    constexpr int d = DPL * 8;
+            float *__restrict__ part_ml, float *__restrict__ part_o, int *status) {
+    constexpr int DPL = 8;                        // dims per lane
+    constexpr int d = LPR * DPL;
+    constexpr int GPW = 32 / LPR;                 // rows (groups) per warp
+    constexpr int ROWB = d * 2;                   // bytes of one cached row
+    constexpr int STAGE = 2 * DA_KT * ROWB;       // K rows, then V rows
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + DA_STAGES * STAGE);
+    uint64_t *empty = full + DA_STAGES;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + DA_STAGES);
+    __shared__ float sm_ml[DA_CWARPS][PMAX][2];
+    __shared__ float sm_o[DA_CWARPS][PMAX][d];
+
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, nch = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int grp = lane >> 3, gl = lane & 7;          // 4 groups of 8 lanes per warp
     const long long bh = (long long)b * H + h;
     const long long r_begin = lo + (long long)chunk * rows_per_chunk;
     const long long r_end = min(hi + 1, r_begin + rows_per_chunk);
-    // this lane's DPL dims of every pseudo-query
-    float q[PMAX][DPL];
-#pragma unroll
-    for (int j = 0; j < PMAX; ++j)
-#pragma unroll
-        for (int e = 0; e < DPL; ++e)
-            q[j][e] = j < P ? __bfloat162float(qt[((bh * P) + j) * d + gl * DPL + e]) * scale_log2 : 0.f;
-    float m[PMAX], l[PMAX], o[PMAX][DPL];
-#pragma unroll
-    for (int j = 0; j < PMAX; ++j) {
-        m[j] = -INFINITY;
-        l[j] = 0.f;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[j][e] = 0.f;
+    const int nrows = (int)(r_end - r_begin);
+    const int nsub = (nrows + DA_KT - 1) / DA_KT;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < DA_STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], DA_CWARPS);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
     }
-    // rows r_begin + 4*warp + grp, stepping by 16 (4 warps x 4 groups).  The loop runs the
-    // same number of times on every lane of the warp (its shuffles name all 32 lanes); a
-    // group whose row is past the chunk loads nothing and skips the update.
-    for (long long base = r_begin + warp * 4; base < r_end; base += 16) {
-        const long long r = base + grp;
-        const bool valid = r < r_end;
-        float kf[DPL], vf[DPL];
+    __syncthreads();
+
+    if (warp == DA_CWARPS) {
+        // ------------------------------- producer -----------------------------------
+        if (lane == 0) {
+            for (int i = 0; i < nsub; ++i) {
+                const int st = i % DA_STAGES;
+                if (!mbar_wait_lazy(&empty[st], ((i / DA_STAGES) & 1) ^ 1, status, kSiteDecodeProducer, abort_flag))
+                    break;
+                const int n = min(DA_KT, nrows - i * DA_KT);
+                const long long row = bh * cache_rows + r_begin + (long long)i * DA_KT;
+                mbar_arrive_expect_tx(&full[st], 2u * n * ROWB);
+                bulk_load(ring + st * STAGE, Kc + row * d, (uint32_t)(n * ROWB), &full[st]);
+                bulk_load(ring + st * STAGE + DA_KT * ROWB, Vc + row * d, (uint32_t)(n * ROWB), &full[st]);
+            }
+        }
+    } else {
+        // ------------------------------- consumers ----------------------------------
+        const int grp = lane / LPR, gl = lane % LPR;   // GPW groups of LPR lanes per warp
+        float q[PMAX][DPL];
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) kf[e] = vf[e] = 0.f;
-        if (valid) {
-            const __nv_bfloat16 *kr = Kc + (bh * cache_rows + r) * d + gl * DPL;
-            const __half *vr = Vc + (bh * cache_rows + r) * d + gl * DPL;
+        for (int j = 0; j < PMAX; ++j)
 #pragma unroll
-            for (int e8 = 0; e8 < DPL; e8 += 8) {
-                const uint4 ku = *reinterpret_cast<const uint4 *>(kr + e8);
-                const uint4 vu = *reinterpret_cast<const uint4 *>(vr + e8);
-                const uint32_t k4[4] = {ku.x, ku.y, ku.z, ku.w}, v4[4] = {vu.x, vu.y, vu.z, vu.w};
+            for (int e = 0; e < DPL; ++e)
+                q[j][e] = j < P ? __bfloat162float(qt[((bh * P) + j) * d + gl * DPL + e]) * scale_log2 : 0.f;
+        float m[PMAX], l[PMAX], o[PMAX][DPL];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kf[e8 + 2 * e] = __uint_as_float(k4[e] << 16);
-                    kf[e8 + 2 * e + 1] = __uint_as_float(k4[e] & 0xffff0000u);
-                    const __half2 vh = *reinterpret_cast<const __half2 *>(&v4[e]);
-                    const float2 vv = __half22float2(vh);
-                    vf[e8 + 2 * e] = vv.x;
-                    vf[e8 + 2 * e + 1] = vv.y;
+        for (int j = 0; j < PMAX; ++j) {
+            m[j] = -INFINITY;
+            l[j] = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[j][e] = 0.f;
+        }
+        for (int i = 0; i < nsub; ++i) {
+            const int st = i % DA_STAGES;
+            // every lane waits (warp-uniform); a failed wait ends the warp's loop on all lanes
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (i / DA_STAGES) & 1, status,
+                                                               kSiteDecodeConsumer, abort_flag));
+            if (!ok) break;
+            const int n = min(DA_KT, nrows - i * DA_KT);
+            const uint8_t *ks = ring + st * STAGE, *vs = ks + DA_KT * ROWB;
+            // row groups warp, warp + DA_CWARPS, ... of the stage (GPW rows each); rows past n
+            // are skipped on every lane of their group
+            for (int qd = warp; qd < DA_KT / GPW; qd += DA_CWARPS) {
+                const int r = qd * GPW + grp;
+                const bool valid = r < n;
+                float kf[DPL], vf[DPL];
+                {
+                    const int off = r * ROWB + gl * 16;
+                    const uint4 ku = valid ? *reinterpret_cast<const uint4 *>(ks + off) : make_uint4(0, 0, 0, 0);
+                    const uint4 vu = valid ? *reinterpret_cast<const uint4 *>(vs + off) : make_uint4(0, 0, 0, 0);
+                    const uint32_t k4[4] = {ku.x, ku.y, ku.z, ku.w}, v4[4] = {vu.x, vu.y, vu.z, vu.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        kf[2 * e] = __uint_as_float(k4[e] << 16);
+                        kf[2 * e + 1] = __uint_as_float(k4[e] & 0xffff0000u);
+                        const __half2 vh = *reinterpret_cast<const __half2 *>(&v4[e]);
+                        const float2 vv = __half22float2(vh);
+                        vf[2 * e] = vv.x;
+                        vf[2 * e + 1] = vv.y;
+                    }
+                }
+                // the P scores as independent chains (queries past P have q = 0), then their
+                // reductions over the group's 8 lanes, then the online-softmax updates
+                float sc[PMAX];
+#pragma unroll
+                for (int j = 0; j < PMAX; ++j) sc[j] = 0.f;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e)
+#pragma unroll
+                    for (int j = 0; j < PMAX; ++j) sc[j] = fmaf(q[j][e], kf[e], sc[j]);
+#pragma unroll
+                for (int off = LPR / 2; off >= 1; off >>= 1)
+#pragma unroll
+                    for (int j = 0; j < PMAX; ++j) sc[j] += __shfl_xor_sync(0xffffffffu, sc[j], off);
+                if (valid) {                                     // uniform over the group
+#pragma unroll
+                    for (int j = 0; j < PMAX; ++j) {
+                        if (j >= P) break;
+                        if (sc[j] > m[j]) {
+                            const float corr = fast_ex2(m[j] - sc[j]);   // m = -inf -> 0
+                            l[j] *= corr;
+#pragma unroll
+                            for (int e = 0; e < DPL; ++e) o[j][e] *= corr;
+                            m[j] = sc[j];
+                        }
+                        const float pr = fast_ex2(sc[j] - m[j]);
+                        l[j] += pr;
+#pragma unroll
+                        for (int e = 0; e < DPL; ++e) o[j][e] = fmaf(pr, vf[e], o[j][e]);
+                    }
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);   // this warp is done with the stage
         }
+        // merge the groups of the warp (lanes gl, gl + LPR, ... hold the same dims)
 #pragma unroll
-        for (int j = 0; j < PMAX; ++j) {
-            if (j >= P) break;   // P is the same on every lane
-            float sc = 0.f;
+        for (int off = LPR; off < 32; off <<= 1) {
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) sc = fmaf(q[j][e], kf[e], sc);
-            sc += __shfl_xor_sync(0xffffffffu, sc, 4);
-            sc += __shfl_xor_sync(0xffffffffu, sc, 2);
-            sc += __shfl_xor_sync(0xffffffffu, sc, 1);   // the group's score in log2 units
-            if (valid) {                                 // uniform over the group
-                if (sc > m[j]) {
-                    const float corr = exp2f(m[j] - sc);     // m = -inf -> 0
-                    l[j] *= corr;
+            for (int j = 0; j < PMAX; ++j) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m[j], off);
+                const float l2 = __shfl_xor_sync(0xffffffffu, l[j], off);
+                const float mn = fmaxf(m[j], m2);
+                const float c1 = m[j] == -INFINITY ? 0.f : exp2f(m[j] - mn);
+                const float c2 = m2 == -INFINITY ? 0.f : exp2f(m2 - mn);
+                l[j] = l[j] * c1 + l2 * c2;
 #pragma unroll
-                    for (int e = 0; e < DPL; ++e) o[j][e] *= corr;
-                    m[j] = sc;
+                for (int e = 0; e < DPL; ++e) {
+                    const float o2 = __shfl_xor_sync(0xffffffffu, o[j][e], off);
+                    o[j][e] = o[j][e] * c1 + o2 * c2;
                 }
-                const float pr = exp2f(sc - m[j]);
-                l[j] += pr;
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) o[j][e] = fmaf(pr, vf[e], o[j][e]);
+                m[j] = mn;
             }
         }
-    }
-    // merge the 4 groups of the warp (lanes gl, gl+8, gl+16, gl+24 hold the same dims)
+        if (grp == 0) {
 #pragma unroll
-    for (int off = 8; off <= 16; off <<= 1) {
+            for (int j = 0; j < PMAX; ++j) {
+                if (gl == 0) {
+                    sm_ml[warp][j][0] = m[j];
+                    sm_ml[warp][j][1] = l[j];
+                }
 #pragma unroll
-        for (int j = 0; j < PMAX; ++j) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m[j], off);
-            const float l2 = __shfl_xor_sync(0xffffffffu, l[j], off);
-            const float mn = fmaxf(m[j], m2);
-            const float c1 = m[j] == -INFINITY ? 0.f : exp2f(m[j] - mn);
-            const float c2 = m2 == -INFINITY ? 0.f : exp2f(m2 - mn);
-            l[j] = l[j] * c1 + l2 * c2;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) {
-                const float o2 = __shfl_xor_sync(0xffffffffu, o[j][e], off);
-                o[j][e] = o[j][e] * c1 + o2 * c2;
+                for (int e = 0; e < DPL; ++e) sm_o[warp][j][gl * DPL + e] = o[j][e];
             }
-            m[j] = mn;
-        }
-    }
-    // merge the 4 warps through shared memory: [warp][j] (m, l) and [warp][j][d] o
-    __shared__ float sm_ml[4][PMAX][2];
-    __shared__ float sm_o[4][PMAX][d];
-    if (grp == 0) {
-#pragma unroll
-        for (int j = 0; j < PMAX; ++j) {
-            if (gl == 0) {
-                sm_ml[warp][j][0] = m[j];
-                sm_ml[warp][j][1] = l[j];
-            }
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) sm_o[warp][j][gl * DPL + e] = o[j][e];
         }
     }
     __syncthreads();
+    // merge the consumer warps and write the chunk's partial result
     for (int i = threadIdx.x; i < P * d; i += blockDim.x) {
         const int j = i / d, c = i % d;
         float mn = -INFINITY;
-        for (int w = 0; w < 4; ++w) mn = fmaxf(mn, sm_ml[w][j][0]);
+        for (int w = 0; w < DA_CWARPS; ++w) mn = fmaxf(mn, sm_ml[w][j][0]);
         float lt = 0.f, ot = 0.f;
-        for (int w = 0; w < 4; ++w) {
+        for (int w = 0; w < DA_CWARPS; ++w) {
             const float mw = sm_ml[w][j][0];
             const float cw = mw == -INFINITY ? 0.f : exp2f(mw - mn);
             lt += sm_ml[w][j][1] * cw;
@@ -262,35 +359,43 @@ decode_attn(const __nv_bfloat16 *__restrict__ qt, const __nv_bfloat16 *__restric
 }
 
 // ---------------------------------------------------------------------------------------
-// 4. merge the chunks, normalise, R contraction; one CTA per b
+// 4a. merge the chunks of one (b, h', j): Pbar[b][h'*P + j][c], one thread per column
 // ---------------------------------------------------------------------------------------
-__global__ void decode_combine(const float *__restrict__ part_ml, const float *__restrict__ part_o,
-                               const float *__restrict__ R, int H, int d, int P, int nch, __nv_bfloat16 *__restrict__ out) {
-    extern __shared__ float pb[];   // Pbar[b] as [H*P][d], fp32
-    const int b = blockIdx.x, HP = H * P;
-    for (int i = threadIdx.x; i < HP * d; i += blockDim.x) {
-        const int k = i / d, c = i % d;             // k = h'*P + j
-        const size_t base = ((size_t)b * H + k / P) * nch;
-        const int j = k % P;
-        float mn = -INFINITY;
-        for (int ch = 0; ch < nch; ++ch) mn = fmaxf(mn, part_ml[((base + ch) * P + j) * 2]);
-        float lt = 0.f, ot = 0.f;
-        for (int ch = 0; ch < nch; ++ch) {
-            const size_t pidx = (base + ch) * P + j;
-            const float mc = part_ml[pidx * 2];
-            const float cw = mc == -INFINITY ? 0.f : exp2f(mc - mn);
-            lt += part_ml[pidx * 2 + 1] * cw;
-            ot += part_o[pidx * d + c] * cw;
-        }
-        pb[i] = lt > 0.f ? ot / lt : 0.f;
+__global__ void decode_merge(const float *__restrict__ part_ml, const float *__restrict__ part_o, int H, int d, int P,
+                             int nch, float *__restrict__ pbar) {
+    const int bh = blockIdx.x, j = blockIdx.y, c = threadIdx.x;
+    const size_t base = (size_t)bh * nch;
+    float mn = -INFINITY;
+    for (int ch = 0; ch < nch; ++ch) mn = fmaxf(mn, part_ml[((base + ch) * P + j) * 2]);
+    float lt = 0.f, ot = 0.f;
+    for (int ch = 0; ch < nch; ++ch) {
+        const size_t pidx = (base + ch) * P + j;
+        const float mc = part_ml[pidx * 2];
+        const float cw = mc == -INFINITY ? 0.f : exp2f(mc - mn);
+        lt += part_ml[pidx * 2 + 1] * cw;
+        ot += part_o[pidx * d + c] * cw;
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < H * d; i += blockDim.x) {
-        const int h = i / d, c = i % d;
-        float v = 0.f;
-        for (int k = 0; k < HP; ++k) v = fmaf(R[(size_t)h * HP + k], pb[k * d + c], v);
-        out[(size_t)b * H * d + i] = __float2bfloat16_rn(v);
+    pbar[((size_t)bh * P + j) * d + c] = lt > 0.f ? ot / lt : 0.f;   // [b][h'][j][c] = [b][h'*P + j][c]
+}
+
+// ---------------------------------------------------------------------------------------
+// 4b. R contraction: out[b][h][c] = sum_k R[h][k] Pbar[b][k][c], one CTA per (b, h)
+// ---------------------------------------------------------------------------------------
+__global__ void decode_contract(const float *__restrict__ pbar, const float *__restrict__ R, int H, int d, int P,
+                                __nv_bfloat16 *__restrict__ out) {
+    const int b = blockIdx.x, h = blockIdx.y, c = threadIdx.x, HP = H * P;
+    const float *pb = pbar + (size_t)b * HP * d;
+    float v = 0.f;
+    int k = 0;
+    for (; k + 8 <= HP; k += 8) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = pb[(size_t)(k + u) * d + c];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v = fmaf(R[(size_t)h * HP + k + u], x[u], v);
     }
+    for (; k < HP; ++k) v = fmaf(R[(size_t)h * HP + k], pb[(size_t)k * d + c], v);
+    out[((size_t)b * H + h) * d + c] = __float2bfloat16_rn(v);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -304,13 +409,14 @@ size_t decode_workspace_bytes(int B, int H, int d, int P) {
     auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
     const size_t D = (size_t)H * d;
     return al((size_t)DC_KS * B * 3 * D * 4) + al((size_t)B * H * P * d * 2) +
-           al((size_t)B * H * DC_NCH_MAX * P * 2 * 4) + al((size_t)B * H * DC_NCH_MAX * P * d * 4);
+           al((size_t)B * H * DC_NCH_MAX * P * 2 * 4) + al((size_t)B * H * DC_NCH_MAX * P * d * 4) +
+           al((size_t)B * H * P * d * 4);
 }
 
 cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const void *WV, const float *aQ,
                           const float *aK, const float *aV, const float *R, int B, int H, int d, int P, int mask_mode,
                           int window, void *Kc, void *Vc, long long cache_tokens, long long t, void *out, void *ws,
-                          cudaStream_t st) {
+                          cudaStream_t st, int *status) {
     auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
     const int D = H * d;
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -321,6 +427,8 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
     float *part_ml = reinterpret_cast<float *>(w);
     w += al((size_t)B * H * DC_NCH_MAX * P * 2 * 4);
     float *part_o = reinterpret_cast<float *>(w);
+    w += al((size_t)B * H * DC_NCH_MAX * P * d * 4);
+    float *pbar = reinterpret_cast<float *>(w);
     const long long cache_rows = cache_tokens * P;
 
     // 1. projections
@@ -333,15 +441,32 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
         D, Yp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 2. mixing + append
-    decode_mix<<<dim3(B, 3, H), d, 0, st>>>(Yp, aQ, aK, aV, B, H, d, P, t, cache_rows, qt, (__nv_bfloat16 *)Kc,
-                                            (__half *)Vc);
+    const size_t smem2 = ((size_t)D + (size_t)H * H * P) * 4;
+    e = cudaFuncSetAttribute(decode_mix, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+    if (e != cudaSuccess) return e;
+    const int nhg = H < 8 ? H : 8;
+    decode_mix<<<dim3(B, 3, nhg), 256, smem2, st>>>(Yp, aQ, aK, aV, B, H, d, P, t, cache_rows, qt, (__nv_bfloat16 *)Kc,
+                                               (__half *)Vc);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 3. attention over the readable cached rows [lo, hi]
     const long long hi = (t + 1) * P - 1;
     long long lo = 0;
     if (mask_mode == 2) lo = (t - window + 1) * P > 0 ? (t - window + 1) * P : 0;
     const long long rows = hi - lo + 1;
-    long long nch = (3LL * device_sm_count() + (long long)B * H - 1) / ((long long)B * H);
+    // one wave of resident CTAs: chunks per (b, h) = resident CTAs / (B * H)
+    int occ = 1;
+    if (d == 128) {
+        e = cudaFuncSetAttribute(decode_attn<16, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, da_smem_bytes<128>());
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_attn<16, 4>, DA_THREADS, da_smem_bytes<128>());
+    } else {
+        e = cudaFuncSetAttribute(decode_attn<8, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, da_smem_bytes<64>());
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_attn<8, 8>, DA_THREADS, da_smem_bytes<64>());
+    }
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+    long long nch = ((long long)occ * device_sm_count()) / ((long long)B * H);
     if (nch > (rows + 63) / 64) nch = (rows + 63) / 64;
     if (nch > DC_NCH_MAX) nch = DC_NCH_MAX;
     if (nch < 1) nch = 1;
@@ -349,18 +474,20 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
     nch = (rows + rpc - 1) / rpc;
     const float sl2 = 1.4426950408889634f / sqrtf((float)d);
     const dim3 g3((unsigned)nch, H, B);
-    if (d == 128)
-        decode_attn<16, 4><<<g3, DC_ATT_THREADS, 0, st>>>(qt, (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P,
-                                                          cache_rows, lo, hi, rpc, sl2, part_ml, part_o);
-    else
-        decode_attn<8, 8><<<g3, DC_ATT_THREADS, 0, st>>>(qt, (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P,
-                                                         cache_rows, lo, hi, rpc, sl2, part_ml, part_o);
+    if (d == 128) {
+        decode_attn<16, 4><<<g3, DA_THREADS, da_smem_bytes<128>(), st>>>(
+            qt, (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P, cache_rows, lo, hi, rpc, sl2, part_ml, part_o,
+            status);
+    } else {
+        decode_attn<8, 8><<<g3, DA_THREADS, da_smem_bytes<64>(), st>>>(
+            qt, (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P, cache_rows, lo, hi, rpc, sl2, part_ml, part_o,
+            status);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // 4. combine + contraction
-    const size_t smem4 = (size_t)H * P * d * 4;
-    e = cudaFuncSetAttribute(decode_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem4);
-    if (e != cudaSuccess) return e;
-    decode_combine<<<B, 256, smem4, st>>>(part_ml, part_o, R, H, d, P, (int)nch, (__nv_bfloat16 *)out);
+    // 4. merge the chunks, then the contraction
+    decode_merge<<<dim3(B * H, P), d, 0, st>>>(part_ml, part_o, H, d, P, (int)nch, pbar);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    decode_contract<<<dim3(B, H), d, 0, st>>>(pbar, R, H, d, P, (__nv_bfloat16 *)out);
     return cudaGetLastError();
 }
 
