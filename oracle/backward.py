@@ -1,0 +1,66 @@
+"""fp64 CPU oracle of the Interleaved Head Attention backward pass.
+
+TEST INFRASTRUCTURE ONLY: the tests and the benchmark's CPU leg call it; the product never
+does.  It shares no code with the CUDA path.
+
+Algorithm 1 ("Interleaved Head Attention" section 4) is written again here in plain PyTorch
+float64 CPU operations, step by step: the per-head projections X W_s^(m), the pseudo-head
+mixing with alpha_s, the j-major stacking of the P pseudo-blocks into a sequence of length
+P*N, masked softmax attention per head over that sequence (dense, the operator of
+"注意力机制" eq. (5.11); the mask reads the original position t of each stacked row),
+unstacking, and the R contraction with the heads concatenated.  The gradients of the output
+with respect to X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V and R are torch.autograd's chain
+rule through exactly these steps (for the softmax part the derivatives of
+"注意力机制" eqs. (5.24)-(5.31)).
+
+Pinned by tests/test_oracle_pins.py: its forward equals the C oracle's (itself pinned to
+the pages), and its gradients equal central finite differences of that forward.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+PARAMS = ("X", "W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")
+
+
+def _allowed(N: int, P: int, mask_mode: int, window: int) -> torch.Tensor:
+    """allowed[r, c] for j-major stacked rows r = j*N + t (original position t = r % N)."""
+    t = torch.arange(P * N) % N
+    tq, tk = t[:, None], t[None, :]
+    ok = torch.ones(P * N, P * N, dtype=torch.bool)
+    if mask_mode >= 1:
+        ok &= tk <= tq
+    if mask_mode == 2:
+        ok &= (tq - tk) < window
+    return ok
+
+
+def forward(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, *, H, d, P, mask_mode=0, window=0):
+    """out [B, N, H*d] of Algorithm 1 in float64 torch ops (differentiable)."""
+    B, N, D = X.shape
+    ok = _allowed(N, P, mask_mode, window)
+
+    def pseudo(W, alpha):
+        Y = (X @ W).reshape(B, N, H, d)                          # X W^(m): [b, t, m, c]
+        S = torch.einsum("mhj,btmc->bhjtc", alpha, Y)             # sum_m alpha[m,h,j] X W^(m)
+        return S.reshape(B, H, P * N, d)                          # j-major stacking: row j*N + t
+
+    Qb, Kb, Vb = pseudo(W_Q, alpha_Q), pseudo(W_K, alpha_K), pseudo(W_V, alpha_V)
+    S = (Qb @ Kb.transpose(-1, -2)) / math.sqrt(d)
+    S = S.masked_fill(~ok, float("-inf"))
+    A = torch.softmax(S, dim=-1)
+    Pb = A @ Vb                                                   # [b, h', j*N + t, c]
+    Pu = Pb.reshape(B, H, P, N, d).reshape(B, H * P, N, d)        # unstack: index h'*P + j
+    O = torch.einsum("hk,bktc->bthc", R, Pu)                      # sum R[h, h'P+j] P_{h',j}[t]
+    return O.reshape(B, N, H * d)
+
+
+def backward(inputs: dict, dO, *, H, d, P, mask_mode=0, window=0):
+    """Gradients of sum(out * dO) for every input of Algorithm 1; float64 numpy-compatible
+    tensors in, a dict of float64 tensors (same keys as PARAMS) out."""
+    leaves = {k: torch.as_tensor(inputs[k], dtype=torch.float64).clone().requires_grad_(True) for k in PARAMS}
+    out = forward(*(leaves[k] for k in PARAMS), H=H, d=d, P=P, mask_mode=mask_mode, window=window)
+    grads = torch.autograd.grad(out, [leaves[k] for k in PARAMS], torch.as_tensor(dO, dtype=torch.float64))
+    return {k: g.detach() for k, g in zip(PARAMS, grads)}

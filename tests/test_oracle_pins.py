@@ -482,3 +482,56 @@ def test_planted_mistakes_are_caught(golden, tmp_path):
         path.write_text(src.replace(old, new, 1))
         lib = oracle.build(force=True, src=str(path), out=str(tmp_path / f"mutant{i}.so"))
         assert _pin_suite(oracle.Oracle(lib), g) > 0, f"planted mistake not caught: {name}"
+
+
+# ---------------------------------------------------------------------------
+# the backward oracle (oracle/backward.py): its forward is the pinned C oracle's, and its
+# gradients are the derivatives of that forward (central finite differences)
+# ---------------------------------------------------------------------------
+
+BWD_CASES = [
+    # B, N, H, d, P, mask_mode, window
+    (2, 9, 3, 4, 2, 1, 0),
+    (1, 7, 2, 5, 3, 2, 3),
+    (1, 6, 2, 4, 1, 0, 0),
+    (2, 5, 2, 3, 4, 2, 1),
+]
+
+
+@pytest.mark.parametrize("case", BWD_CASES)
+def test_backward_oracle_forward_is_the_c_oracle(case):
+    """The autograd graph is Algorithm 1 as the C oracle computes it (same inputs, float64)."""
+    import torch
+    from oracle import backward as bwd
+    B, N, H, d, P, mode, w = case
+    p = rand_problem(RNG, B, N, H, d, P)
+    ref = run(oracle, p, H, d, P, mask_mode=mode, window=w)
+    got = bwd.forward(*(torch.as_tensor(p[k]) for k in bwd.PARAMS), H=H, d=d, P=P, mask_mode=mode,
+                      window=w).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("case", BWD_CASES)
+def test_backward_oracle_matches_finite_differences(case):
+    """<grad, v> equals the central difference of <out, dO> along a random direction v, for
+    every input of Algorithm 1 (X, the three W, the three alpha, R)."""
+    import torch
+    from oracle import backward as bwd
+    B, N, H, d, P, mode, w = case
+    rng = np.random.default_rng(777 + P)
+    p = rand_problem(rng, B, N, H, d, P)
+    dO = rng.standard_normal((B, N, H * d))
+    grads = bwd.backward(p, dO, H=H, d=d, P=P, mask_mode=mode, window=w)
+
+    def f(q):
+        out = bwd.forward(*(torch.as_tensor(q[k]) for k in bwd.PARAMS), H=H, d=d, P=P, mask_mode=mode, window=w)
+        return float((out.numpy() * dO).sum())
+
+    eps = 1e-6
+    for k in bwd.PARAMS:
+        v = rng.standard_normal(np.shape(p[k]))
+        plus = dict(p, **{k: p[k] + eps * v})
+        minus = dict(p, **{k: p[k] - eps * v})
+        fd = (f(plus) - f(minus)) / (2 * eps)
+        an = float((grads[k].numpy() * v).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (k, fd, an)
