@@ -272,6 +272,22 @@ IHA_API int iha_decode_step(const void *x, const void *W_Q, const void *W_K, con
                             void *K_cache, void *V_cache, int cache_tokens, int t, void *out,
                             int dtype, void *stream, void *workspace, size_t workspace_bytes);
 
+/* The backward pass of one IHA layer: given dO [B][N][H*d] (the gradient of a loss with
+ * respect to iha_forward's output for the same inputs), the gradients with respect to every
+ * input of Algorithm 1.  bf16 only, d in {64, 128}, H <= 16, H*P <= 128
+ * (IHA_ERR_UNSUPPORTED otherwise); every mask mode.
+ *   dX [B][N][H*d], dW_Q/dW_K/dW_V [H*d][H*d]: bfloat16, layouts of X and W;
+ *   dalpha_Q/K/V [H][H][P] and dR [H][H*P]: float32, layouts of alpha and R.
+ * The forward intermediates are recomputed inside the call.  workspace: NULL (allocated
+ * and freed on `stream`) or iha_backward_workspace_bytes(...) bytes, 256-byte aligned. */
+IHA_API size_t iha_backward_workspace_bytes(int B, int N, int H, int d, int P, int dtype);
+IHA_API int iha_backward(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                         const float *alpha_Q, const float *alpha_K, const float *alpha_V, const float *R,
+                         int B, int N, int H, int d, int P, int mask_mode, int window, const void *dO,
+                         void *dX, void *dW_Q, void *dW_K, void *dW_V,
+                         float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR,
+                         int dtype, void *stream, void *workspace, size_t workspace_bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -176,3 +176,27 @@ def test_decode_validation(iha):
     # prefill: the cache must hold the prompt
     assert iha.iha_prefill(*args, B, 50, H, d, P, 1, 0, fake, fake, fake, 49, 1) == iha.IHA_ERR_INVALID_ARG
     assert iha.iha_prefill(*args, B, 50, H, d, P, 0, 0, fake, fake, fake, 60, 1) == iha.IHA_ERR_INVALID_ARG
+
+
+def test_backward_validation(iha):
+    fake = 1 << 40                                           # never dereferenced
+    B, N, H, d, P = 2, 64, 4, 64, 2
+    assert iha.iha_backward_workspace_bytes(B, N, H, d, P, 1) > 0
+    assert iha.iha_backward_workspace_bytes(B, N, 20, d, P, 1) == 0      # H > 16
+    assert iha.iha_backward_workspace_bytes(B, N, 16, d, 9, 1) == 0      # H*P > 128
+    assert iha.iha_backward_workspace_bytes(B, N, H, d, P, 0) == 0       # fp32
+    ins = [fake] * 8
+    outs = [fake] * 8
+
+    def call(**kw):
+        a = dict(B=B, N=N, H=H, d=d, P=P, mode=1, window=0, dO=fake, dtype=1, ws=None, wsb=0, outs=outs)
+        a.update(kw)
+        return iha.iha_backward(*ins, a["B"], a["N"], a["H"], a["d"], a["P"], a["mode"], a["window"], a["dO"],
+                                *a["outs"], a["dtype"], None, a["ws"], a["wsb"])
+    assert call(dO=None) == iha.IHA_ERR_INVALID_ARG
+    assert call(outs=[fake] * 7 + [None]) == iha.IHA_ERR_INVALID_ARG
+    assert call(mode=2, window=0) == iha.IHA_ERR_INVALID_ARG
+    assert call(dtype=0) == iha.IHA_ERR_UNSUPPORTED
+    assert call(H=20) == iha.IHA_ERR_UNSUPPORTED
+    assert call(dO=fake + 8) == iha.IHA_ERR_INVALID_ARG                 # dO is read by TMA: 16-byte aligned
+    assert call(ws=fake, wsb=256) == iha.IHA_ERR_WORKSPACE

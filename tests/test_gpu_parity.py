@@ -393,3 +393,40 @@ def test_decode_from_empty_cache(iha):
                                   iha.IHA_DTYPE_BF16))
     torch.cuda.synchronize()
     assert_parity(w, o.double().cpu().numpy(), oracle_rows(w, inp))
+
+
+# ---------------------------------------------------------------------------
+# backward pass: every gradient against the fp64 autograd oracle (oracle/backward.py)
+# ---------------------------------------------------------------------------
+
+BWD_TOL = 3e-2   # RMS(err) <= BWD_TOL * RMS(ref) per gradient tensor
+
+
+@pytest.mark.parametrize("B,N,H,d,P,mode,window", [
+    (2, 40, 4, 64, 2, C, 0), (1, 37, 4, 64, 3, WN, 9), (1, 50, 2, 128, 4, C, 0),
+    (2, 33, 4, 64, 1, NM, 0), (1, 45, 16, 64, 2, WN, 20), (1, 70, 8, 128, 2, C, 0)])
+def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
+    from oracle import backward as bwd
+    w = gi.Workload("bwd", B=B, N=N, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=90 + P)
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    D = w.D
+    g = torch.Generator().manual_seed(1234 + N)
+    dO = torch.randn(B, N, D, generator=g).to(torch.bfloat16)
+    dev = lambda shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device="cuda:0")
+    out = {"X": dev((B, N, D)), "W_Q": dev((D, D)), "W_K": dev((D, D)), "W_V": dev((D, D)),
+           "alpha_Q": dev((H, H, P), torch.float32), "alpha_K": dev((H, H, P), torch.float32),
+           "alpha_V": dev((H, H, P), torch.float32), "R": dev((H, H * P), torch.float32)}
+    iha.check(iha.iha_backward(*(dinp[k] for k in bwd.PARAMS), B, N, H, d, P, mode, window,
+                               dO.to("cuda:0").contiguous(), *(out[k] for k in bwd.PARAMS), iha.IHA_DTYPE_BF16),
+              "iha_backward")
+    torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status()
+    assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
+    ref = bwd.backward(gi.as_f64(inp), dO.double(), H=H, d=d, P=P, mask_mode=mode, window=window)
+    for k in bwd.PARAMS:
+        got = out[k].double().cpu().numpy()
+        r = ref[k].numpy()
+        assert np.isfinite(got).all(), k
+        err = rms(got - r)
+        assert err <= BWD_TOL * rms(r), f"{k}: rms err {err:.3g} vs rms ref {rms(r):.3g}"

@@ -1,0 +1,136 @@
+// iha_backward.cu -- the C-ABI of the backward pass of one IHA layer (kernels in
+// k_backward.cu and the forward kernels it reuses).
+//
+// Step order (one stream, bf16 tensors, fp32 arithmetic):
+//   forward pieces:  Y = X [W_Q|W_K|W_V];  Q~K~V~ = mix(Y);  Pbar, lse = attention(Q~, K~, V~)
+//   dPbar  = the mixing of dO with R in alpha's place (stacked; dPbar_{h',j} = sum_h R[h,h'P+j] dO_h)
+//   dR     = sum over tokens and columns of dO_h Pbar_k                 (token_gram)
+//   D, dq~, dk~, dv~ from the attention rule                           (rowdot, bwd_attn_*)
+//   dalpha_s = sum over tokens and columns of Y_s,m dS~_s,hj           (token_gram)
+//   dY_s   = the contraction of dS~_s with alpha_s in R's place        (contract_tc)
+//   dX     = sum_s dY_s W_s^T,  dW_s = X^T dY_s                        (gemm_strided)
+#include <cuda_runtime.h>
+
+#include "iha.h"
+#include "iha_internal.h"
+
+namespace iha {
+cudaError_t launch_bwd_rowdot(const void *dPst, const void *Pbar, const Shape &sh, float *Dv, cudaStream_t st);
+cudaError_t launch_bwd_attention(const void *QKV, const void *dPst, const float *lse, const float *Dv, const Shape &sh,
+                                 int mask_mode, int window, void *dQtm, void *dKtm, void *dVtm, cudaStream_t st);
+size_t bwd_gram_part_floats(long long ntok, int NA, int NB);
+cudaError_t launch_bwd_gram(const void *U, long long us, int NA, const void *V, long long vs, int NB, int d,
+                            long long ntok, float *part, float *out, cudaStream_t st);
+cudaError_t launch_bwd_gemm(const void *A, long long am, long long ak, const void *Bm, long long bk, long long bn, int M,
+                            int N, int K, float *C, bool accumulate, cudaStream_t st);
+cudaError_t launch_bwd_to_bf16(const float *in, long long n, void *out, cudaStream_t st);
+
+struct BwdLayout {
+    size_t y, qkv, pbar, lse, dpst, dv, ds, dy, cacc, part, total;
+};
+
+static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static BwdLayout bwd_layout(const Shape &sh) {
+    const size_t T = (size_t)sh.B * sh.N, D = (size_t)sh.D(), HP = (size_t)sh.H * sh.P, L = (size_t)sh.L();
+    const size_t BHL = (size_t)sh.B * sh.H * L;
+    BwdLayout l{};
+    size_t o = 0;
+    l.y = o;    o += al256(3 * T * D * 2);
+    l.qkv = o;  o += al256(3 * (size_t)sh.qkv_elems() * 2);
+    l.pbar = o; o += al256(T * HP * sh.d * 2);
+    l.lse = o;  o += al256(BHL * 4);
+    l.dpst = o; o += al256(BHL * sh.d * 2);
+    l.dv = o;   o += al256(BHL * 4);
+    l.ds = o;   o += al256(3 * T * HP * sh.d * 2);
+    l.dy = o;   o += al256(3 * T * D * 2);
+    l.cacc = o; o += al256((T * D > D * D ? T * D : D * D) * 4);
+    l.part = o; o += al256(bwd_gram_part_floats((long long)T, sh.H, (int)HP) * 4);
+    l.total = o;
+    return l;
+}
+
+static bool bwd_supported(const Shape &sh, int dtype) {
+    return dtype == IHA_DTYPE_BF16 && (sh.d == 64 || sh.d == 128) && sh.H <= 16 && sh.H * sh.P <= 128;
+}
+
+}  // namespace iha
+
+using namespace iha;
+
+extern "C" {
+
+size_t iha_backward_workspace_bytes(int B, int N, int H, int d, int P, int dtype) {
+    if (iha_workspace_bytes(B, N, H, d, P, dtype) == 0) return 0;   // the forward's shape checks
+    const Shape sh{B, N, H, d, P};
+    if (!bwd_supported(sh, dtype)) return 0;
+    return bwd_layout(sh).total;
+}
+
+int iha_backward(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
+                 const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
+                 int mask_mode, int window, const void *dO, void *dX, void *dW_Q, void *dW_K, void *dW_V,
+                 float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR, int dtype, void *stream,
+                 void *workspace, size_t workspace_bytes) {
+    int rc = check_forward_args(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window,
+                                dO, dtype);
+    if (rc != IHA_OK) return rc;
+    if (!dX || !dW_Q || !dW_K || !dW_V || !dalpha_Q || !dalpha_K || !dalpha_V || !dR) return IHA_ERR_INVALID_ARG;
+    const Shape sh{B, N, H, d, P};
+    if (!bwd_supported(sh, dtype)) return IHA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(dO) & 15) != 0) return IHA_ERR_INVALID_ARG;   // read by TMA
+    const BwdLayout lay = bwd_layout(sh);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool own = false;
+    if (!workspace) {
+        if (cudaMallocAsync(&workspace, lay.total, st) != cudaSuccess) return IHA_ERR_CUDA;
+        own = true;
+    } else if (workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255)) {
+        return IHA_ERR_WORKSPACE;
+    }
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int *status = status_word_ptr();
+    const long long T = (long long)B * N, D = sh.D(), HP = (long long)H * P;
+    uint8_t *Y = ws + lay.y, *QKV = ws + lay.qkv, *Pbar = ws + lay.pbar, *dPst = ws + lay.dpst, *dS = ws + lay.ds,
+            *dY = ws + lay.dy;
+    float *lse = reinterpret_cast<float *>(ws + lay.lse), *Dv = reinterpret_cast<float *>(ws + lay.dv);
+    float *C = reinterpret_cast<float *>(ws + lay.cacc), *part = reinterpret_cast<float *>(ws + lay.part);
+    const size_t ds_bytes = (size_t)T * HP * d * 2, dy_bytes = (size_t)T * D * 2;
+    const void *W[3] = {W_Q, W_K, W_V};
+    const float *alpha[3] = {alpha_Q, alpha_K, alpha_V};
+    float *dalpha[3] = {dalpha_Q, dalpha_K, dalpha_V};
+    void *dW[3] = {dW_Q, dW_K, dW_V};
+
+    cudaError_t e = launch_project_heads(X, W_Q, W_K, W_V, sh, Y, st, status);
+    if (e == cudaSuccess) e = launch_mix(Y, alpha_Q, alpha_K, alpha_V, sh, QKV, st, status);
+    if (e == cudaSuccess) e = launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, lse, st, status);
+    // dPbar (stacked) = dO mixed with R in alpha's place
+    if (e == cudaSuccess) e = launch_mix_sets(dO, R, R, R, sh, 1, dPst, st, status);
+    if (e == cudaSuccess) e = launch_bwd_gram(dO, D, H, Pbar, HP * d, (int)HP, d, T, part, dR, st);
+    if (e == cudaSuccess) e = launch_bwd_rowdot(dPst, Pbar, sh, Dv, st);
+    if (e == cudaSuccess)
+        e = launch_bwd_attention(QKV, dPst, lse, Dv, sh, mask_mode, window, dS, dS + ds_bytes, dS + 2 * ds_bytes, st);
+    for (int s = 0; s < 3 && e == cudaSuccess; ++s) {
+        const uint8_t *dSs = dS + s * ds_bytes;
+        uint8_t *dYs = dY + s * dy_bytes;
+        // dalpha_s[m][h*P + j] = sum_t,c Y_s[t][m][c] dS~_s[t][h*P + j][c]
+        e = launch_bwd_gram(Y + (size_t)s * D * 2, 3 * D, H, dSs, HP * d, (int)HP, d, T, part, dalpha[s], st);
+        // dY_s[t][m][c] = sum_hj alpha_s[m][hj] dS~_s[t][hj][c]
+        if (e == cudaSuccess) e = launch_contract_tc(dSs, alpha[s], sh, dYs, st, status);
+        // dX += dY_s W_s^T
+        if (e == cudaSuccess) e = launch_bwd_gemm(dYs, D, 1, W[s], 1, D, (int)T, (int)D, (int)D, C, s > 0, st);
+    }
+    if (e == cudaSuccess) e = launch_bwd_to_bf16(C, T * D, dX, st);
+    for (int s = 0; s < 3 && e == cudaSuccess; ++s) {
+        // dW_s[k][n] = sum_t X[t][k] dY_s[t][n]
+        e = launch_bwd_gemm(X, 1, D, dY + s * dy_bytes, D, 1, (int)D, (int)D, (int)T, C, false, st);
+        if (e == cudaSuccess) e = launch_bwd_to_bf16(C, D * D, dW[s], st);
+    }
+    if (own) {
+        const cudaError_t e2 = cudaFreeAsync(workspace, st);
+        if (e == cudaSuccess) e = e2;
+    }
+    return e == cudaSuccess ? IHA_OK : IHA_ERR_CUDA;
+}
+
+}  // extern "C"

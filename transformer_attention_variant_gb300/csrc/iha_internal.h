@@ -65,6 +65,14 @@ inline bool unfolded_route(const Shape &sh, int dtype) {
     return dtype == 1 && sh.P >= 2 && sh.H <= 16 && sh.H * sh.P <= 128;
 }
 
+// The mixing kernel for nsets projections: Y [t][nsets][H][d] -> QKV [nsets][B][H][N*P][d].
+cudaError_t launch_mix_sets(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh,
+                            int nsets, void *QKV, cudaStream_t st, int *status);
+
+// Attention that also writes each stacked row's log2 softmax normaliser (bf16 only).
+cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
+                                 void *Pbar, float *lse, cudaStream_t st, int *status);
+
 // Step 3: masked softmax attention per head over the stacked sequence -> Pbar [B][N][H][P][d].
 cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
                              void *Pbar, cudaStream_t st, int *status);

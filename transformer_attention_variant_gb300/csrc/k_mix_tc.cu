@@ -59,7 +59,8 @@ struct MixParams {
     int tpt;              // tokens per tile (G * tpg)
     int stg_bytes;        // one staging buffer: H * mix_head_stride(G, P)
     int nstg;             // staging buffers (2..4)
-    long long num_tiles;  // 3 * ceil(ntok / tpt)
+    int nsets;            // mixed projections: 3 (Q, K, V) or 1
+    long long num_tiles;  // nsets * ceil(ntok / tpt)
     int *status;
 };
 
@@ -151,8 +152,8 @@ mix_tc(const __grid_constant__ CUtensorMap tmY, const float *__restrict__ aQ, co
             int stage = 0;
             uint32_t phase = 0;
             for (long long tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-                const long long tb = tile / 3;
-                const int s = (int)(tile % 3);
+                const long long tb = tile / p.nsets;
+                const int s = (int)(tile % p.nsets);
                 if (!mbar_wait_lazy(&empty[stage], phase ^ 1, p.status, kSiteMixProducer, abort_flag)) break;
                 mbar_arrive_expect_tx(&full[stage], G * MX_GROUP_BYTES);
                 // group g, token i, c half hf -> 64-column chunk i*halves + hf of group g's B
@@ -162,7 +163,7 @@ mix_tc(const __grid_constant__ CUtensorMap tmY, const float *__restrict__ aQ, co
                         for (int hf = 0; hf < halves; ++hf)
                             tma_load_3d(&tmY, &full[stage],
                                         sB + stage * MX_B_BYTES + g * MX_GROUP_BYTES + (i * halves + hf) * (16 * 128),
-                                        hf * 64, 0, (int)((tb * p.tpt + g * p.tpg + i) * 3 + s));
+                                        hf * 64, 0, (int)((tb * p.tpt + g * p.tpg + i) * p.nsets + s));
                 if (++stage == MX_STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -176,7 +177,7 @@ mix_tc(const __grid_constant__ CUtensorMap tmY, const float *__restrict__ aQ, co
             uint32_t phase = 0;
             int it = 0;
             for (long long tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-                const int s = (int)(tile % 3);
+                const int s = (int)(tile % p.nsets);
                 const int acc = it % MX_NACC;
                 if (!mbar_wait(&tempty[acc], ((it / MX_NACC) & 1) ^ 1, p.status, kSiteMixMma, abort_flag)) break;
                 if (!mbar_wait(&full[stage], phase, p.status, kSiteMixMma, abort_flag)) break;
@@ -206,8 +207,8 @@ mix_tc(const __grid_constant__ CUtensorMap tmY, const float *__restrict__ aQ, co
         const bool issuer = warp == 2 && lane < H;   // sends head `lane`'s run of each tile
         int it = 0, sb = 0;
         for (long long tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-            const long long tb = tile / 3;
-            const int s = (int)(tile % 3);
+            const long long tb = tile / p.nsets;
+            const int s = (int)(tile % p.nsets);
             const int acc = it % MX_NACC;
             uint8_t *stg = sStg + sb * p.stg_bytes;
             if (++sb == p.nstg) sb = 0;
@@ -278,15 +279,15 @@ mix_tc(const __grid_constant__ CUtensorMap tmY, const float *__restrict__ aQ, co
     }
 }
 
-cudaError_t launch_mix(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh, void *QKV,
-                       cudaStream_t st, int *status) {
+cudaError_t launch_mix_sets(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh,
+                            int nsets, void *QKV, cudaStream_t st, int *status) {
     if ((sh.d != 64 && sh.d != 128) || sh.H > MX_K || sh.H * sh.P > MX_M) return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(QKV) & 15) != 0) return cudaErrorInvalidValue;   // bulk-copy alignment
     const long long ntok = (long long)sh.B * sh.N;
     CUtensorMap tmY;
     {
-        // Y [t][s][m][c] viewed as (c, m, t*3 + s); boxes of [16 m][64 c]
-        const uint64_t dims[3] = {(uint64_t)sh.d, (uint64_t)sh.H, (uint64_t)(ntok * 3)};
+        // Y [t][s][m][c] viewed as (c, m, t*nsets + s); boxes of [16 m][64 c]
+        const uint64_t dims[3] = {(uint64_t)sh.d, (uint64_t)sh.H, (uint64_t)(ntok * nsets)};
         const uint64_t strides[2] = {(uint64_t)sh.d * 2, (uint64_t)sh.H * sh.d * 2};
         const uint32_t box[3] = {64, (uint32_t)MX_K, 1};
         if (!make_tmap_bf16(&tmY, Y, 3, dims, strides, box)) return cudaErrorInvalidValue;
@@ -305,7 +306,8 @@ cudaError_t launch_mix(const void *Y, const float *aQ, const float *aK, const fl
     p.stg_bytes = sh.H * mix_head_stride(p.G, sh.P);
     p.nstg = mix_staging_buffers(p.stg_bytes);
     if (p.nstg < 2) return cudaErrorInvalidValue;
-    p.num_tiles = 3 * ((ntok + p.tpt - 1) / p.tpt);
+    p.nsets = nsets;
+    p.num_tiles = nsets * ((ntok + p.tpt - 1) / p.tpt);
     p.status = status;
     const int smem = MX_SMEM_FIXED + p.nstg * p.stg_bytes;
     cudaError_t e = cudaFuncSetAttribute(mix_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -315,4 +317,11 @@ cudaError_t launch_mix(const void *Y, const float *aQ, const float *aK, const fl
     return cudaGetLastError();
 }
 
+}  // namespace iha
+
+namespace iha {
+cudaError_t launch_mix(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh, void *QKV,
+                       cudaStream_t st, int *status) {
+    return launch_mix_sets(Y, aQ, aK, aV, sh, 3, QKV, st, status);
+}
 }  // namespace iha
