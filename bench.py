@@ -569,6 +569,75 @@ def run_decode(args, w):
         dist.destroy_process_group()
 
 
+def run_backward(args, w):
+    """One backward pass of the layer (iha_backward, forward pieces recomputed inside) on
+    workload w; reports gradient passes per second and the algorithmic TFLOP/s (the
+    backward's flops: twice the forward's projections and mixing, 2.5x its attention
+    pairs, the contraction and token reductions)."""
+    rank, world, local, dist = dist_setup(args.gpus)
+    import transformer_attention_variant_gb300 as iha
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    B, N, H, d, P, D = w.B, w.N, w.H, w.d, w.P, w.D
+    host = gi.make_inputs(w)
+    dd = {k: v.to(dev).contiguous() for k, v in host.items()}
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    dO = torch.randn(B, N, D, generator=g, device=dev).to(torch.bfloat16)
+    keys = ("X", "W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")
+    outs = [torch.empty_like(dd[k]) for k in keys]
+    ws_bytes = iha.iha_backward_workspace_bytes(B, N, H, d, P, iha.IHA_DTYPE_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    wk = work(w)
+    # gradients: projections (dX and dW: 2x the head projections), mixing and contraction
+    # (2x each), attention (QK^T, dP, dS K, dS^T Q, P^T dO: 10 d flops per pair, 2.5x forward)
+    flops = 2 * wk["proj_heads"] + 2 * (wk["algorithmic"] - wk["proj_heads"] - wk["attn"]) + 2.5 * wk["attn"]
+
+    def step():
+        iha.check(iha.iha_backward(*(dd[k] for k in keys), B, N, H, d, P, w.mask_mode, w.window, dO, *outs,
+                                   iha.IHA_DTYPE_BF16, stream, ws, ws_bytes), "backward")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status(stream)
+    iha.check(rc, f"device status after timed steps ({code:#x})")
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    ms = max_over_ranks(ms, dist, dev)
+    barrier(dist)
+    if rank == 0:
+        tf = flops / (ms * 1e-3) / 1e12
+        line = {
+            "metric": "IHA backward (all input gradients) pseudo-tokens/s and TFLOP/s, 1 GPU per replica",
+            "value": job_value(world, wk["pseudo_tokens"], ms), "unit": "pseudo-tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": DATA,
+            "config": config_of(w, "flushed between steps (256 MiB write outside the timed events)"),
+            "tflops_algorithmic": tf,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16"], "traffic": None,
+                         "note": "whole backward (forward recomputed inside counts as overhead, not work)"},
+            "gpu_launches": None, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def traffic_per_launch(workload, kernel):
     """DRAM bytes (read + write) per launch recorded from ncu in profiles/dram_traffic.txt,
     provided the kernel's source is unchanged since that capture; None otherwise."""
@@ -604,6 +673,8 @@ def main():
                     help="time the four-local + one-global layer stack on the workload's shape instead")
     ap.add_argument("--decode", action="store_true",
                     help="time one decoding step over a full cache of the workload's shape instead")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (iha_backward) on the workload instead")
     ap.add_argument("--N", type=int, default=None,
                     help="shrink the workload's sequence length (smaller cases for profiler captures); "
                          "the window stays N/(2P) for windowed workloads")
@@ -620,6 +691,8 @@ def main():
         run_stack(args, w)
     elif args.decode:
         run_decode(args, w)
+    elif args.backward:
+        run_backward(args, w)
     else:
         run_gpu(args, w)
 
