@@ -5,10 +5,13 @@
 //   forward pieces:  Y = X [W_Q|W_K|W_V];  Q~K~V~ = mix(Y);  Pbar, lse = attention(Q~, K~, V~)
 //   dPbar  = the mixing of dO with R in alpha's place (stacked; dPbar_{h',j} = sum_h R[h,h'P+j] dO_h)
 //   dR     = sum over tokens and columns of dO_h Pbar_k                 (token_gram)
-//   D, dq~, dk~, dv~ from the attention rule                           (rowdot, bwd_attn_*)
+//   D      = rowdot(dPbar, Pbar)                                       (rowdot)
+//   dq~, dk~, dv~ from the attention rule, on the tensor cores           (bwd_attn_tc)
 //   dalpha_s = sum over tokens and columns of Y_s,m dS~_s,hj           (token_gram)
 //   dY_s   = the contraction of dS~_s with alpha_s in R's place        (contract_tc)
-//   dX     = sum_s dY_s W_s^T,  dW_s = X^T dY_s                        (gemm_strided)
+//   dX     = sum_s dY_s W_s^T,  dW_s = X^T dY_s                        (bwd_gemm_tc)
+// The attention gradients need Vbar in bf16 (its products with dPbar pair two bf16
+// operands); the forward's copy is f16, so the mixing runs once more for V in bf16.
 #include <cuda_runtime.h>
 
 #include "iha.h"
@@ -16,17 +19,19 @@
 
 namespace iha {
 cudaError_t launch_bwd_rowdot(const void *dPst, const void *Pbar, const Shape &sh, float *Dv, cudaStream_t st);
-cudaError_t launch_bwd_attention(const void *QKV, const void *dPst, const float *lse, const float *Dv, const Shape &sh,
-                                 int mask_mode, int window, void *dQtm, void *dKtm, void *dVtm, cudaStream_t st);
+cudaError_t launch_bwd_attention_tc(const void *Q, const void *K, const void *Vb, const void *dPst, const float *lse,
+                                    const float *Dv, const Shape &sh, int mask_mode, int window, void *dQ, void *dK,
+                                    void *dV, cudaStream_t st, int *status);
 size_t bwd_gram_part_floats(long long ntok, int NA, int NB);
 cudaError_t launch_bwd_gram(const void *U, long long us, int NA, const void *V, long long vs, int NB, int d,
                             long long ntok, float *part, float *out, cudaStream_t st);
-cudaError_t launch_bwd_gemm(const void *A, long long am, long long ak, const void *Bm, long long bk, long long bn, int M,
-                            int N, int K, float *C, bool accumulate, cudaStream_t st);
-cudaError_t launch_bwd_to_bf16(const float *in, long long n, void *out, cudaStream_t st);
+cudaError_t launch_bwd_dx_tc(const void *const dY[3], const void *const W[3], long long T, int D, void *dX,
+                             cudaStream_t st, int *status);
+cudaError_t launch_bwd_dw_tc(const void *X, const void *const dY[3], long long T, int D, void *const dW[3],
+                             cudaStream_t st, int *status);
 
 struct BwdLayout {
-    size_t y, qkv, pbar, lse, dpst, dv, ds, dy, cacc, part, total;
+    size_t y, qkv, vb, pbar, lse, dpst, dv, ds, dy, part, total;
 };
 
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -38,13 +43,13 @@ static BwdLayout bwd_layout(const Shape &sh) {
     size_t o = 0;
     l.y = o;    o += al256(3 * T * D * 2);
     l.qkv = o;  o += al256(3 * (size_t)sh.qkv_elems() * 2);
+    l.vb = o;   o += al256((size_t)sh.qkv_elems() * 2);
     l.pbar = o; o += al256(T * HP * sh.d * 2);
     l.lse = o;  o += al256(BHL * 4);
     l.dpst = o; o += al256(BHL * sh.d * 2);
     l.dv = o;   o += al256(BHL * 4);
     l.ds = o;   o += al256(3 * T * HP * sh.d * 2);
     l.dy = o;   o += al256(3 * T * D * 2);
-    l.cacc = o; o += al256((T * D > D * D ? T * D : D * D) * 4);
     l.part = o; o += al256(bwd_gram_part_floats((long long)T, sh.H, (int)HP) * 4);
     l.total = o;
     return l;
@@ -91,41 +96,40 @@ int iha_backward(const void *X, const void *W_Q, const void *W_K, const void *W_
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int *status = status_word_ptr();
     const long long T = (long long)B * N, D = sh.D(), HP = (long long)H * P;
-    uint8_t *Y = ws + lay.y, *QKV = ws + lay.qkv, *Pbar = ws + lay.pbar, *dPst = ws + lay.dpst, *dS = ws + lay.ds,
-            *dY = ws + lay.dy;
+    uint8_t *Y = ws + lay.y, *QKV = ws + lay.qkv, *Vb = ws + lay.vb, *Pbar = ws + lay.pbar, *dPst = ws + lay.dpst,
+            *dS = ws + lay.ds, *dY = ws + lay.dy;
     float *lse = reinterpret_cast<float *>(ws + lay.lse), *Dv = reinterpret_cast<float *>(ws + lay.dv);
-    float *C = reinterpret_cast<float *>(ws + lay.cacc), *part = reinterpret_cast<float *>(ws + lay.part);
+    float *part = reinterpret_cast<float *>(ws + lay.part);
     const size_t ds_bytes = (size_t)T * HP * d * 2, dy_bytes = (size_t)T * D * 2;
+    const size_t third = (size_t)sh.qkv_elems() * 2;
     const void *W[3] = {W_Q, W_K, W_V};
     const float *alpha[3] = {alpha_Q, alpha_K, alpha_V};
     float *dalpha[3] = {dalpha_Q, dalpha_K, dalpha_V};
     void *dW[3] = {dW_Q, dW_K, dW_V};
+    const void *dYs[3] = {dY, dY + dy_bytes, dY + 2 * dy_bytes};
 
     cudaError_t e = launch_project_heads(X, W_Q, W_K, W_V, sh, Y, st, status);
     if (e == cudaSuccess) e = launch_mix(Y, alpha_Q, alpha_K, alpha_V, sh, QKV, st, status);
     if (e == cudaSuccess) e = launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, lse, st, status);
+    // Vbar again, in bf16: the V third of Y mixed with alpha_V
+    if (e == cudaSuccess)
+        e = launch_mix_sets(Y + (size_t)2 * D * 2, alpha_V, alpha_V, alpha_V, sh, 1, Vb, st, status, 3, -1);
     // dPbar (stacked) = dO mixed with R in alpha's place
     if (e == cudaSuccess) e = launch_mix_sets(dO, R, R, R, sh, 1, dPst, st, status);
     if (e == cudaSuccess) e = launch_bwd_gram(dO, D, H, Pbar, HP * d, (int)HP, d, T, part, dR, st);
     if (e == cudaSuccess) e = launch_bwd_rowdot(dPst, Pbar, sh, Dv, st);
     if (e == cudaSuccess)
-        e = launch_bwd_attention(QKV, dPst, lse, Dv, sh, mask_mode, window, dS, dS + ds_bytes, dS + 2 * ds_bytes, st);
+        e = launch_bwd_attention_tc(QKV, QKV + third, Vb, dPst, lse, Dv, sh, mask_mode, window, dS, dS + ds_bytes,
+                                    dS + 2 * ds_bytes, st, status);
     for (int s = 0; s < 3 && e == cudaSuccess; ++s) {
         const uint8_t *dSs = dS + s * ds_bytes;
-        uint8_t *dYs = dY + s * dy_bytes;
         // dalpha_s[m][h*P + j] = sum_t,c Y_s[t][m][c] dS~_s[t][h*P + j][c]
         e = launch_bwd_gram(Y + (size_t)s * D * 2, 3 * D, H, dSs, HP * d, (int)HP, d, T, part, dalpha[s], st);
         // dY_s[t][m][c] = sum_hj alpha_s[m][hj] dS~_s[t][hj][c]
-        if (e == cudaSuccess) e = launch_contract_tc(dSs, alpha[s], sh, dYs, st, status);
-        // dX += dY_s W_s^T
-        if (e == cudaSuccess) e = launch_bwd_gemm(dYs, D, 1, W[s], 1, D, (int)T, (int)D, (int)D, C, s > 0, st);
+        if (e == cudaSuccess) e = launch_contract_tc(dSs, alpha[s], sh, dY + s * dy_bytes, st, status);
     }
-    if (e == cudaSuccess) e = launch_bwd_to_bf16(C, T * D, dX, st);
-    for (int s = 0; s < 3 && e == cudaSuccess; ++s) {
-        // dW_s[k][n] = sum_t X[t][k] dY_s[t][n]
-        e = launch_bwd_gemm(X, 1, D, dY + s * dy_bytes, D, 1, (int)D, (int)D, (int)T, C, false, st);
-        if (e == cudaSuccess) e = launch_bwd_to_bf16(C, D * D, dW[s], st);
-    }
+    if (e == cudaSuccess) e = launch_bwd_dx_tc(dYs, W, T, (int)D, dX, st, status);
+    if (e == cudaSuccess) e = launch_bwd_dw_tc(X, dYs, T, (int)D, dW, st, status);
     if (own) {
         const cudaError_t e2 = cudaFreeAsync(workspace, st);
         if (e == cudaSuccess) e = e2;

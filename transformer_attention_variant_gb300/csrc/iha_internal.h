@@ -32,6 +32,13 @@ enum WaitSite {
     kSiteContractEpilogue = 36,
     kSiteDecodeProducer = 37,
     kSiteDecodeConsumer = 38,
+    kSiteBwdProducer = 40,
+    kSiteBwdMma = 41,
+    kSiteBwdSoftmax = 42,
+    kSiteBwdEpilogue = 43,
+    kSiteBwdGemmProducer = 44,
+    kSiteBwdGemmMma = 45,
+    kSiteBwdGemmEpilogue = 46,
     kSiteSelfTest = 99,
 };
 
@@ -65,9 +72,11 @@ inline bool unfolded_route(const Shape &sh, int dtype) {
     return dtype == 1 && sh.P >= 2 && sh.H <= 16 && sh.H * sh.P <= 128;
 }
 
-// The mixing kernel for nsets projections: Y [t][nsets][H][d] -> QKV [nsets][B][H][N*P][d].
+// The mixing kernel for nsets projections: Y [t][y_sets][H][d] (the first nsets of each
+// token's y_sets blocks are mixed) -> QKV [nsets][B][H][N*P][d]; set f16_set is written as
+// f16 (2: Vbar for the forward's P V product; -1: every set bf16).
 cudaError_t launch_mix_sets(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh,
-                            int nsets, void *QKV, cudaStream_t st, int *status);
+                            int nsets, void *QKV, cudaStream_t st, int *status, int y_sets = -1, int f16_set = 2);
 
 // Attention that also writes each stacked row's log2 softmax normaliser (bf16 only).
 cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,

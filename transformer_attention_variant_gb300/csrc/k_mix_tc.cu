@@ -60,6 +60,7 @@ struct MixParams {
     int stg_bytes;        // one staging buffer: H * mix_head_stride(G, P)
     int nstg;             // staging buffers (2..4)
     int nsets;            // mixed projections: 3 (Q, K, V) or 1
+    int f16_set;          // the set written as f16 (-1: none)
     long long num_tiles;  // nsets * ceil(ntok / tpt)
     int *status;
 };
@@ -231,7 +232,7 @@ mix_tc(const __grid_constant__ CUtensorMap tmY, const float *__restrict__ aQ, co
                         const int ti = g * p.tpg + col / p.d, cc = col % p.d;   // token within the tile
                         uint4 v[4];
                         uint32_t *vw = reinterpret_cast<uint32_t *>(v);
-                        if (s == 2) {
+                        if (s == p.f16_set) {
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
                                 vw[i] = pack_f16x2(__uint_as_float(u[c][2 * i]), __uint_as_float(u[c][2 * i + 1]));
@@ -280,15 +281,18 @@ mix_tc(const __grid_constant__ CUtensorMap tmY, const float *__restrict__ aQ, co
 }
 
 cudaError_t launch_mix_sets(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh,
-                            int nsets, void *QKV, cudaStream_t st, int *status) {
+                            int nsets, void *QKV, cudaStream_t st, int *status, int y_sets, int f16_set) {
+    if (y_sets < 0) y_sets = nsets;
+    if (nsets != y_sets && nsets != 1) return cudaErrorInvalidValue;
     if ((sh.d != 64 && sh.d != 128) || sh.H > MX_K || sh.H * sh.P > MX_M) return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(QKV) & 15) != 0) return cudaErrorInvalidValue;   // bulk-copy alignment
     const long long ntok = (long long)sh.B * sh.N;
     CUtensorMap tmY;
     {
-        // Y [t][s][m][c] viewed as (c, m, t*nsets + s); boxes of [16 m][64 c]
+        // Y [t][s][m][c] viewed as (c, m, t*nsets + s); boxes of [16 m][64 c].  One set out
+        // of y_sets: the row stride skips the other sets.
         const uint64_t dims[3] = {(uint64_t)sh.d, (uint64_t)sh.H, (uint64_t)(ntok * nsets)};
-        const uint64_t strides[2] = {(uint64_t)sh.d * 2, (uint64_t)sh.H * sh.d * 2};
+        const uint64_t strides[2] = {(uint64_t)sh.d * 2, (uint64_t)(nsets == y_sets ? 1 : y_sets) * sh.H * sh.d * 2};
         const uint32_t box[3] = {64, (uint32_t)MX_K, 1};
         if (!make_tmap_bf16(&tmY, Y, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
@@ -307,6 +311,7 @@ cudaError_t launch_mix_sets(const void *Y, const float *aQ, const float *aK, con
     p.nstg = mix_staging_buffers(p.stg_bytes);
     if (p.nstg < 2) return cudaErrorInvalidValue;
     p.nsets = nsets;
+    p.f16_set = f16_set;
     p.num_tiles = nsets * ((ntok + p.tpt - 1) / p.tpt);
     p.status = status;
     const int smem = MX_SMEM_FIXED + p.nstg * p.stg_bytes;
