@@ -4,10 +4,10 @@
 // Step order (one stream, bf16 tensors, fp32 arithmetic):
 //   forward pieces:  Y = X [W_Q|W_K|W_V];  Q~K~V~ = mix(Y);  Pbar, lse = attention(Q~, K~, V~)
 //   dPbar  = the mixing of dO with R in alpha's place (stacked; dPbar_{h',j} = sum_h R[h,h'P+j] dO_h)
-//   dR     = sum over tokens and columns of dO_h Pbar_k                 (token_gram)
+//   dR     = sum over tokens and columns of dO_h Pbar_k                 (gram_tc)
 //   D      = rowdot(dPbar, Pbar)                                       (rowdot)
 //   dq~, dk~, dv~ from the attention rule, on the tensor cores           (bwd_attn_tc)
-//   dalpha_s = sum over tokens and columns of Y_s,m dS~_s,hj           (token_gram)
+//   dalpha_s = sum over tokens and columns of Y_s,m dS~_s,hj           (gram_tc)
 //   dY_s   = the contraction of dS~_s with alpha_s in R's place        (contract_tc)
 //   dX     = sum_s dY_s W_s^T,  dW_s = X^T dY_s                        (bwd_gemm_tc)
 // The attention gradients need Vbar in bf16 (its products with dPbar pair two bf16
@@ -18,13 +18,15 @@
 #include "iha_internal.h"
 
 namespace iha {
-cudaError_t launch_bwd_rowdot(const void *dPst, const void *Pbar, const Shape &sh, float *Dv, cudaStream_t st);
+cudaError_t launch_bwd_rowdot(const void *dPst, const void *Pbar, const Shape &sh, long long ld, float *Dv,
+                              cudaStream_t st);
+int bwd_ld_stride(long long L);
 cudaError_t launch_bwd_attention_tc(const void *Q, const void *K, const void *Vb, const void *dPst, const float *lse,
                                     const float *Dv, const Shape &sh, int mask_mode, int window, void *dQ, void *dK,
                                     void *dV, cudaStream_t st, int *status);
 size_t bwd_gram_part_floats(long long ntok, int NA, int NB);
 cudaError_t launch_bwd_gram(const void *U, long long us, int NA, const void *V, long long vs, int NB, int d,
-                            long long ntok, float *part, float *out, cudaStream_t st);
+                            long long ntok, float *part, float *out, cudaStream_t st, int *status);
 cudaError_t launch_bwd_dx_tc(const void *const dY[3], const void *const W[3], long long T, int D, void *dX,
                              cudaStream_t st, int *status);
 cudaError_t launch_bwd_dw_tc(const void *X, const void *const dY[3], long long T, int D, void *const dW[3],
@@ -32,6 +34,7 @@ cudaError_t launch_bwd_dw_tc(const void *X, const void *const dY[3], long long T
 
 struct BwdLayout {
     size_t y, qkv, vb, pbar, lse, dpst, dv, ds, dy, part, total;
+    size_t ld_bytes;   // lse and D: [B*H][bwd_ld_stride(L)] floats each
 };
 
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -39,15 +42,17 @@ static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 static BwdLayout bwd_layout(const Shape &sh) {
     const size_t T = (size_t)sh.B * sh.N, D = (size_t)sh.D(), HP = (size_t)sh.H * sh.P, L = (size_t)sh.L();
     const size_t BHL = (size_t)sh.B * sh.H * L;
+    const size_t BHLp = (size_t)sh.B * sh.H * bwd_ld_stride((long long)L);
     BwdLayout l{};
     size_t o = 0;
     l.y = o;    o += al256(3 * T * D * 2);
     l.qkv = o;  o += al256(3 * (size_t)sh.qkv_elems() * 2);
     l.vb = o;   o += al256((size_t)sh.qkv_elems() * 2);
     l.pbar = o; o += al256(T * HP * sh.d * 2);
-    l.lse = o;  o += al256(BHL * 4);
+    l.ld_bytes = BHLp * 4;
+    l.lse = o;  o += al256(BHLp * 4);
     l.dpst = o; o += al256(BHL * sh.d * 2);
-    l.dv = o;   o += al256(BHL * 4);
+    l.dv = o;   o += al256(BHLp * 4);
     l.ds = o;   o += al256(3 * T * HP * sh.d * 2);
     l.dy = o;   o += al256(3 * T * D * 2);
     l.part = o; o += al256(bwd_gram_part_floats((long long)T, sh.H, (int)HP) * 4);
@@ -108,23 +113,28 @@ int iha_backward(const void *X, const void *W_Q, const void *W_K, const void *W_
     void *dW[3] = {dW_Q, dW_K, dW_V};
     const void *dYs[3] = {dY, dY + dy_bytes, dY + 2 * dy_bytes};
 
-    cudaError_t e = launch_project_heads(X, W_Q, W_K, W_V, sh, Y, st, status);
+    // lse and D rows are padded so that every 64-row block of them starts 256 bytes into a
+    // 256-aligned row; the padding reads as 0 (its pairs are masked)
+    const int ld = bwd_ld_stride(sh.L());
+    cudaError_t e = cudaMemsetAsync(lse, 0, lay.ld_bytes, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(Dv, 0, lay.ld_bytes, st);
+    if (e == cudaSuccess) e = launch_project_heads(X, W_Q, W_K, W_V, sh, Y, st, status);
     if (e == cudaSuccess) e = launch_mix(Y, alpha_Q, alpha_K, alpha_V, sh, QKV, st, status);
-    if (e == cudaSuccess) e = launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, lse, st, status);
+    if (e == cudaSuccess) e = launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, lse, ld, st, status);
     // Vbar again, in bf16: the V third of Y mixed with alpha_V
     if (e == cudaSuccess)
         e = launch_mix_sets(Y + (size_t)2 * D * 2, alpha_V, alpha_V, alpha_V, sh, 1, Vb, st, status, 3, -1);
     // dPbar (stacked) = dO mixed with R in alpha's place
     if (e == cudaSuccess) e = launch_mix_sets(dO, R, R, R, sh, 1, dPst, st, status);
-    if (e == cudaSuccess) e = launch_bwd_gram(dO, D, H, Pbar, HP * d, (int)HP, d, T, part, dR, st);
-    if (e == cudaSuccess) e = launch_bwd_rowdot(dPst, Pbar, sh, Dv, st);
+    if (e == cudaSuccess) e = launch_bwd_gram(dO, D, H, Pbar, HP * d, (int)HP, d, T, part, dR, st, status);
+    if (e == cudaSuccess) e = launch_bwd_rowdot(dPst, Pbar, sh, ld, Dv, st);
     if (e == cudaSuccess)
         e = launch_bwd_attention_tc(QKV, QKV + third, Vb, dPst, lse, Dv, sh, mask_mode, window, dS, dS + ds_bytes,
                                     dS + 2 * ds_bytes, st, status);
     for (int s = 0; s < 3 && e == cudaSuccess; ++s) {
         const uint8_t *dSs = dS + s * ds_bytes;
         // dalpha_s[m][h*P + j] = sum_t,c Y_s[t][m][c] dS~_s[t][h*P + j][c]
-        e = launch_bwd_gram(Y + (size_t)s * D * 2, 3 * D, H, dSs, HP * d, (int)HP, d, T, part, dalpha[s], st);
+        e = launch_bwd_gram(Y + (size_t)s * D * 2, 3 * D, H, dSs, HP * d, (int)HP, d, T, part, dalpha[s], st, status);
         // dY_s[t][m][c] = sum_hj alpha_s[m][hj] dS~_s[t][hj][c]
         if (e == cudaSuccess) e = launch_contract_tc(dSs, alpha[s], sh, dY + s * dy_bytes, st, status);
     }

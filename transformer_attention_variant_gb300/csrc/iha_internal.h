@@ -39,6 +39,9 @@ enum WaitSite {
     kSiteBwdGemmProducer = 44,
     kSiteBwdGemmMma = 45,
     kSiteBwdGemmEpilogue = 46,
+    kSiteGramProducer = 47,
+    kSiteGramMma = 48,
+    kSiteGramEpilogue = 49,
     kSiteSelfTest = 99,
 };
 
@@ -78,9 +81,10 @@ inline bool unfolded_route(const Shape &sh, int dtype) {
 cudaError_t launch_mix_sets(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh,
                             int nsets, void *QKV, cudaStream_t st, int *status, int y_sets = -1, int f16_set = 2);
 
-// Attention that also writes each stacked row's log2 softmax normaliser (bf16 only).
+// Attention that also writes each stacked row's log2 softmax normaliser (bf16 only) into
+// lse[b*H + h][lse_stride] (lse_stride >= N*P).
 cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
-                                 void *Pbar, float *lse, cudaStream_t st, int *status);
+                                 void *Pbar, float *lse, int lse_stride, cudaStream_t st, int *status);
 
 // Step 3: masked softmax attention per head over the stacked sequence -> Pbar [B][N][H][P][d].
 cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,

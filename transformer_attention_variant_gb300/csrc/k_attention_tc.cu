@@ -86,8 +86,9 @@ struct AttnParams {
     int head_group;        // heads per scheduling group
     int stage_o;           // epilogue through shared memory and TMA (P divides 128)
     unsigned int *ticket;  // this launch's work counter (0 at launch)
-    float *lse;            // optional [B*H][L]: log2 of each row's softmax normaliser, scale
-                           // included (p = 2^(s*log2(e)/sqrt(d) - lse)); NULL: not written
+    float *lse;            // optional [B*H][lse_stride]: log2 of each row's softmax normaliser,
+                           // scale included (p = 2^(s*log2(e)/sqrt(d) - lse)); NULL: not written
+    int lse_stride;        // >= L
     int *status;
 };
 
@@ -564,7 +565,7 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             const bool have = ok && mbar_wait(&o_full[tile], n & 1, p.status, kSiteAttnEpilogue, abort_flag);
             if (have && p.lse) {
                 const int rr = it.qb * 2 * AT_BM + tile * AT_BM + row;
-                if (rr < p.L) p.lse[(size_t)it.bh * p.L + rr] = m_run + log2f(l_run);
+                if (rr < p.L) p.lse[(size_t)it.bh * p.lse_stride + rr] = m_run + log2f(l_run);
             }
             uint32_t ob[DH / 2];   // bf16 pairs of this row
             if (have) {
@@ -647,7 +648,7 @@ static unsigned int *attn_ticket(cudaStream_t st, cudaError_t &e) {
 
 template <int DH>
 static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mode, int window, void *Pbar,
-                                  float *lse, cudaStream_t st, int *status) {
+                                  float *lse, int lse_stride, cudaStream_t st, int *status) {
     using C = AttnCfg<DH>;
     const long long L = sh.L(), BH = (long long)sh.B * sh.H;
     const __nv_bfloat16 *base = (const __nv_bfloat16 *)QKV;
@@ -684,6 +685,7 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     p.num_qblocks = (int)((L + 2 * AT_BM - 1) / (2 * AT_BM));
     p.stage_o = stage_o ? 1 : 0;
     p.lse = lse;
+    p.lse_stride = lse_stride;
     p.status = status;
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
@@ -710,18 +712,18 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
 }
 
 cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
-                                 void *Pbar, float *lse, cudaStream_t st, int *status);
+                                 void *Pbar, float *lse, int lse_stride, cudaStream_t st, int *status);
 
 cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype, void *Pbar,
                              cudaStream_t st, int *status) {
-    return launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, nullptr, st, status);
+    return launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, nullptr, 0, st, status);
 }
 
 cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
-                                 void *Pbar, float *lse, cudaStream_t st, int *status) {
+                                 void *Pbar, float *lse, int lse_stride, cudaStream_t st, int *status) {
     if (dtype == 0) return launch_attention_f32(QKV, sh, mask_mode, window, Pbar, st);
-    if (sh.d == 128) return launch_attn_tc<128>(QKV, sh, mask_mode, window, Pbar, lse, st, status);
-    if (sh.d == 64) return launch_attn_tc<64>(QKV, sh, mask_mode, window, Pbar, lse, st, status);
+    if (sh.d == 128) return launch_attn_tc<128>(QKV, sh, mask_mode, window, Pbar, lse, lse_stride, st, status);
+    if (sh.d == 64) return launch_attn_tc<64>(QKV, sh, mask_mode, window, Pbar, lse, lse_stride, st, status);
     return cudaErrorInvalidValue;
 }
 

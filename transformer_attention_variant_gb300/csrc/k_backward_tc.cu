@@ -24,9 +24,16 @@
 // Roles (384 threads): warps 0-3 and 4-7 are two softmax warpgroups, one thread per
 // resident row, taking alternate blocks (TMEM buffers 0 / 1) so that one group's
 // exponentials overlap the other's MMAs; warp 8 = TMA producer (128B-swizzled tiles, a
-// 4-stage ring of moving blocks; it also stages the KV launch's lse/D of each block in
-// shared memory); warp 9 = MMA issuer.  The MMA order S(i), dP(i), [wait P(i-1)] acc(i-1),
-// S(i+1), ... keeps the tensor pipe busy while a block's exponentials run.
+// 4-stage ring of moving blocks; in the KV launch each slot also receives the block's lse
+// and D by bulk copy, on the same barrier); warp 9 = MMA issuer.  The MMA order S(i),
+// dP(i), [wait P(i-1)] acc(i-1), S(i+1), ... keeps the tensor pipe busy while a block's
+// exponentials run.
+// CTAs may run in clusters of BA_CLUSTER adjacent resident tiles that stream the same
+// blocks: each CTA loads a slice of every block and multicasts it to the cluster, and a
+// ring slot is refilled only after the MMA warps of all the cluster's CTAs have released
+// it.  Measured on the causal P=4 N=8192 and windowed N=4096 layers, clusters of 2 and 4
+// were 1-5% slower than single CTAs (the score products, not L2 streaming, bound these
+// kernels), so BA_CLUSTER is 1.
 // TMEM: buffer b: S at 128b, dP at 128b+64 (P^T / dS overwrite their first 32 columns as
 // bf16 pairs); accumulators at 256 (dK or dQ) and 256+d (dV).  512 columns.
 //
@@ -49,6 +56,7 @@ namespace iha {
 constexpr int BA_ROWS = 128;       // resident rows per CTA
 constexpr int BA_BLK = 64;         // streamed rows per block
 constexpr int BA_STAGES = 4;       // moving-block ring
+constexpr int BA_CLUSTER = 1;      // CTAs (adjacent resident tiles) sharing each streamed block
 constexpr int BA_THREADS = 384;
 constexpr int BA_LAUNCH_REGS = 168, BA_REGS_SOFTMAX = 216, BA_REGS_CONTROL = 72;
 static_assert(128 * BA_REGS_CONTROL + 256 * BA_REGS_SOFTMAX <= BA_THREADS * BA_LAUNCH_REGS, "register split");
@@ -58,7 +66,7 @@ struct BwdAttnCfg {
     static constexpr int CHUNKS = DH / 64;
     static constexpr int STAT_BYTES = BA_ROWS * DH * 2;   // one resident tile
     static constexpr int MOV_BYTES = BA_BLK * DH * 2;     // one streamed block
-    static constexpr int NBARS = 1 + 2 * BA_STAGES + 2 + 2 + 1 + 1;
+    static constexpr int NBARS = 1 + 2 * BA_STAGES + 2 + 2 + 2 + 1 + 1;
     static constexpr int LD_BYTES = BA_STAGES * 2 * BA_BLK * 4;   // lse and D of each ring slot
     static constexpr int CTRL_BYTES = 256;
     static constexpr int SMEM = 2 * STAT_BYTES + BA_STAGES * 2 * MOV_BYTES + LD_BYTES + CTRL_BYTES + 1024;
@@ -68,13 +76,14 @@ struct BwdAttnCfg {
 };
 
 struct BwdAttnParams {
-    const float *lse;        // [B*H][L]
-    const float *Dv;         // [B*H][L]
+    const float *lse;        // [B*H][ld]
+    const float *Dv;         // [B*H][ld]
     __nv_bfloat16 *out0;     // KV: dV, Q: dQ   (token-major [B*N][H*P][d])
     __nv_bfloat16 *out1;     // KV: dK
     int N, H, P, L;
     int mask_mode, window;
     int ntiles;              // resident tiles per head
+    int ld;                  // row stride of lse and D: L rounded up to BA_BLK (zero padding)
     float sl2;               // log2(e)/sqrt(d)
     float scale;             // 1/sqrt(d)
     int *status;
@@ -97,15 +106,19 @@ __device__ __forceinline__ void ba_query_interval(const BwdAttnParams &p, int c,
     if (p.mask_mode == 2) hi = min(hi, (t + p.window) * p.P - 1);
 }
 
-// The resident tile of this CTA and the blocks it streams: [mb0, mb0 + nmov).  Both
-// interval ends are nondecreasing in the row, so the union over the tile's rows is the
-// interval from its first row's lower end to its last row's upper end.
-template <bool KV>
+// The resident tile of this CTA and the blocks its cluster streams: [mb0, mb0 + nmov).
+// A cluster holds CS adjacent tiles (the grid is padded to a multiple of CS; padding tiles
+// have no rows) and streams the union of their ranges.  Both interval ends are
+// nondecreasing in the row, so that union runs from the first row's lower end to the last
+// row's upper end.
+template <bool KV, int CS>
 __device__ __forceinline__ void ba_range(const BwdAttnParams &p, int &tile, int &mb0, int &nmov) {
     // KV: early key tiles are read by the most queries (causal), Q: late query tiles read
-    // the most keys -- heaviest tiles first
-    tile = KV ? (int)blockIdx.x : p.ntiles - 1 - (int)blockIdx.x;
-    const int r0 = tile * BA_ROWS, r1 = min(r0 + BA_ROWS - 1, p.L - 1);
+    // the most keys -- heaviest clusters first
+    const int ncl = (int)gridDim.x / CS, c = (int)blockIdx.x / CS;
+    const int cl = KV ? c : ncl - 1 - c;
+    tile = cl * CS + (int)blockIdx.x % CS;
+    const int r0 = cl * CS * BA_ROWS, r1 = min((cl + 1) * CS * BA_ROWS - 1, p.L - 1);
     int lo0, hi0, lo1, hi1;
     if (KV) {
         ba_query_interval(p, r0, lo0, hi0);
@@ -125,8 +138,10 @@ __device__ __forceinline__ float ba_exp2(float x) {
 }
 
 // tmS1/tmS2: resident operands of the score and dP products (KV: K, V; Q: Q, dPbar), box
-// 128 rows; tmM1/tmM2: streamed (KV: Q, dPbar; Q: K, V), box 64 rows.  All [B*H][L][d] bf16.
-template <int DH, bool KV>
+// 128 rows; tmM1/tmM2: streamed (KV: Q, dPbar; Q: K, V), box 64/CS rows: each CTA of a
+// cluster loads one slice of every streamed block and multicasts it to all CS CTAs, so the
+// cluster reads each block from L2 once.  All [B*H][L][d] bf16.
+template <int DH, bool KV, int CS>
 __global__ void __launch_bounds__(BA_THREADS, 1)
 bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmS2,
             const __grid_constant__ CUtensorMap tmM1, const __grid_constant__ CUtensorMap tmM2,
@@ -142,7 +157,8 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
     uint64_t *mov_full = stat_full + 1;            // [BA_STAGES]
     uint64_t *mov_empty = mov_full + BA_STAGES;    // [BA_STAGES]
     uint64_t *s_full = mov_empty + BA_STAGES;      // [2]
-    uint64_t *p_full = s_full + 2;                 // [2]
+    uint64_t *dp_full = s_full + 2;                // [2]
+    uint64_t *p_full = dp_full + 2;                // [2]
     uint64_t *acc_full = p_full + 2;               // [1]
     uint64_t *drain = acc_full + 1;                // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -151,17 +167,19 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
     const int warp = warp_id(), lane = lane_id();
     const int bh = blockIdx.y;
     int tile, mb0, nmov;
-    ba_range<KV>(p, tile, mb0, nmov);
+    ba_range<KV, CS>(p, tile, mb0, nmov);
+    constexpr uint16_t kAll = (1u << CS) - 1;   // every CTA of the cluster
     const int row0 = tile * BA_ROWS;
 
     if (threadIdx.x == 0) {
         mbar_init(stat_full, 1);
         for (int s = 0; s < BA_STAGES; ++s) {
             mbar_init(&mov_full[s], 1);
-            mbar_init(&mov_empty[s], 1);
+            mbar_init(&mov_empty[s], CS);   // released by the MMA warp of every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
+            mbar_init(&dp_full[b], 1);
             mbar_init(&p_full[b], 4);   // lane 0 of each warp of the group
         }
         mbar_init(acc_full, 1);
@@ -183,6 +201,7 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    cluster_sync();   // every CTA's barriers are initialised before any multicast reaches them
 
     if (warp >= 8) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BA_REGS_CONTROL));
@@ -200,34 +219,31 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
                 }
             }
             int issued = 0;
+            const int slice = (int)cluster_ctarank() * (BA_BLK / CS);   // this CTA's rows of each block
             for (int i = 0; i < nmov; ++i) {
                 const int st = i % BA_STAGES;
                 if (!wait(&mov_empty[st], ((i / BA_STAGES) & 1) ^ 1)) break;
                 const int rb = (mb0 + i) * BA_BLK;
-                if (KV) {
-                    // lse and D of the block's 64 query rows (rows past the end: p = 0)
-                    float *ld = sLD + st * 2 * BA_BLK;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int r = rb + h * 32 + lane;
-                        const bool in = r < p.L;
-                        ld[h * 32 + lane] = in ? p.lse[(size_t)bh * p.L + r] : INFINITY;
-                        ld[BA_BLK + h * 32 + lane] = in ? p.Dv[(size_t)bh * p.L + r] : 0.f;
-                    }
-                    __syncwarp();
-                }
                 if (leader) {
-                    mbar_arrive_expect_tx(&mov_full[st], 2 * C::MOV_BYTES);
-                    uint8_t *dst = sM + st * 2 * C::MOV_BYTES;
+                    mbar_arrive_expect_tx(&mov_full[st], 2 * C::MOV_BYTES + (KV ? 2 * BA_BLK * 4 : 0));
+                    if (KV) {
+                        // lse and D of the block's 64 query rows (this CTA's own copy; rows past
+                        // the end are zero padding, and every pair with them is masked)
+                        float *ld = sLD + st * 2 * BA_BLK;
+                        bulk_load(ld, p.lse + (size_t)bh * p.ld + rb, BA_BLK * 4, &mov_full[st]);
+                        bulk_load(ld + BA_BLK, p.Dv + (size_t)bh * p.ld + rb, BA_BLK * 4, &mov_full[st]);
+                    }
+                    uint8_t *dst = sM + st * 2 * C::MOV_BYTES + slice * 128;
                     for (int c = 0; c < C::CHUNKS; ++c) {
-                        tma_load_3d(&tmM1, &mov_full[st], dst + c * (BA_BLK * 128), c * 64, rb, bh);
-                        tma_load_3d(&tmM2, &mov_full[st], dst + C::MOV_BYTES + c * (BA_BLK * 128), c * 64, rb, bh);
+                        tma_load_3d_mc(&tmM1, &mov_full[st], dst + c * (BA_BLK * 128), c * 64, rb + slice, bh, kAll);
+                        tma_load_3d_mc(&tmM2, &mov_full[st], dst + C::MOV_BYTES + c * (BA_BLK * 128), c * 64,
+                                       rb + slice, bh, kAll);
                     }
                 }
                 ++issued;
             }
-            // every copy this warp started has landed before the CTA may exit (the normal
-            // path has consumed them all already)
+            // every copy into this CTA (its own slices and the other CTAs') has landed before
+            // the CTA may exit (the normal path has consumed them all already)
             for (int k = issued - BA_STAGES > 0 ? issued - BA_STAGES : 0; k < issued; ++k)
                 mbar_wait(&mov_full[k % BA_STAGES], (k / BA_STAGES) & 1, p.status, kSiteBwdProducer, nullptr,
                           kWaitLimitNs);
@@ -244,6 +260,8 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
             const uint32_t s2_lo = sdesc_sw128_lo(smem_u32(sS + C::STAT_BYTES), 16);
             const uint32_t mk_lo = sdesc_sw128_lo(smem_u32(sM), 16);               // K-major view
             const uint32_t mn_lo = sdesc_sw128_lo(smem_u32(sM), BA_BLK * 128);     // MN-major view
+            // S(i) then dP(i) into buffer i&1, each committed on its own barrier so that the
+            // exponentials of S start while dP is still being computed
             auto issue_scores = [&](int i) {
                 const int st = i % BA_STAGES, b = i & 1;
                 const uint32_t m1 = (st * 2 * C::MOV_BYTES) >> 4, m2 = (st * 2 * C::MOV_BYTES + C::MOV_BYTES) >> 4;
@@ -253,12 +271,14 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
                     const uint32_t ob = ((kk / 4) * (BA_BLK * 128) + (kk % 4) * 32) >> 4;
                     mma_ss_w(tmem + b * 128, s1_lo + oa, mk_lo + m1 + ob, hi, idesc_s, kk > 0);
                 }
+                mma_commit(&s_full[b]);
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk) {
                     const uint32_t oa = ((kk / 4) * (BA_ROWS * 128) + (kk % 4) * 32) >> 4;
                     const uint32_t ob = ((kk / 4) * (BA_BLK * 128) + (kk % 4) * 32) >> 4;
                     mma_ss_w(tmem + b * 128 + 64, s2_lo + oa, mk_lo + m2 + ob, hi, idesc_s, kk > 0);
                 }
+                mma_commit(&dp_full[b]);
             };
             auto issue_acc = [&](int i) {
                 const int st = i % BA_STAGES, b = i & 1;
@@ -281,10 +301,7 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
                     ok = wait(&mov_full[st], (i / BA_STAGES) & 1);
                     if (!ok) break;
                     tc_fence_after();
-                    if (leader) {
-                        issue_scores(i);
-                        mma_commit(&s_full[i & 1]);
-                    }
+                    if (leader) issue_scores(i);
                 }
                 if (i >= 1) {
                     const int j = i - 1;
@@ -293,7 +310,7 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
                     tc_fence_after();
                     if (leader) {
                         issue_acc(j);
-                        mma_commit(&mov_empty[j % BA_STAGES]);
+                        mma_commit_mc(&mov_empty[j % BA_STAGES], kAll);
                         if (j == nmov - 1) mma_commit(acc_full);
                     }
                 }
@@ -318,8 +335,8 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
         }
         float lse_r = 0.f, D_r = 0.f;
         if (!KV && valid) {
-            lse_r = p.lse[(size_t)bh * p.L + R];
-            D_r = p.Dv[(size_t)bh * p.L + R];
+            lse_r = p.lse[(size_t)bh * p.ld + R];
+            D_r = p.Dv[(size_t)bh * p.ld + R];
         }
         const float sl2 = p.sl2;
         bool ok = true;
@@ -332,20 +349,12 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
             if (!ok) break;
             tc_fence_after();
             const uint32_t sc = tmem + lane_addr + grp * 128;
-            float s[BA_BLK], dp[BA_BLK];
+            float pv[BA_BLK];   // the scores, then the probabilities
             {
-                uint32_t u[32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tmem_ld32(sc + h * 32, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) s[h * 32 + e] = __uint_as_float(u[e]);
-                    tmem_ld32(sc + 64 + h * 32, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) dp[h * 32 + e] = __uint_as_float(u[e]);
-                }
+                uint32_t (&u)[BA_BLK] = *reinterpret_cast<uint32_t (*)[BA_BLK]>(pv);
+                tmem_ld32(sc, *reinterpret_cast<uint32_t (*)[32]>(u));
+                tmem_ld32(sc + 32, *reinterpret_cast<uint32_t (*)[32]>(u + 32));
+                tmem_ld_wait();
             }
             {
                 const int rb = (mb0 + i) * BA_BLK;
@@ -353,32 +362,52 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
                 if (__any_sync(0xffffffffu, a > 0 || b < BA_BLK - 1)) {
 #pragma unroll
                     for (int c = 0; c < BA_BLK; ++c)
-                        if (c < a || c > b) s[c] = -INFINITY;
+                        if (c < a || c > b) pv[c] = -INFINITY;
                 }
             }
-            uint32_t pw[BA_BLK / 2], dw[BA_BLK / 2];
+            const float4 *l4 = reinterpret_cast<const float4 *>(sLD + st * 2 * BA_BLK);
+            const float4 *d4 = l4 + BA_BLK / 4;
             if (KV) {
-                const float4 *l4 = reinterpret_cast<const float4 *>(sLD + st * 2 * BA_BLK);
-                const float4 *d4 = l4 + BA_BLK / 4;
+                uint32_t pw[BA_BLK / 2];
 #pragma unroll
                 for (int c4 = 0; c4 < BA_BLK / 4; ++c4) {
-                    const float4 l = l4[c4], dd = d4[c4];
-                    const float p0 = ba_exp2(fmaf(s[4 * c4 + 0], sl2, -l.x));
-                    const float p1 = ba_exp2(fmaf(s[4 * c4 + 1], sl2, -l.y));
-                    const float p2 = ba_exp2(fmaf(s[4 * c4 + 2], sl2, -l.z));
-                    const float p3 = ba_exp2(fmaf(s[4 * c4 + 3], sl2, -l.w));
-                    pw[2 * c4] = pack_bf16x2(p0, p1);
-                    pw[2 * c4 + 1] = pack_bf16x2(p2, p3);
-                    dw[2 * c4] = pack_bf16x2(p0 * (dp[4 * c4 + 0] - dd.x), p1 * (dp[4 * c4 + 1] - dd.y));
-                    dw[2 * c4 + 1] = pack_bf16x2(p2 * (dp[4 * c4 + 2] - dd.z), p3 * (dp[4 * c4 + 3] - dd.w));
+                    const float4 l = l4[c4];
+                    pv[4 * c4 + 0] = ba_exp2(fmaf(pv[4 * c4 + 0], sl2, -l.x));
+                    pv[4 * c4 + 1] = ba_exp2(fmaf(pv[4 * c4 + 1], sl2, -l.y));
+                    pv[4 * c4 + 2] = ba_exp2(fmaf(pv[4 * c4 + 2], sl2, -l.z));
+                    pv[4 * c4 + 3] = ba_exp2(fmaf(pv[4 * c4 + 3], sl2, -l.w));
+                    pw[2 * c4] = pack_bf16x2(pv[4 * c4], pv[4 * c4 + 1]);
+                    pw[2 * c4 + 1] = pack_bf16x2(pv[4 * c4 + 2], pv[4 * c4 + 3]);
                 }
-                tmem_st32(sc, pw);
+                tmem_st32(sc, pw);   // P^T over the S columns (dP is in other columns)
             } else {
 #pragma unroll
-                for (int c2 = 0; c2 < BA_BLK / 2; ++c2) {
-                    const float p0 = ba_exp2(fmaf(s[2 * c2], sl2, -lse_r));
-                    const float p1 = ba_exp2(fmaf(s[2 * c2 + 1], sl2, -lse_r));
-                    dw[c2] = pack_bf16x2(p0 * (dp[2 * c2] - D_r), p1 * (dp[2 * c2 + 1] - D_r));
+                for (int c = 0; c < BA_BLK; ++c) pv[c] = ba_exp2(fmaf(pv[c], sl2, -lse_r));
+            }
+            if (!mbar_wait(&dp_full[grp], jj & 1, p.status, kSiteBwdSoftmax, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t dw[BA_BLK / 2];
+            {
+                float dp[BA_BLK];
+                uint32_t (&u)[BA_BLK] = *reinterpret_cast<uint32_t (*)[BA_BLK]>(dp);
+                tmem_ld32(sc + 64, *reinterpret_cast<uint32_t (*)[32]>(u));
+                tmem_ld32(sc + 96, *reinterpret_cast<uint32_t (*)[32]>(u + 32));
+                tmem_ld_wait();
+                if (KV) {
+#pragma unroll
+                    for (int c4 = 0; c4 < BA_BLK / 4; ++c4) {
+                        const float4 dd = d4[c4];
+                        dw[2 * c4] = pack_bf16x2(pv[4 * c4] * (dp[4 * c4] - dd.x), pv[4 * c4 + 1] * (dp[4 * c4 + 1] - dd.y));
+                        dw[2 * c4 + 1] =
+                            pack_bf16x2(pv[4 * c4 + 2] * (dp[4 * c4 + 2] - dd.z), pv[4 * c4 + 3] * (dp[4 * c4 + 3] - dd.w));
+                    }
+                } else {
+#pragma unroll
+                    for (int c2 = 0; c2 < BA_BLK / 2; ++c2)
+                        dw[c2] = pack_bf16x2(pv[2 * c2] * (dp[2 * c2] - D_r), pv[2 * c2 + 1] * (dp[2 * c2 + 1] - D_r));
                 }
             }
             tmem_st32(sc + 64, dw);
@@ -424,6 +453,7 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();   // no CTA leaves while another may still multicast into it or release its slots
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -434,21 +464,38 @@ template <int DH, bool KV>
 static cudaError_t launch_bwd_attn_kernel(const CUtensorMap (&tm)[4], const BwdAttnParams &p, int BH,
                                           cudaStream_t st) {
     using C = BwdAttnCfg<DH>;
-    cudaError_t e = cudaFuncSetAttribute(bwd_attn_tc<DH, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    constexpr int CS = BA_CLUSTER;
+    auto kern = bwd_attn_tc<DH, KV, CS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, bwd_attn_tc<DH, KV>);
+    e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != BA_LAUNCH_REGS) return cudaErrorInvalidConfiguration;   // the register split needs it
-    const dim3 grid((unsigned)p.ntiles, (unsigned)BH);
-    if (KV)
-        bwd_attn_tc<DH, KV><<<grid, BA_THREADS, C::SMEM, st>>>(tm[1], tm[2], tm[0], tm[3], p);
-    else
-        bwd_attn_tc<DH, KV><<<grid, BA_THREADS, C::SMEM, st>>>(tm[0], tm[3], tm[1], tm[2], p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.ntiles + CS - 1) / CS * CS), (unsigned)BH);
+    cfg.blockDim = dim3(BA_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (KV) e = cudaLaunchKernelEx(&cfg, kern, tm[1], tm[2], tm[0], tm[3], p);
+    else e = cudaLaunchKernelEx(&cfg, kern, tm[0], tm[3], tm[1], tm[2], p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-// Q, K, Vb (bf16 copy of Vbar), dPst: stacked [B*H][L][d] bf16; lse, Dv [B*H][L];
+// Row stride of the lse and D arrays the attention-gradient kernels read: whole 64-row
+// blocks, so that each block is one 256-byte bulk copy.
+int bwd_ld_stride(long long L) { return (int)((L + BA_BLK - 1) / BA_BLK * BA_BLK); }
+
+// Q, K, Vb (bf16 copy of Vbar), dPst: stacked [B*H][L][d] bf16; lse, Dv [B*H][ld] (ld =
+// bwd_ld_stride(L), 256-byte aligned, padding zero);
 // dQ, dK, dV token-major [B*N][H*P][d] bf16.
 cudaError_t launch_bwd_attention_tc(const void *Q, const void *K, const void *Vb, const void *dPst, const float *lse,
                                     const float *Dv, const Shape &sh, int mask_mode, int window, void *dQ, void *dK,
@@ -456,13 +503,16 @@ cudaError_t launch_bwd_attention_tc(const void *Q, const void *K, const void *Vb
     if (sh.d != 64 && sh.d != 128) return cudaErrorInvalidValue;
     const long long L = sh.L(), BH = (long long)sh.B * sh.H;
     if (BH > 65535) return cudaErrorInvalidValue;
-    // maps [0] Q, [1] K, [2] Vb, [3] dPst with 64-row boxes (streamed) and 128-row boxes (resident)
+    if ((reinterpret_cast<uintptr_t>(lse) & 15) || (reinterpret_cast<uintptr_t>(Dv) & 15)) return cudaErrorInvalidValue;
+    static_assert(BA_BLK % (8 * BA_CLUSTER) == 0, "slices are whole 8-row swizzle atoms");
+    // maps [0] Q, [1] K, [2] Vb, [3] dPst with 128-row boxes (resident) and one cluster
+    // member's slice of a streamed block
     const void *src[4] = {Q, K, Vb, dPst};
     CUtensorMap big[4], small[4];
     for (int s = 0; s < 4; ++s) {
         const uint64_t dims[3] = {(uint64_t)sh.d, (uint64_t)L, (uint64_t)BH};
         const uint64_t strides[2] = {(uint64_t)sh.d * 2, (uint64_t)L * sh.d * 2};
-        const uint32_t box_b[3] = {64, BA_ROWS, 1}, box_s[3] = {64, BA_BLK, 1};
+        const uint32_t box_b[3] = {64, BA_ROWS, 1}, box_s[3] = {64, BA_BLK / BA_CLUSTER, 1};
         if (!make_tmap_bf16(&big[s], src[s], 3, dims, strides, box_b)) return cudaErrorInvalidValue;
         if (!make_tmap_bf16(&small[s], src[s], 3, dims, strides, box_s)) return cudaErrorInvalidValue;
     }
@@ -476,6 +526,7 @@ cudaError_t launch_bwd_attention_tc(const void *Q, const void *K, const void *Vb
     p.mask_mode = mask_mode;
     p.window = window;
     p.ntiles = (int)((L + BA_ROWS - 1) / BA_ROWS);
+    p.ld = bwd_ld_stride(L);
     p.scale = 1.f / sqrtf((float)sh.d);
     p.sl2 = 1.4426950408889634f * p.scale;
     p.status = status;
@@ -741,6 +792,195 @@ cudaError_t launch_bwd_dw_tc(const void *X, const void *const dY[3], long long T
     p.nprob = 3;
     p.status = status;
     return launch_bwd_gemm_kernel<true, true>(ta, tb, p, st);
+}
+
+}  // namespace iha
+
+namespace iha {
+
+// =========================================================================================
+// token gram: out[a][b] = sum over tokens t and c < d of U(t, a, c) V(t, b, c)
+// =========================================================================================
+// The gradients of the mixing matrices (alpha_s from Y_s and dS_s, R from dO and Pbar) are
+// sums over every token of a small product of two head blocks.  As one contraction over
+// K = (token, c) it is a GEMM with M = NB <= 128 rows (V, H*P head rows per token), N = NA
+// <= 16 (U, H head rows per token, padded to 16) and a very long K: the tensor cores do it
+// in a few cycles per token, so the kernel is a stream of both operands from HBM.  Each CTA
+// owns a contiguous token range, accumulates in TMEM and writes its partial [NA][NB]; a
+// second pass sums the partials in a fixed order.  Rows past NB / NA in a tile (the next
+// token's rows, or zero fill) only produce accumulator rows / columns that are ignored.
+constexpr int TG_M = 128, TG_N = 16, TG_STAGES = 8;
+constexpr int TG_A_BYTES = TG_M * 128, TG_B_BYTES = TG_N * 128;   // one 64-column chunk each
+constexpr int TG_THREADS = 192;
+constexpr int TG_SMEM = TG_STAGES * (TG_A_BYTES + TG_B_BYTES) + 256 + 1024;
+
+struct GramParams {
+    float *part;        // [gridDim.x][NA][NB]
+    int NA, NB, chunks; // chunks = d / 64
+    long long ntok;
+    int u_rows, v_rows; // rows of U / V per token in the tensor maps' row views
+    int *status;
+};
+
+__global__ void __launch_bounds__(TG_THREADS, 1)
+gram_tc(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmV, const GramParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + TG_STAGES * TG_A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + TG_STAGES * TG_B_BYTES);
+    uint64_t *empty = full + TG_STAGES;
+    uint64_t *done = empty + TG_STAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = warp_id(), lane = lane_id();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TG_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 32);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // this CTA's tokens
+    const long long per = (p.ntok + gridDim.x - 1) / gridDim.x;
+    const long long t0 = (long long)blockIdx.x * per, t1 = min(p.ntok, t0 + per);
+    const int nk = t1 > t0 ? (int)(t1 - t0) * p.chunks : 0;
+    const uint32_t bytes = (uint32_t)(p.NB + TG_N) * 128;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int k = 0; k < nk; ++k) {
+                const int st = k % TG_STAGES;
+                if (!mbar_wait_lazy(&empty[st], ((k / TG_STAGES) & 1) ^ 1, p.status, kSiteGramProducer, abort_flag))
+                    break;
+                const long long t = t0 + k / p.chunks;
+                const int c = (k % p.chunks) * 64;
+                mbar_arrive_expect_tx(&full[st], bytes);
+                tma_load_2d(&tmV, &full[st], sA + st * TG_A_BYTES, c, (int)(t * p.v_rows));
+                tma_load_2d(&tmU, &full[st], sB + st * TG_B_BYTES, c, (int)(t * p.u_rows));
+                ++issued;
+            }
+            for (int k = issued - TG_STAGES > 0 ? issued - TG_STAGES : 0; k < issued; ++k)
+                mbar_wait(&full[k % TG_STAGES], (k / TG_STAGES) & 1, p.status, kSiteGramProducer, nullptr, kWaitLimitNs);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(TG_M, TG_N, 0, 0);
+            bool ok = true;
+            for (int k = 0; k < nk; ++k) {
+                const int st = k % TG_STAGES;
+                if (!mbar_wait(&full[st], (k / TG_STAGES) & 1, p.status, kSiteGramMma, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + st * TG_A_BYTES), b0 = smem_u32(sB + st * TG_B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tmem, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024), idesc,
+                           (k | kk) != 0);
+                mma_commit(&empty[st]);
+            }
+            // arrives once every MMA issued above is done: the accumulator is final (and, if a
+            // wait gave up, no MMA is still writing TMEM when it is released)
+            mma_commit(done);
+            (void)ok;
+            mbar_wait(done, 0, p.status, kSiteGramMma, nullptr, kWaitLimitNs);
+        }
+    } else {
+        // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1; row m = b (V row), column n = a
+        const int q = warp & 3;
+        const int m = q * 32 + lane;
+        const bool have = nk > 0 && mbar_wait(done, 0, p.status, kSiteGramEpilogue, abort_flag);
+        uint32_t r[16];
+        if (have) {
+            tc_fence_after();
+            tmem_ld16(tmem + (uint32_t(q * 32) << 16), r);
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int n = 0; n < 16; ++n) r[n] = 0u;   // no tokens: a zero partial
+        }
+        if (m < p.NB) {
+            float *dst = p.part + (size_t)blockIdx.x * p.NA * p.NB;
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+                if (n < p.NA) dst[n * p.NB + m] = __uint_as_float(r[n]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 32);
+    }
+}
+
+__global__ void gram_sum(const float *__restrict__ part, int nparts, int n, float *__restrict__ out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float v = 0.f;
+    for (int k = 0; k < nparts; ++k) v += part[(size_t)k * n + i];
+    out[i] = v;
+}
+
+static int gram_ctas(long long ntok) {
+    const long long g = device_sm_count();
+    return (int)(ntok < g ? (ntok > 0 ? ntok : 1) : g);
+}
+
+size_t bwd_gram_part_floats(long long ntok, int NA, int NB) { return (size_t)gram_ctas(ntok) * NA * NB; }
+
+// out[a][b] = sum_t sum_c U[t*us + a*d + c] V[t*vs + b*d + c]  (bf16 U, V; us, vs multiples
+// of d; NA <= 16, NB <= 128, d in {64, 128}); part holds bwd_gram_part_floats floats.
+cudaError_t launch_bwd_gram(const void *U, long long us, int NA, const void *V, long long vs, int NB, int d,
+                            long long ntok, float *part, float *out, cudaStream_t st, int *status) {
+    if (NA < 1 || NA > TG_N || NB < 1 || NB > TG_M || (d != 64 && d != 128) || us % d || vs % d || ntok < 1)
+        return cudaErrorInvalidValue;
+    GramParams p{};
+    p.part = part;
+    p.NA = NA;
+    p.NB = NB;
+    p.chunks = d / 64;
+    p.ntok = ntok;
+    p.u_rows = (int)(us / d);
+    p.v_rows = (int)(vs / d);
+    p.status = status;
+    if ((long long)ntok * p.u_rows >= (1LL << 31) || (long long)ntok * p.v_rows >= (1LL << 31))
+        return cudaErrorInvalidValue;
+    CUtensorMap tmU, tmV;
+    {
+        // U as rows of d: row t*u_rows + a; only the rows up to the last token's are mapped
+        const uint64_t dims[2] = {(uint64_t)d, (uint64_t)((ntok - 1) * p.u_rows + NA)};
+        const uint64_t strides[1] = {(uint64_t)d * 2};
+        const uint32_t box[2] = {64, TG_N};
+        if (!make_tmap_bf16(&tmU, U, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)d, (uint64_t)((ntok - 1) * p.v_rows + NB)};
+        const uint64_t strides[1] = {(uint64_t)d * 2};
+        const uint32_t box[2] = {64, (uint32_t)NB};
+        if (!make_tmap_bf16(&tmV, V, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(gram_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, TG_SMEM);
+    if (e != cudaSuccess) return e;
+    const int g = gram_ctas(ntok);
+    gram_tc<<<g, TG_THREADS, TG_SMEM, st>>>(tmU, tmV, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int n = NA * NB;
+    gram_sum<<<(n + 255) / 256, 256, 0, st>>>(part, g, n, out);
+    return cudaGetLastError();
 }
 
 }  // namespace iha
