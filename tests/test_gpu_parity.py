@@ -344,10 +344,14 @@ def test_layer_stack(iha, P_local, N):
 # must be the row the forward pass gives that token of the whole sequence (the oracle)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("H,d,P,mode,window", [(4, 64, 2, C, 0), (4, 64, 8, WN, 5), (16, 128, 4, C, 0),
-                                                (3, 128, 3, WN, 20), (2, 128, 1, C, 0)])
-def test_decode_matches_oracle(iha, H, d, P, mode, window):
-    B, T, steps = 2, 37, 4
+@pytest.mark.parametrize("H,d,P,mode,window,T", [
+    (4, 64, 2, C, 0, 37), (4, 64, 8, WN, 5, 37), (16, 128, 4, C, 0, 37), (3, 128, 3, WN, 20, 37),
+    (2, 128, 1, C, 0, 37),
+    # long caches: many 128-row tiles per chunk, several chunks, a ragged last tile, and (window)
+    # a first readable row that is not tile-aligned
+    (2, 128, 4, C, 0, 700), (3, 128, 2, WN, 333, 900)])
+def test_decode_matches_oracle(iha, H, d, P, mode, window, T):
+    B, steps = 2, 4
     n_all = T + steps
     w = gi.Workload("decode", B=B, N=n_all, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=70 + P)
     inp = gi.make_inputs(w)
@@ -379,9 +383,10 @@ def test_decode_matches_oracle(iha, H, d, P, mode, window):
     assert_parity(w, out_prompt.reshape(B * T, D).double().cpu().numpy(), oracle_rows(w, inp, rows=rows_p))
 
 
-def test_decode_from_empty_cache(iha):
+@pytest.mark.parametrize("d,P", [(64, 2), (128, 4)])
+def test_decode_from_empty_cache(iha, d, P):
     """t = 0: the token reads only its own P pseudo-keys."""
-    B, H, d, P = 3, 4, 64, 2
+    B, H = 3, 4
     w = gi.Workload("decode0", B=B, N=1, H=H, d=d, P=P, mask_mode=C, window=0, dtype="bf16", seed=77)
     inp = gi.make_inputs(w)
     dinp = to_dev(inp)

@@ -42,6 +42,9 @@ enum WaitSite {
     kSiteGramProducer = 47,
     kSiteGramMma = 48,
     kSiteGramEpilogue = 49,
+    kSiteDecodeTcProducer = 50,
+    kSiteDecodeTcMma = 51,
+    kSiteDecodeTc = 52,
     kSiteSelfTest = 99,
 };
 

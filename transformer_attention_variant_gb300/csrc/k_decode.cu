@@ -7,7 +7,8 @@
 //   1. decode_proj:    y_s[b] = x[b] W_s (s = Q, K, V) as a split-K GEMV; W is read once.
 //   2. decode_mix:     q~/k~/v~_{h,j}[b] = sum_m alpha_s[m,h,j] y_s[b][m]; k~ and v~ go into
 //                      the cache at stacked row t*P + j, q~ into the workspace.
-//   3. decode_attn:    split-KV attention: a CTA takes a chunk of the cached rows of one
+//   3. decode_attn:    (d = 64; d = 128 runs decode_attn_tc, k_decode_tc.cu, on the tensor
+//                      cores) split-KV attention: a CTA takes a chunk of the cached rows of one
 //                      (b, h); a producer warp streams the chunk's K and V rows into a
 //                      6-stage shared-memory ring with bulk copies (about 96 KB in flight per
 //                      CTA); all P pseudo-queries share each row (eight lanes hold one key
@@ -401,6 +402,12 @@ __global__ void decode_contract(const float *__restrict__ pbar, const float *__r
 // ---------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------
+bool decode_tc_supported(int d, int P, const void *Kc, const void *Vc);
+int decode_tc_chunks(int B, int H, long long rows, int max_chunks, int &rows_per_chunk);
+cudaError_t launch_decode_attn_tc(const void *qt, const void *Kc, const void *Vc, int B, int H, int P,
+                                  long long cache_rows, long long lo, long long hi, int nch, int rows_per_chunk,
+                                  float *part_ml, float *part_o, cudaStream_t st, int *status);
+
 bool decode_supported(int H, int d, int P) {
     return (d == 64 && P <= 8) || (d == 128 && P <= 4);
 }
@@ -453,6 +460,17 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
     long long lo = 0;
     if (mask_mode == 2) lo = (t - window + 1) * P > 0 ? (t - window + 1) * P : 0;
     const long long rows = hi - lo + 1;
+    if (decode_tc_supported(d, P, Kc, Vc)) {
+        // d = 128: the tensor-core kernel (k_decode_tc.cu)
+        int rpc = 0;
+        const int nch = decode_tc_chunks(B, H, rows, DC_NCH_MAX, rpc);
+        e = launch_decode_attn_tc(qt, Kc, Vc, B, H, P, cache_rows, lo, hi, nch, rpc, part_ml, part_o, st, status);
+        if (e != cudaSuccess) return e;
+        decode_merge<<<dim3(B * H, P), d, 0, st>>>(part_ml, part_o, H, d, P, nch, pbar);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        decode_contract<<<dim3(B, H), d, 0, st>>>(pbar, R, H, d, P, (__nv_bfloat16 *)out);
+        return cudaGetLastError();
+    }
     // one wave of resident CTAs: chunks per (b, h) = resident CTAs / (B * H)
     int occ = 1;
     if (d == 128) {

@@ -368,6 +368,12 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint3
 // 32*(w%4) .. 32*(w%4)+31; thread i of the warp gets lane 32*(w%4)+i, one 32-bit
 // column per register.
 // ------------------------------------------------------------------------------------
+// 4 consecutive 32-bit columns of this warp's lane quarter.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
 // 16 consecutive 32-bit columns of this warp's lane quarter.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
