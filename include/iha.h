@@ -247,10 +247,12 @@ IHA_API int iha_forward_stack(const void *X, int num_layers,
 /* Incremental decoding over a cache of pseudo-keys and pseudo-values (Algorithm 1 evaluated
  * for the rows of one new token; the mask is by original position, so the P pseudo-queries
  * of token t read the cached pseudo-tokens of positions t' <= t, and t - t' < window).
- * bf16 only; d = 64 with P <= 8, or d = 128 with P <= 4 (IHA_ERR_UNSUPPORTED otherwise);
+ * bf16 only; d = 64 with P <= 8, or d = 128 with P <= 4, and H*d <= 2048 (IHA_ERR_UNSUPPORTED otherwise);
  * mask_mode 1 or 2 (mode 0 would read future tokens: IHA_ERR_INVALID_ARG).
  *   K_cache [B][H][cache_tokens*P][d] bfloat16, V_cache same shape float16: stacked row
- *     t*P + j holds pseudo-key/value j of token t (the layout of Kbar/Vbar in iha_project).
+ *     t*P + j holds pseudo-key/value j of token t (the layout of Kbar/Vbar in iha_project);
+ *     both 16-byte aligned for iha_decode_step, as are W_Q, W_K, W_V (IHA_ERR_INVALID_ARG
+ *     otherwise).
  *
  * iha_prefill: iha_forward_ex over X [B][N][H*d] (the prompt) that also writes the prompt's
  *   pseudo-keys/values into rows 0 .. N*P-1 of the caches (cache_tokens >= N). */

@@ -23,6 +23,11 @@ int iha_decode_step(const void *x, const void *W_Q, const void *W_K, const void 
                                 out, dtype);
     if (rc != IHA_OK) return rc;
     if (!K_cache || !V_cache || t < 0 || t >= cache_tokens || mask_mode == IHA_MASK_NONE) return IHA_ERR_INVALID_ARG;
+    // cache rows are written 16 bytes at a time and read by TMA; W rows are read by bulk copies
+    if ((reinterpret_cast<uintptr_t>(K_cache) & 15) || (reinterpret_cast<uintptr_t>(V_cache) & 15) ||
+        (reinterpret_cast<uintptr_t>(W_Q) & 15) || (reinterpret_cast<uintptr_t>(W_K) & 15) ||
+        (reinterpret_cast<uintptr_t>(W_V) & 15))
+        return IHA_ERR_INVALID_ARG;
     if (dtype != IHA_DTYPE_BF16 || !decode_supported(H, d, P)) return IHA_ERR_UNSUPPORTED;
     const size_t need = decode_workspace_bytes(B, H, d, P);
     cudaStream_t st = static_cast<cudaStream_t>(stream);

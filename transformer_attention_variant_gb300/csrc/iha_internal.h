@@ -45,6 +45,7 @@ enum WaitSite {
     kSiteDecodeTcProducer = 50,
     kSiteDecodeTcMma = 51,
     kSiteDecodeTc = 52,
+    kSiteDecodeProj = 53,
     kSiteSelfTest = 99,
 };
 

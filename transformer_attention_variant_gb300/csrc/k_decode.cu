@@ -26,133 +26,181 @@
 namespace iha {
 
 constexpr int DC_KS = 16;         // K splits of the projection GEMV
-constexpr int DC_BMAX = 8;        // batch rows per pass of the GEMV
+constexpr int DC_BMAX = 8;        // batch rows per pass of the GEMV (at most)
+constexpr int DC_KROWS_MAX = 128; // rows per K split: D / DC_KS, D <= 2048
 constexpr int DC_NCH_MAX = 64;    // KV chunks per (b, h)
 
 // ---------------------------------------------------------------------------------------
 // 1. projection GEMV: Yp[ks][b][s][n] = sum_{k in split ks} x[b][k] W_s[k][n]
 // ---------------------------------------------------------------------------------------
+// A CTA owns up to 256 columns of one W_s and one split of D / DC_KS rows (a 64 KB slab).
+// Warp 0 moves the slab into shared memory with one bulk copy per row (no registers held,
+// so three CTAs fit on an SM and the whole of W is in flight at once); then a lane owns 8
+// columns and warp w the rows w, w+8, ..., and the 8 warps' sums are added in shared
+// memory.  BM batch rows per pass.
+constexpr int DP_SLAB = DC_KROWS_MAX * 256 * 2;   // 64 KB
+template <int BM>
+constexpr size_t dp_smem_bytes() {
+    return DP_SLAB + (size_t)BM * DC_KROWS_MAX * 4 + (size_t)8 * BM * 256 * 4 + 16 + 128;
+}
+template <int BM>
 __global__ void __launch_bounds__(256)
 decode_proj(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ WQ,
             const __nv_bfloat16 *__restrict__ WK, const __nv_bfloat16 *__restrict__ WV, int B, int D,
-            float *__restrict__ Yp) {
-    extern __shared__ float dsm[];
+            float *__restrict__ Yp, int *status) {
+    extern __shared__ uint8_t psm_raw[];
+    uint8_t *psm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(psm_raw) + 127) & ~uintptr_t(127));
+    pdl_trigger();   // the mixing kernel may launch; it waits for this grid before reading Yp
     const int nblk = (D + 255) / 256;
     const int s = blockIdx.x / nblk, n0 = (blockIdx.x % nblk) * 256;
     const int ks = blockIdx.y, krows = D / DC_KS, k0 = ks * krows;
+    const int ncols = min(256, D - n0);
     const __nv_bfloat16 *W = s == 0 ? WQ : (s == 1 ? WK : WV);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = n0 + lane * 8;                      // this lane's 8 columns
-    float *xs = dsm;                                  // [DC_BMAX][krows]
-    float *red = dsm + DC_BMAX * krows;               // [8 warps][DC_BMAX][256]
-    for (int b0 = 0; b0 < B; b0 += DC_BMAX) {
-        const int nb = min(DC_BMAX, B - b0);
-        __syncthreads();
+    uint8_t *slab = psm;                                                    // [krows][256] bf16
+    float *xs = reinterpret_cast<float *>(psm + DP_SLAB);                   // [BM][krows]
+    float *red = xs + BM * DC_KROWS_MAX;                                    // [8 warps][BM][256]
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + 8 * BM * 256);
+    if (threadIdx.x == 0) {
+        mbar_init(full, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(krows * ncols * 2));
+        __syncwarp();
+        for (int k = lane; k < krows; k += 32)
+            bulk_load(slab + k * 512, W + (size_t)(k0 + k) * D + n0, (uint32_t)ncols * 2, full);
+    }
+    const int n = lane * 8;   // this lane's 8 columns of the slab
+    for (int b0 = 0; b0 < B; b0 += BM) {
+        const int nb = min(BM, B - b0);
+        if (b0 > 0) __syncthreads();
         for (int i = threadIdx.x; i < nb * krows; i += blockDim.x)
             xs[i] = __bfloat162float(x[(size_t)(b0 + i / krows) * D + k0 + i % krows]);
         __syncthreads();
-        float acc[DC_BMAX][8];
+        // the slab has landed (a wait that gives up leaves zeros and records the timeout)
+        const bool have = mbar_wait(full, 0, status, kSiteDecodeProj, nullptr, kWaitLimitNs);
+        float acc[BM][8];
 #pragma unroll
-        for (int b = 0; b < DC_BMAX; ++b)
+        for (int b = 0; b < BM; ++b)
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[b][e] = 0.f;
-        if (n < D) {
-            // rows warp, warp+8, ... of the split; eight rows' loads in flight per lane
-            for (int k8 = warp; k8 < krows; k8 += 64) {
-                uint4 wv[8];
+        if (have && n < ncols) {
+#pragma unroll 4
+            for (int k = warp; k < krows; k += 8) {
+                const uint4 wv = *reinterpret_cast<const uint4 *>(slab + k * 512 + n * 2);
+                const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+                float wf[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int k = k8 + 8 * u;
-                    wv[u] = k < krows ? *reinterpret_cast<const uint4 *>(W + (size_t)(k0 + k) * D + n)
-                                      : make_uint4(0, 0, 0, 0);
+                for (int e = 0; e < 4; ++e) {
+                    wf[2 * e] = __uint_as_float(w4[e] << 16);
+                    wf[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
                 }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int k = k8 + 8 * u;
-                    if (k >= krows) break;
-                    const uint32_t w4[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
-                    float wf[8];
+                for (int b = 0; b < BM; ++b) {
+                    if (b < nb) {
+                        const float xv = xs[b * krows + k];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        wf[2 * e] = __uint_as_float(w4[e] << 16);
-                        wf[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
-                    }
-#pragma unroll
-                    for (int b = 0; b < DC_BMAX; ++b) {
-                        if (b < nb) {
-                            const float xv = xs[b * krows + k];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[b][e] = fmaf(xv, wf[e], acc[b][e]);
-                        }
+                        for (int e = 0; e < 8; ++e) acc[b][e] = fmaf(xv, wf[e], acc[b][e]);
                     }
                 }
             }
         }
         // reduce over the 8 warps
 #pragma unroll
-        for (int b = 0; b < DC_BMAX; ++b)
+        for (int b = 0; b < BM; ++b)
             if (b < nb)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) red[(warp * DC_BMAX + b) * 256 + lane * 8 + e] = acc[b][e];
+                for (int e = 0; e < 8; ++e) red[(warp * BM + b) * 256 + n + e] = acc[b][e];
         __syncthreads();
         for (int i = threadIdx.x; i < nb * 256; i += blockDim.x) {
             const int b = i / 256, c = i % 256;
-            if (n0 + c >= D) continue;
+            if (c >= ncols) continue;
             float v = 0.f;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) v += red[(w * DC_BMAX + b) * 256 + c];
+            for (int w = 0; w < 8; ++w) v += red[(w * BM + b) * 256 + c];
             Yp[(((size_t)ks * B + b0 + b) * 3 + s) * D + n0 + c] = v;
         }
     }
 }
 
 // ---------------------------------------------------------------------------------------
-// 2. mixing + cache append, one CTA per (b, s): y_s[b] = sum of the K-split partials into
-//    shared memory (all loads of a thread in flight), alpha_s into shared memory, then every
-//    (h, j, c) output of the projection
+// 2. mixing + cache append, DM_GROUPS CTAs of DM_THREADS per (b, s): y_s[b] = the sum of the
+//    K-split partials (every load of a thread in flight at once) and alpha_s go to shared
+//    memory, then each thread makes 8 consecutive columns of one (h, j) output row of the
+//    CTA's share: 8 FMAs per two 16-byte shared loads of y and one of alpha
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
+constexpr int DM_THREADS = 1024, DM_GROUPS = 4;
+__global__ void __launch_bounds__(DM_THREADS)
 decode_mix(const float *__restrict__ Yp, const float *__restrict__ aQ, const float *__restrict__ aK,
            const float *__restrict__ aV, int B, int H, int d, int P, long long t, long long cache_rows,
            __nv_bfloat16 *__restrict__ qt, __nv_bfloat16 *__restrict__ Kc, __half *__restrict__ Vc) {
     extern __shared__ float msm[];
-    const int b = blockIdx.x, s = blockIdx.y, hg = blockIdx.z, nhg = gridDim.z;   // heads h = hg, hg + nhg, ...
+    pdl_trigger();
+    const int b = blockIdx.x, s = blockIdx.y, g = blockIdx.z;
     const int D = H * d, HP = H * P;
     float *y = msm;              // [H][d]
     float *al = msm + D;         // alpha_s [H][H][P]
     const float *alg = s == 0 ? aQ : (s == 1 ? aK : aV);
-    for (int i0 = threadIdx.x; i0 < D; i0 += 4 * blockDim.x) {
-        float v[4][DC_KS];
+    for (int i = threadIdx.x; i < H * HP; i += DM_THREADS) al[i] = alg[i];   // an input: no wait
+    pdl_wait();   // the projection's partial sums
+    constexpr int PER = 2;       // D <= PER * DM_THREADS
+    {
+        float v[PER][DC_KS];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * blockDim.x;
+        for (int u = 0; u < PER; ++u) {
+            const int i = threadIdx.x + u * DM_THREADS;
 #pragma unroll
             for (int ks = 0; ks < DC_KS; ++ks) v[u][ks] = i < D ? Yp[(((size_t)ks * B + b) * 3 + s) * D + i] : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * blockDim.x;
+        for (int u = 0; u < PER; ++u) {
+            const int i = threadIdx.x + u * DM_THREADS;
             float acc = 0.f;
 #pragma unroll
             for (int ks = 0; ks < DC_KS; ++ks) acc += v[u][ks];
             if (i < D) y[i] = acc;
         }
     }
-    for (int i = threadIdx.x; i < H * HP; i += blockDim.x) al[i] = alg[i];
     __syncthreads();
-    const int nh = (H - hg + nhg - 1) / nhg;   // heads of this group
-    for (int i = threadIdx.x; i < nh * P * d; i += blockDim.x) {
-        const int hj = i / d, c = i % d, h = hg + (hj / P) * nhg, j = hj % P;
-        float acc = 0.f;
-        for (int m = 0; m < H; ++m) acc = fmaf(al[(m * H + h) * P + j], y[m * d + c], acc);   // alpha_s[m][h][j]
+    // this CTA's rows (h, j): hj in [g*HP/G, (g+1)*HP/G); 8-column units of each row
+    const int hj0 = (int)((long long)g * HP / DM_GROUPS), hj1 = (int)((long long)(g + 1) * HP / DM_GROUPS);
+    const int upr = d / 8;   // units per row
+    for (int i = threadIdx.x; i < (hj1 - hj0) * upr; i += DM_THREADS) {
+        const int hj = hj0 + i / upr, c0 = (i % upr) * 8, h = hj / P, j = hj % P;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int m = 0; m < H; ++m) {
+            const float a = al[(m * H + h) * P + j];   // alpha_s[m][h][j]
+            const float4 y0 = *reinterpret_cast<const float4 *>(y + m * d + c0);
+            const float4 y1 = *reinterpret_cast<const float4 *>(y + m * d + c0 + 4);
+            acc[0] = fmaf(a, y0.x, acc[0]);
+            acc[1] = fmaf(a, y0.y, acc[1]);
+            acc[2] = fmaf(a, y0.z, acc[2]);
+            acc[3] = fmaf(a, y0.w, acc[3]);
+            acc[4] = fmaf(a, y1.x, acc[4]);
+            acc[5] = fmaf(a, y1.y, acc[5]);
+            acc[6] = fmaf(a, y1.z, acc[6]);
+            acc[7] = fmaf(a, y1.w, acc[7]);
+        }
+        uint4 pk;
+        if (s == 2) {
+            pk = make_uint4(pack_f16x2(acc[0], acc[1]), pack_f16x2(acc[2], acc[3]), pack_f16x2(acc[4], acc[5]),
+                            pack_f16x2(acc[6], acc[7]));
+        } else {
+            pk = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                            pack_bf16x2(acc[6], acc[7]));
+        }
         if (s == 0) {
-            qt[(((size_t)b * H + h) * P + j) * d + c] = __float2bfloat16_rn(acc);
+            *reinterpret_cast<uint4 *>(qt + (((size_t)b * H + h) * P + j) * d + c0) = pk;
         } else {
             const size_t row = ((size_t)b * H + h) * cache_rows + (size_t)t * P + j;   // stacked row t*P + j
             if (s == 1)
-                Kc[row * d + c] = __float2bfloat16_rn(acc);
+                *reinterpret_cast<uint4 *>(Kc + row * d + c0) = pk;
             else
-                Vc[row * d + c] = __float2half_rn(acc);
+                *reinterpret_cast<uint4 *>(Vc + row * d + c0) = pk;
         }
     }
 }
@@ -195,6 +243,8 @@ decode_attn(const __nv_bfloat16 *__restrict__ qt, const __nv_bfloat16 *__restric
     __shared__ float sm_ml[DA_CWARPS][PMAX][2];
     __shared__ float sm_o[DA_CWARPS][PMAX][d];
 
+    pdl_trigger();
+    pdl_wait();   // the mixing kernel's q~ and appended cache rows
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, nch = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long bh = (long long)b * H + h;
@@ -360,42 +410,68 @@ decode_attn(const __nv_bfloat16 *__restrict__ qt, const __nv_bfloat16 *__restric
 }
 
 // ---------------------------------------------------------------------------------------
-// 4a. merge the chunks of one (b, h', j): Pbar[b][h'*P + j][c], one thread per column
+// 4a. merge the chunks of one (b, h', j): Pbar[b][h'*P + j][c], one thread per column; the
+//     chunks' partial results are read 16 at a time, all loads of a group in flight
 // ---------------------------------------------------------------------------------------
+constexpr int DM_CHUNK_GROUP = 16;
 __global__ void decode_merge(const float *__restrict__ part_ml, const float *__restrict__ part_o, int H, int d, int P,
                              int nch, float *__restrict__ pbar) {
+    pdl_trigger();
+    pdl_wait();   // the attention's partial results
     const int bh = blockIdx.x, j = blockIdx.y, c = threadIdx.x;
     const size_t base = (size_t)bh * nch;
-    float mn = -INFINITY;
-    for (int ch = 0; ch < nch; ++ch) mn = fmaxf(mn, part_ml[((base + ch) * P + j) * 2]);
-    float lt = 0.f, ot = 0.f;
-    for (int ch = 0; ch < nch; ++ch) {
-        const size_t pidx = (base + ch) * P + j;
-        const float mc = part_ml[pidx * 2];
-        const float cw = mc == -INFINITY ? 0.f : exp2f(mc - mn);
-        lt += part_ml[pidx * 2 + 1] * cw;
-        ot += part_o[pidx * d + c] * cw;
+    float mt = -INFINITY, lt = 0.f, ot = 0.f;   // running merge (max, sum, output) in log2 units
+    for (int c0 = 0; c0 < nch; c0 += DM_CHUNK_GROUP) {
+        float m[DM_CHUNK_GROUP], l[DM_CHUNK_GROUP], o[DM_CHUNK_GROUP];
+#pragma unroll
+        for (int u = 0; u < DM_CHUNK_GROUP; ++u) {
+            const bool in = c0 + u < nch;
+            const size_t pidx = (base + c0 + u) * P + j;
+            m[u] = in ? part_ml[pidx * 2] : -INFINITY;
+            l[u] = in ? part_ml[pidx * 2 + 1] : 0.f;
+            o[u] = in ? part_o[pidx * d + c] : 0.f;
+        }
+        float mg = mt;
+#pragma unroll
+        for (int u = 0; u < DM_CHUNK_GROUP; ++u) mg = fmaxf(mg, m[u]);
+        if (mg == -INFINITY) continue;
+        const float f = exp2f(mt - mg);   // mt = -inf -> 0
+        lt *= f;
+        ot *= f;
+#pragma unroll
+        for (int u = 0; u < DM_CHUNK_GROUP; ++u) {
+            const float cw = m[u] == -INFINITY ? 0.f : exp2f(m[u] - mg);
+            lt = fmaf(l[u], cw, lt);
+            ot = fmaf(o[u], cw, ot);
+        }
+        mt = mg;
     }
     pbar[((size_t)bh * P + j) * d + c] = lt > 0.f ? ot / lt : 0.f;   // [b][h'][j][c] = [b][h'*P + j][c]
 }
 
 // ---------------------------------------------------------------------------------------
-// 4b. R contraction: out[b][h][c] = sum_k R[h][k] Pbar[b][k][c], one CTA per (b, h)
+// 4b. R contraction: out[b][h][c] = sum_k R[h][k] Pbar[b][k][c], one CTA per (b, h); R[h][:]
+//     goes to shared memory, and a thread's H*P loads are issued 64 at a time
 // ---------------------------------------------------------------------------------------
+constexpr int DK_GROUP = 64, DK_HPMAX = 256;
 __global__ void decode_contract(const float *__restrict__ pbar, const float *__restrict__ R, int H, int d, int P,
                                 __nv_bfloat16 *__restrict__ out) {
+    pdl_trigger();
     const int b = blockIdx.x, h = blockIdx.y, c = threadIdx.x, HP = H * P;
+    __shared__ float rs[DK_HPMAX];
+    for (int i = threadIdx.x; i < HP; i += blockDim.x) rs[i] = R[(size_t)h * HP + i];   // an input: no wait
+    __syncthreads();
+    pdl_wait();   // the merged Pbar
     const float *pb = pbar + (size_t)b * HP * d;
     float v = 0.f;
-    int k = 0;
-    for (; k + 8 <= HP; k += 8) {
-        float x[8];
+    for (int k0 = 0; k0 < HP; k0 += DK_GROUP) {
+        float xv[DK_GROUP];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = pb[(size_t)(k + u) * d + c];
+        for (int u = 0; u < DK_GROUP; ++u) xv[u] = k0 + u < HP ? pb[(size_t)(k0 + u) * d + c] : 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v = fmaf(R[(size_t)h * HP + k + u], x[u], v);
+        for (int u = 0; u < DK_GROUP; ++u)
+            if (k0 + u < HP) v = fmaf(rs[k0 + u], xv[u], v);
     }
-    for (; k < HP; ++k) v = fmaf(R[(size_t)h * HP + k], pb[(size_t)k * d + c], v);
     out[((size_t)b * H + h) * d + c] = __float2bfloat16_rn(v);
 }
 
@@ -408,8 +484,27 @@ cudaError_t launch_decode_attn_tc(const void *qt, const void *Kc, const void *Vc
                                   long long cache_rows, long long lo, long long hi, int nch, int rows_per_chunk,
                                   float *part_ml, float *part_o, cudaStream_t st, int *status);
 
+// Launch with programmatic stream serialization: the kernel may start while its
+// predecessor on the stream is still running (it calls pdl_wait() before reading that
+// predecessor's results), so launch latency and prologue overlap the predecessor's tail.
+template <typename Kern, typename... Act>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Act... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 bool decode_supported(int H, int d, int P) {
-    return (d == 64 && P <= 8) || (d == 128 && P <= 4);
+    // H*d <= 2048: one K split of the projection GEMV is at most DC_KROWS_MAX rows
+    return ((d == 64 && P <= 8) || (d == 128 && P <= 4)) && H * d <= DC_KS * DC_KROWS_MAX;
 }
 
 size_t decode_workspace_bytes(int B, int H, int d, int P) {
@@ -440,21 +535,31 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
 
     // 1. projections
     const int krows = D / DC_KS;
-    const size_t smem1 = (size_t)DC_BMAX * krows * 4 + (size_t)8 * DC_BMAX * 256 * 4;
-    cudaError_t e = cudaFuncSetAttribute(decode_proj, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
-    if (e != cudaSuccess) return e;
-    decode_proj<<<dim3(3 * ((D + 255) / 256), DC_KS), 256, smem1, st>>>(
-        (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)WQ, (const __nv_bfloat16 *)WK, (const __nv_bfloat16 *)WV, B,
-        D, Yp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (krows > DC_KROWS_MAX || D > 2 * DM_THREADS || H * P > DK_HPMAX) return cudaErrorInvalidValue;   // decode_supported
+    cudaError_t e = cudaSuccess;
+    {
+        const int bm = B <= 1 ? 1 : (B <= 2 ? 2 : (B <= 4 ? 4 : 8));
+        const dim3 g1(3 * ((D + 255) / 256), DC_KS);
+        auto run = [&](auto kern, size_t smem1) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+            if (e == cudaSuccess)
+                kern<<<g1, 256, smem1, st>>>((const __nv_bfloat16 *)x, (const __nv_bfloat16 *)WQ,
+                                             (const __nv_bfloat16 *)WK, (const __nv_bfloat16 *)WV, B, D, Yp, status);
+        };
+        if (bm == 1) run(decode_proj<1>, dp_smem_bytes<1>());
+        else if (bm == 2) run(decode_proj<2>, dp_smem_bytes<2>());
+        else if (bm == 4) run(decode_proj<4>, dp_smem_bytes<4>());
+        else run(decode_proj<8>, dp_smem_bytes<8>());
+        if (e != cudaSuccess) return e;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     // 2. mixing + append
     const size_t smem2 = ((size_t)D + (size_t)H * H * P) * 4;
     e = cudaFuncSetAttribute(decode_mix, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
     if (e != cudaSuccess) return e;
-    const int nhg = H < 8 ? H : 8;
-    decode_mix<<<dim3(B, 3, nhg), 256, smem2, st>>>(Yp, aQ, aK, aV, B, H, d, P, t, cache_rows, qt, (__nv_bfloat16 *)Kc,
-                                               (__half *)Vc);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_pdl(decode_mix, dim3(B, 3, DM_GROUPS), dim3(DM_THREADS), smem2, st, (const float *)Yp, aQ, aK, aV, B, H,
+                   d, P, t, cache_rows, qt, (__nv_bfloat16 *)Kc, (__half *)Vc);
+    if (e != cudaSuccess) return e;
     // 3. attention over the readable cached rows [lo, hi]
     const long long hi = (t + 1) * P - 1;
     long long lo = 0;
@@ -466,10 +571,11 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
         const int nch = decode_tc_chunks(B, H, rows, DC_NCH_MAX, rpc);
         e = launch_decode_attn_tc(qt, Kc, Vc, B, H, P, cache_rows, lo, hi, nch, rpc, part_ml, part_o, st, status);
         if (e != cudaSuccess) return e;
-        decode_merge<<<dim3(B * H, P), d, 0, st>>>(part_ml, part_o, H, d, P, nch, pbar);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        decode_contract<<<dim3(B, H), d, 0, st>>>(pbar, R, H, d, P, (__nv_bfloat16 *)out);
-        return cudaGetLastError();
+        e = launch_pdl(decode_merge, dim3(B * H, P), dim3(d), 0, st, (const float *)part_ml, (const float *)part_o, H,
+                       d, P, nch, pbar);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(decode_contract, dim3(B, H), dim3(d), 0, st, (const float *)pbar, R, H, d, P,
+                          (__nv_bfloat16 *)out);
     }
     // one wave of resident CTAs: chunks per (b, h) = resident CTAs / (B * H)
     int occ = 1;
@@ -493,20 +599,21 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
     const float sl2 = 1.4426950408889634f / sqrtf((float)d);
     const dim3 g3((unsigned)nch, H, B);
     if (d == 128) {
-        decode_attn<16, 4><<<g3, DA_THREADS, da_smem_bytes<128>(), st>>>(
-            qt, (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P, cache_rows, lo, hi, rpc, sl2, part_ml, part_o,
-            status);
+        e = launch_pdl(decode_attn<16, 4>, g3, dim3(DA_THREADS), da_smem_bytes<128>(), st, (const __nv_bfloat16 *)qt,
+                       (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P, cache_rows, lo, hi, rpc, sl2, part_ml,
+                       part_o, status);
     } else {
-        decode_attn<8, 8><<<g3, DA_THREADS, da_smem_bytes<64>(), st>>>(
-            qt, (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P, cache_rows, lo, hi, rpc, sl2, part_ml, part_o,
-            status);
+        e = launch_pdl(decode_attn<8, 8>, g3, dim3(DA_THREADS), da_smem_bytes<64>(), st, (const __nv_bfloat16 *)qt,
+                       (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P, cache_rows, lo, hi, rpc, sl2, part_ml,
+                       part_o, status);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
     // 4. merge the chunks, then the contraction
-    decode_merge<<<dim3(B * H, P), d, 0, st>>>(part_ml, part_o, H, d, P, (int)nch, pbar);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    decode_contract<<<dim3(B, H), d, 0, st>>>(pbar, R, H, d, P, (__nv_bfloat16 *)out);
-    return cudaGetLastError();
+    e = launch_pdl(decode_merge, dim3(B * H, P), dim3(d), 0, st, (const float *)part_ml, (const float *)part_o, H, d,
+                   P, (int)nch, pbar);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_contract, dim3(B, H), dim3(d), 0, st, (const float *)pbar, R, H, d, P,
+                      (__nv_bfloat16 *)out);
 }
 
 }  // namespace iha

@@ -94,9 +94,11 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const int ntiles = (int)((r_end - r_begin + DT_ROWS - 1) / DT_ROWS);
     const int P = p.P;
 
+    pdl_trigger();
     // Q (bf16) and zeroed P^T buffers: the rows past P stay zero
     for (int i = threadIdx.x; i < (DT_Q_BYTES + 2 * DT_PT_BYTES) / 16; i += blockDim.x)
         reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0, 0, 0, 0);
+    pdl_wait();   // the mixing kernel's q~ and appended cache rows
     __syncthreads();
     for (int i = threadIdx.x; i < P * DT_D; i += blockDim.x) {
         const int q = i / DT_D, c = i % DT_D;
@@ -349,8 +351,18 @@ cudaError_t launch_decode_attn_tc(const void *qt, const void *Kc, const void *Vc
     p.status = status;
     cudaError_t e = cudaFuncSetAttribute(decode_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, DT_SMEM);
     if (e != cudaSuccess) return e;
-    decode_attn_tc<<<dim3((unsigned)nch, H, B), DT_THREADS, DT_SMEM, st>>>(tmK, tmV, p);
-    return cudaGetLastError();
+    // programmatic stream serialization: the launch and prologue overlap the mixing kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nch, H, B);
+    cfg.blockDim = dim3(DT_THREADS);
+    cfg.dynamicSmemBytes = DT_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_attn_tc, tmK, tmV, p);
 }
 
 }  // namespace iha

@@ -289,6 +289,15 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) 
 }
 
 // ------------------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while its predecessor on the stream runs; pdl_wait() returns once the
+// predecessor grid has completed and its writes are visible (immediately when the kernel
+// was launched without that attribute), and pdl_trigger() lets the next kernel launch.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ------------------------------------------------------------------------------------
 // thread-block clusters
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
