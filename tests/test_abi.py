@@ -171,6 +171,11 @@ def test_decode_validation(iha):
     assert step(K_cache=None) == iha.IHA_ERR_INVALID_ARG
     assert step(dtype=0) == iha.IHA_ERR_UNSUPPORTED
     assert step(d=128, P=8) == iha.IHA_ERR_UNSUPPORTED
+    assert step(H=64, d=64) == iha.IHA_ERR_UNSUPPORTED       # H*d > 2048
+    assert step(K_cache=fake + 8) == iha.IHA_ERR_INVALID_ARG  # caches and W are read 16 bytes at a time
+    assert step(V_cache=fake + 2) == iha.IHA_ERR_INVALID_ARG
+    assert iha.iha_decode_step(fake, fake + 4, *args[2:], B, H, d, P, 1, 0, fake, fake, 100, 5, fake, 1) == \
+        iha.IHA_ERR_INVALID_ARG
     assert iha.iha_decode_step(*args, B, H, d, P, 1, 0, fake, fake, 100, 5, fake, 1, None, fake, 16) == \
         iha.IHA_ERR_WORKSPACE
     # prefill: the cache must hold the prompt
