@@ -280,8 +280,12 @@ def test_caller_workspace_and_default_stream_entry(iha):
     assert torch.equal(out2, ref)
 
 
-def test_forward_host_buffers(iha):
-    w = W("host", B=2, N=150, H=2, d=64, P=2, mask_mode=C, window=0, dtype="bf16", seed=45)
+@pytest.mark.parametrize("B,N,H,d,P,mode,window", [
+    (2, 150, 2, 64, 2, C, 0),        # unfolded route: copies overlapped with chunked work
+    (1, 777, 4, 128, 3, WN, 60),     # chunks of 194-195 tokens
+    (2, 99, 4, 64, 1, C, 0)])        # folded route (P = 1): the plain sequence
+def test_forward_host_buffers(iha, B, N, H, d, P, mode, window):
+    w = W("host", B=B, N=N, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=45)
     inp = gi.make_inputs(w)
     ref = run_gpu(iha, w, inp)
     hin = {k: v.contiguous().pin_memory() for k, v in inp.items()}
