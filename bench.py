@@ -638,6 +638,83 @@ def run_backward(args, w):
         dist.destroy_process_group()
 
 
+def run_train(args, w):
+    """One training step of the layer on workload w without recomputation: iha_forward_train
+    (the forward, leaving its pieces in the backward workspace) then iha_backward_saved (every
+    input gradient from them).  Reports steps/s as pseudo-tokens/s, the algorithmic TFLOP/s of
+    forward + backward, and each half's time (CUDA events between the two calls)."""
+    rank, world, local, dist = dist_setup(args.gpus)
+    import transformer_attention_variant_gb300 as iha
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    B, N, H, d, P, D = w.B, w.N, w.H, w.d, w.P, w.D
+    host = gi.make_inputs(w)
+    dd = {k: v.to(dev).contiguous() for k, v in host.items()}
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    dO = torch.randn(B, N, D, generator=g, device=dev).to(torch.bfloat16)
+    keys = ("X", "W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")
+    grads = [torch.empty_like(dd[k]) for k in keys]
+    out = torch.empty(B, N, D, dtype=torch.bfloat16, device=dev)
+    ws_bytes = iha.iha_backward_workspace_bytes(B, N, H, d, P, iha.IHA_DTYPE_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    wk = work(w)
+    fwd_flops = wk["algorithmic"]
+    bwd_flops = 2 * wk["proj_heads"] + 2 * (wk["algorithmic"] - wk["proj_heads"] - wk["attn"]) + 2.5 * wk["attn"]
+    args_in = [dd[k] for k in keys] + [B, N, H, d, P, w.mask_mode, w.window]
+
+    def fwd():
+        iha.check(iha.iha_forward_train(*args_in, out, iha.IHA_DTYPE_BF16, stream, ws, ws_bytes), "forward_train")
+
+    def bwd():
+        iha.check(iha.iha_backward_saved(*args_in, dO, *grads, iha.IHA_DTYPE_BF16, stream, ws, ws_bytes),
+                  "backward_saved")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            fwd()
+            bwd()
+    torch.cuda.synchronize()
+    barrier(dist)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                fwd()
+                ev[i][1].record(stream)
+                bwd()
+                ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status(stream)
+    iha.check(rc, f"device status after timed steps ({code:#x})")
+    ms_f = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    ms_b = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    ms = max_over_ranks(ms_f + ms_b, dist, dev)
+    barrier(dist)
+    if rank == 0:
+        tf = (fwd_flops + bwd_flops) / (ms * 1e-3) / 1e12
+        line = {
+            "metric": "IHA training step (forward + all input gradients, no recomputation) pseudo-tokens/s, 1 GPU "
+                      "per replica",
+            "value": job_value(world, wk["pseudo_tokens"], ms), "unit": "pseudo-tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": DATA,
+            "config": config_of(w, "flushed between steps (256 MiB write outside the timed events)"),
+            "forward_train_ms": ms_f, "backward_saved_ms": ms_b, "tflops_algorithmic": tf,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16"], "traffic": None},
+            "gpu_launches": None, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def traffic_per_launch(workload, kernel):
     """DRAM bytes (read + write) per launch recorded from ncu in profiles/dram_traffic.txt,
     provided the kernel's source is unchanged since that capture; None otherwise."""
@@ -675,6 +752,8 @@ def main():
                     help="time one decoding step over a full cache of the workload's shape instead")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (iha_backward) on the workload instead")
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step (iha_forward_train + iha_backward_saved) on the workload instead")
     ap.add_argument("--N", type=int, default=None,
                     help="shrink the workload's sequence length (smaller cases for profiler captures); "
                          "the window stays N/(2P) for windowed workloads")
@@ -693,6 +772,8 @@ def main():
         run_decode(args, w)
     elif args.backward:
         run_backward(args, w)
+    elif args.train:
+        run_train(args, w)
     else:
         run_gpu(args, w)
 

@@ -290,6 +290,27 @@ IHA_API int iha_backward(const void *X, const void *W_Q, const void *W_K, const 
                          float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR,
                          int dtype, void *stream, void *workspace, size_t workspace_bytes);
 
+/* A training step without recomputation, on the shapes iha_backward takes:
+ * iha_forward_train computes the layer output `out` [B][N][H*d] (bfloat16; bit-identical to
+ *   iha_forward's when iha_projection_route() is 1, i.e. P >= 2; for P = 1 iha_forward folds
+ *   alpha into W and rounds differently) and leaves the forward pieces the gradients need
+ *   (head projections, stacked pseudo-queries/keys/values, the attention output and each
+ *   row's softmax normaliser) in `workspace`, which is required here:
+ *   iha_backward_workspace_bytes(...) bytes, 256-byte aligned.
+ * iha_backward_saved then computes the same gradients as iha_backward (bit-identical) from
+ *   that workspace: same inputs, same shape and mask, and the workspace untouched in between
+ *   (stream-ordered after iha_forward_train).  NULL workspace: IHA_ERR_WORKSPACE. */
+IHA_API int iha_forward_train(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                              const float *alpha_Q, const float *alpha_K, const float *alpha_V, const float *R,
+                              int B, int N, int H, int d, int P, int mask_mode, int window, void *out,
+                              int dtype, void *stream, void *workspace, size_t workspace_bytes);
+IHA_API int iha_backward_saved(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                               const float *alpha_Q, const float *alpha_K, const float *alpha_V, const float *R,
+                               int B, int N, int H, int d, int P, int mask_mode, int window, const void *dO,
+                               void *dX, void *dW_Q, void *dW_K, void *dW_V,
+                               float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR,
+                               int dtype, void *stream, void *workspace, size_t workspace_bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -183,6 +183,23 @@ def test_decode_validation(iha):
     assert iha.iha_prefill(*args, B, 50, H, d, P, 0, 0, fake, fake, fake, 60, 1) == iha.IHA_ERR_INVALID_ARG
 
 
+def test_training_pair_validation(iha):
+    fake = 1 << 40                                           # never dereferenced
+    B, N, H, d, P = 2, 64, 4, 64, 2
+    args = [fake] * 8
+    nb = iha.iha_backward_workspace_bytes(B, N, H, d, P, 1)
+    # the workspace carries the forward pieces from one call to the other: it is required
+    assert iha.iha_forward_train(*args, B, N, H, d, P, 1, 0, fake, 1, None, None, 0) == iha.IHA_ERR_WORKSPACE
+    assert iha.iha_backward_saved(*args, B, N, H, d, P, 1, 0, fake, *([fake] * 8), 1, None, None, 0) == \
+        iha.IHA_ERR_WORKSPACE
+    assert iha.iha_forward_train(*args, B, N, H, d, P, 1, 0, fake, 1, None, fake, nb - 256) == iha.IHA_ERR_WORKSPACE
+    assert iha.iha_forward_train(*args, B, N, 20, d, P, 1, 0, fake, 1, None, fake, nb) == iha.IHA_ERR_UNSUPPORTED
+    assert iha.iha_forward_train(*args, B, N, H, d, P, 1, 0, fake, 0, None, fake, nb) == iha.IHA_ERR_UNSUPPORTED
+    assert iha.iha_forward_train(*args, B, N, H, d, P, 1, 0, None, 1, None, fake, nb) == iha.IHA_ERR_INVALID_ARG
+    assert iha.iha_backward_saved(*args, B, N, H, d, P, 1, 0, fake, None, *([fake] * 7), 1, None, fake, nb) == \
+        iha.IHA_ERR_INVALID_ARG
+
+
 def test_backward_validation(iha):
     fake = 1 << 40                                           # never dereferenced
     B, N, H, d, P = 2, 64, 4, 64, 2

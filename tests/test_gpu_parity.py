@@ -441,3 +441,43 @@ def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
         assert np.isfinite(got).all(), k
         err = rms(got - r)
         assert err <= BWD_TOL * rms(r), f"{k}: rms err {err:.3g} vs rms ref {rms(r):.3g}"
+
+
+@pytest.mark.parametrize("B,N,H,d,P,mode,window", [
+    (2, 150, 4, 64, 2, C, 0), (1, 300, 8, 128, 4, WN, 40), (1, 77, 4, 128, 1, NM, 0)])
+def test_training_pair_matches_recompute(iha, B, N, H, d, P, mode, window):
+    """iha_forward_train + iha_backward_saved give iha_forward's output (P >= 2: the same
+    route) and iha_backward's gradients bit for bit."""
+    from oracle import backward as bwd
+    w = gi.Workload("train", B=B, N=N, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=31 + P)
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    D = w.D
+    g = torch.Generator().manual_seed(99 + N)
+    dO = torch.randn(B, N, D, generator=g).to(torch.bfloat16).to("cuda:0").contiguous()
+    nb = iha.iha_backward_workspace_bytes(B, N, H, d, P, iha.IHA_DTYPE_BF16)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda:0")
+    out = torch.empty(B, N, D, dtype=torch.bfloat16, device="cuda:0")
+    args = [dinp[k] for k in bwd.PARAMS] + [B, N, H, d, P, mode, window]
+    iha.check(iha.iha_forward_train(*args, out, iha.IHA_DTYPE_BF16, None, ws, nb), "iha_forward_train")
+
+    def grads():
+        return {"X": torch.empty(B, N, D, dtype=torch.bfloat16, device="cuda:0"),
+                **{k: torch.empty(D, D, dtype=torch.bfloat16, device="cuda:0") for k in ("W_Q", "W_K", "W_V")},
+                **{k: torch.empty(H, H, P, dtype=torch.float32, device="cuda:0")
+                   for k in ("alpha_Q", "alpha_K", "alpha_V")},
+                "R": torch.empty(H, H * P, dtype=torch.float32, device="cuda:0")}
+    g_saved, g_full = grads(), grads()
+    iha.check(iha.iha_backward_saved(*args, dO, *(g_saved[k] for k in bwd.PARAMS), iha.IHA_DTYPE_BF16, None, ws,
+                                     nb), "iha_backward_saved")
+    iha.check(iha.iha_backward(*args, dO, *(g_full[k] for k in bwd.PARAMS), iha.IHA_DTYPE_BF16), "iha_backward")
+    torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status()
+    assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
+    for k in bwd.PARAMS:
+        assert torch.equal(g_saved[k], g_full[k]), k
+    if P >= 2:
+        assert torch.equal(out, run_gpu(iha, w, inp))
+    else:   # the forward folds alpha into W for P = 1: same layer, other rounding
+        assert_parity(w, out.double().cpu().numpy(), oracle_rows(w, inp))
+

@@ -34,7 +34,8 @@ EXPORTED = ("iha_forward", "iha_forward_ex", "iha_workspace_bytes", "iha_error_s
             "iha_selftest_wait_timeout", "iha_fold_weights", "iha_project", "iha_attention",
             "iha_contract", "iha_forward_noalloc", "iha_projection_route", "iha_project_heads",
             "iha_mix_heads", "iha_stack_workspace_bytes", "iha_forward_stack", "iha_prefill",
-            "iha_decode_workspace_bytes", "iha_decode_step", "iha_backward_workspace_bytes", "iha_backward")
+            "iha_decode_workspace_bytes", "iha_decode_step", "iha_backward_workspace_bytes", "iha_backward",
+            "iha_forward_train", "iha_backward_saved")
 
 IHA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -101,6 +102,10 @@ def _load():
     lib.iha_backward_workspace_bytes.restype = sz
     lib.iha_backward.argtypes = [vp] * 4 + [fp] * 4 + shape + [i, i, vp] + [vp] * 4 + [fp] * 4 + [i, vp, vp, sz]
     lib.iha_backward.restype = i
+    lib.iha_forward_train.argtypes = [vp] * 4 + [fp] * 4 + shape + [i, i, vp, i, vp, vp, sz]
+    lib.iha_forward_train.restype = i
+    lib.iha_backward_saved.argtypes = lib.iha_backward.argtypes
+    lib.iha_backward_saved.restype = i
     return lib
 
 
@@ -261,6 +266,21 @@ def iha_backward(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, 
     return _lib.iha_backward(_p(X), _p(W_Q), _p(W_K), _p(W_V), _p(alpha_Q), _p(alpha_K), _p(alpha_V), _p(R), B, N, H,
                              d, P, mask_mode, window, _p(dO), _p(dX), _p(dW_Q), _p(dW_K), _p(dW_V), _p(dalpha_Q),
                              _p(dalpha_K), _p(dalpha_V), _p(dR), dtype, _s(stream), _p(workspace), workspace_bytes)
+
+
+def iha_forward_train(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, out, dtype,
+                      stream, workspace, workspace_bytes) -> int:
+    return _lib.iha_forward_train(_p(X), _p(W_Q), _p(W_K), _p(W_V), _p(alpha_Q), _p(alpha_K), _p(alpha_V), _p(R), B,
+                                  N, H, d, P, mask_mode, window, _p(out), dtype, _s(stream), _p(workspace),
+                                  workspace_bytes)
+
+
+def iha_backward_saved(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, dO, dX, dW_Q,
+                       dW_K, dW_V, dalpha_Q, dalpha_K, dalpha_V, dR, dtype, stream, workspace, workspace_bytes) -> int:
+    return _lib.iha_backward_saved(_p(X), _p(W_Q), _p(W_K), _p(W_V), _p(alpha_Q), _p(alpha_K), _p(alpha_V), _p(R), B,
+                                   N, H, d, P, mask_mode, window, _p(dO), _p(dX), _p(dW_Q), _p(dW_K), _p(dW_V),
+                                   _p(dalpha_Q), _p(dalpha_K), _p(dalpha_V), _p(dR), dtype, _s(stream),
+                                   _p(workspace), workspace_bytes)
 
 
 def check(status: int, what: str = "") -> None:

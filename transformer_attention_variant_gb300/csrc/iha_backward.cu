@@ -1,5 +1,7 @@
 // iha_backward.cu -- the C-ABI of the backward pass of one IHA layer (kernels in
-// k_backward.cu and the forward kernels it reuses).
+// k_backward.cu, k_backward_tc.cu and the forward kernels it reuses): iha_backward (forward
+// pieces recomputed), and the training pair iha_forward_train (the forward, leaving its
+// pieces in the backward workspace) + iha_backward_saved (the gradients from them).
 //
 // Step order (one stream, bf16 tensors, fp32 arithmetic):
 //   forward pieces:  Y = X [W_Q|W_K|W_V];  Q~K~V~ = mix(Y);  Pbar, lse = attention(Q~, K~, V~)
@@ -77,42 +79,20 @@ size_t iha_backward_workspace_bytes(int B, int N, int H, int d, int P, int dtype
     return bwd_layout(sh).total;
 }
 
-int iha_backward(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
-                 const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
-                 int mask_mode, int window, const void *dO, void *dX, void *dW_Q, void *dW_K, void *dW_V,
-                 float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR, int dtype, void *stream,
-                 void *workspace, size_t workspace_bytes) {
-    int rc = check_forward_args(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window,
-                                dO, dtype);
-    if (rc != IHA_OK) return rc;
-    if (!dX || !dW_Q || !dW_K || !dW_V || !dalpha_Q || !dalpha_K || !dalpha_V || !dR) return IHA_ERR_INVALID_ARG;
-    const Shape sh{B, N, H, d, P};
-    if (!bwd_supported(sh, dtype)) return IHA_ERR_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(dO) & 15) != 0) return IHA_ERR_INVALID_ARG;   // read by TMA
-    const BwdLayout lay = bwd_layout(sh);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    bool own = false;
-    if (!workspace) {
-        if (cudaMallocAsync(&workspace, lay.total, st) != cudaSuccess) return IHA_ERR_CUDA;
-        own = true;
-    } else if (workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255)) {
-        return IHA_ERR_WORKSPACE;
-    }
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    int *status = status_word_ptr();
-    const long long T = (long long)B * N, D = sh.D(), HP = (long long)H * P;
-    uint8_t *Y = ws + lay.y, *QKV = ws + lay.qkv, *Vb = ws + lay.vb, *Pbar = ws + lay.pbar, *dPst = ws + lay.dpst,
-            *dS = ws + lay.ds, *dY = ws + lay.dy;
-    float *lse = reinterpret_cast<float *>(ws + lay.lse), *Dv = reinterpret_cast<float *>(ws + lay.dv);
-    float *part = reinterpret_cast<float *>(ws + lay.part);
-    const size_t ds_bytes = (size_t)T * HP * d * 2, dy_bytes = (size_t)T * D * 2;
-    const size_t third = (size_t)sh.qkv_elems() * 2;
-    const void *W[3] = {W_Q, W_K, W_V};
-    const float *alpha[3] = {alpha_Q, alpha_K, alpha_V};
-    float *dalpha[3] = {dalpha_Q, dalpha_K, dalpha_V};
-    void *dW[3] = {dW_Q, dW_K, dW_V};
-    const void *dYs[3] = {dY, dY + dy_bytes, dY + 2 * dy_bytes};
+}  // extern "C"
 
+namespace iha {
+
+// The forward pieces the gradients need, written into the workspace regions: Y, Q~ K~ V~ (V~
+// f16), Pbar and lse (the forward attention), V~ again in bf16; and the layer output when
+// `out` is given (the contraction of Pbar with R).
+static cudaError_t bwd_forward_pieces(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                                      const float *alpha_Q, const float *alpha_K, const float *alpha_V,
+                                      const float *R, const Shape &sh, int mask_mode, int window, void *out,
+                                      const BwdLayout &lay, uint8_t *ws, cudaStream_t st, int *status) {
+    uint8_t *Y = ws + lay.y, *QKV = ws + lay.qkv, *Vb = ws + lay.vb, *Pbar = ws + lay.pbar;
+    float *lse = reinterpret_cast<float *>(ws + lay.lse), *Dv = reinterpret_cast<float *>(ws + lay.dv);
+    const long long D = sh.D();
     // lse and D rows are padded so that every 64-row block of them starts 256 bytes into a
     // 256-aligned row; the padding reads as 0 (its pairs are masked)
     const int ld = bwd_ld_stride(sh.L());
@@ -120,12 +100,38 @@ int iha_backward(const void *X, const void *W_Q, const void *W_K, const void *W_
     if (e == cudaSuccess) e = cudaMemsetAsync(Dv, 0, lay.ld_bytes, st);
     if (e == cudaSuccess) e = launch_project_heads(X, W_Q, W_K, W_V, sh, Y, st, status);
     if (e == cudaSuccess) e = launch_mix(Y, alpha_Q, alpha_K, alpha_V, sh, QKV, st, status);
-    if (e == cudaSuccess) e = launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, lse, ld, st, status);
+    if (e == cudaSuccess)
+        e = launch_attention_lse(QKV, sh, mask_mode, window, IHA_DTYPE_BF16, Pbar, lse, ld, st, status);
     // Vbar again, in bf16: the V third of Y mixed with alpha_V
     if (e == cudaSuccess)
         e = launch_mix_sets(Y + (size_t)2 * D * 2, alpha_V, alpha_V, alpha_V, sh, 1, Vb, st, status, 3, -1);
+    if (e == cudaSuccess && out) e = launch_contract_tc(Pbar, R, sh, out, st, status);
+    return e;
+}
+
+// Everything after the forward pieces: the gradients of every input.
+static cudaError_t bwd_gradients(const void *X, const void *W_Q, const void *W_K, const void *W_V,
+                                 const float *alpha_Q, const float *alpha_K, const float *alpha_V, const float *R,
+                                 const Shape &sh, int mask_mode, int window, const void *dO, void *dX, void *dW_Q,
+                                 void *dW_K, void *dW_V, float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR,
+                                 const BwdLayout &lay, uint8_t *ws, cudaStream_t st, int *status) {
+    const int H = sh.H, d = sh.d;
+    const long long T = (long long)sh.B * sh.N, D = sh.D(), HP = (long long)H * sh.P;
+    uint8_t *Y = ws + lay.y, *QKV = ws + lay.qkv, *Vb = ws + lay.vb, *Pbar = ws + lay.pbar, *dPst = ws + lay.dpst,
+            *dS = ws + lay.ds, *dY = ws + lay.dy;
+    float *lse = reinterpret_cast<float *>(ws + lay.lse), *Dv = reinterpret_cast<float *>(ws + lay.dv);
+    float *part = reinterpret_cast<float *>(ws + lay.part);
+    const size_t ds_bytes = (size_t)T * HP * d * 2, dy_bytes = (size_t)T * D * 2;
+    const size_t third = (size_t)sh.qkv_elems() * 2;
+    const int ld = bwd_ld_stride(sh.L());
+    const void *W[3] = {W_Q, W_K, W_V};
+    const float *alpha[3] = {alpha_Q, alpha_K, alpha_V};
+    float *dalpha[3] = {dalpha_Q, dalpha_K, dalpha_V};
+    void *dW[3] = {dW_Q, dW_K, dW_V};
+    const void *dYs[3] = {dY, dY + dy_bytes, dY + 2 * dy_bytes};
+
     // dPbar (stacked) = dO mixed with R in alpha's place
-    if (e == cudaSuccess) e = launch_mix_sets(dO, R, R, R, sh, 1, dPst, st, status);
+    cudaError_t e = launch_mix_sets(dO, R, R, R, sh, 1, dPst, st, status);
     if (e == cudaSuccess) e = launch_bwd_gram(dO, D, H, Pbar, HP * d, (int)HP, d, T, part, dR, st, status);
     if (e == cudaSuccess) e = launch_bwd_rowdot(dPst, Pbar, sh, ld, Dv, st);
     if (e == cudaSuccess)
@@ -140,11 +146,98 @@ int iha_backward(const void *X, const void *W_Q, const void *W_K, const void *W_
     }
     if (e == cudaSuccess) e = launch_bwd_dx_tc(dYs, W, T, (int)D, dX, st, status);
     if (e == cudaSuccess) e = launch_bwd_dw_tc(X, dYs, T, (int)D, dW, st, status);
+    return e;
+}
+
+// The checks shared by the three entry points; the workspace (caller's, or allocated).
+static int bwd_begin(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
+                     const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
+                     int mask_mode, int window, const void *o_or_dO, int dtype, cudaStream_t st, void *&workspace,
+                     size_t workspace_bytes, bool &own, bool may_allocate) {
+    int rc = check_forward_args(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window,
+                                o_or_dO, dtype);
+    if (rc != IHA_OK) return rc;
+    const Shape sh{B, N, H, d, P};
+    if (!bwd_supported(sh, dtype)) return IHA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(o_or_dO) & 15) != 0) return IHA_ERR_INVALID_ARG;   // read or written by TMA
+    const BwdLayout lay = bwd_layout(sh);
+    own = false;
+    if (!workspace) {
+        if (!may_allocate) return IHA_ERR_WORKSPACE;
+        if (cudaMallocAsync(&workspace, lay.total, st) != cudaSuccess) return IHA_ERR_CUDA;
+        own = true;
+    } else if (workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255)) {
+        return IHA_ERR_WORKSPACE;
+    }
+    return IHA_OK;
+}
+
+static int bwd_end(cudaError_t e, bool own, void *workspace, cudaStream_t st) {
     if (own) {
         const cudaError_t e2 = cudaFreeAsync(workspace, st);
         if (e == cudaSuccess) e = e2;
     }
     return e == cudaSuccess ? IHA_OK : IHA_ERR_CUDA;
+}
+
+}  // namespace iha
+
+extern "C" {
+
+int iha_backward(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
+                 const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
+                 int mask_mode, int window, const void *dO, void *dX, void *dW_Q, void *dW_K, void *dW_V,
+                 float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR, int dtype, void *stream,
+                 void *workspace, size_t workspace_bytes) {
+    if (!dX || !dW_Q || !dW_K || !dW_V || !dalpha_Q || !dalpha_K || !dalpha_V || !dR) return IHA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool own = false;
+    int rc = bwd_begin(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, dO, dtype,
+                       st, workspace, workspace_bytes, own, true);
+    if (rc != IHA_OK) return rc;
+    const Shape sh{B, N, H, d, P};
+    const BwdLayout lay = bwd_layout(sh);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int *status = status_word_ptr();
+    cudaError_t e = bwd_forward_pieces(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, sh, mask_mode, window, nullptr,
+                                       lay, ws, st, status);
+    if (e == cudaSuccess)
+        e = bwd_gradients(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, sh, mask_mode, window, dO, dX, dW_Q, dW_K,
+                          dW_V, dalpha_Q, dalpha_K, dalpha_V, dR, lay, ws, st, status);
+    return bwd_end(e, own, workspace, st);
+}
+
+int iha_forward_train(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
+                      const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
+                      int mask_mode, int window, void *out, int dtype, void *stream, void *workspace,
+                      size_t workspace_bytes) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool own = false;
+    int rc = bwd_begin(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, out, dtype,
+                       st, workspace, workspace_bytes, own, false);
+    if (rc != IHA_OK) return rc;
+    const Shape sh{B, N, H, d, P};
+    return bwd_end(bwd_forward_pieces(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, sh, mask_mode, window, out,
+                                      bwd_layout(sh), static_cast<uint8_t *>(workspace), st, status_word_ptr()),
+                   own, workspace, st);
+}
+
+int iha_backward_saved(const void *X, const void *W_Q, const void *W_K, const void *W_V, const float *alpha_Q,
+                       const float *alpha_K, const float *alpha_V, const float *R, int B, int N, int H, int d, int P,
+                       int mask_mode, int window, const void *dO, void *dX, void *dW_Q, void *dW_K, void *dW_V,
+                       float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR, int dtype, void *stream,
+                       void *workspace, size_t workspace_bytes) {
+    if (!dX || !dW_Q || !dW_K || !dW_V || !dalpha_Q || !dalpha_K || !dalpha_V || !dR) return IHA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool own = false;
+    int rc = bwd_begin(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, dO, dtype,
+                       st, workspace, workspace_bytes, own, false);
+    if (rc != IHA_OK) return rc;
+    const Shape sh{B, N, H, d, P};
+    return bwd_end(bwd_gradients(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, sh, mask_mode, window, dO, dX, dW_Q,
+                                 dW_K, dW_V, dalpha_Q, dalpha_K, dalpha_V, dR, bwd_layout(sh),
+                                 static_cast<uint8_t *>(workspace), st, status_word_ptr()),
+                   own, workspace, st);
 }
 
 }  // extern "C"
