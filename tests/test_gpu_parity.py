@@ -415,7 +415,9 @@ BWD_TOL = 3e-2   # RMS(err) <= BWD_TOL * RMS(ref) per gradient tensor
     (2, 40, 4, 64, 2, C, 0), (1, 37, 4, 64, 3, WN, 9), (1, 50, 2, 128, 4, C, 0),
     (2, 33, 4, 64, 1, NM, 0), (1, 45, 16, 64, 2, WN, 20), (1, 70, 8, 128, 2, C, 0),
     # several 128-row tiles and 64-row blocks with a ragged tail: stacked lengths 600, 800, 1024
-    (1, 300, 4, 64, 2, WN, 37), (1, 200, 4, 128, 4, WN, 50), (1, 512, 8, 128, 2, C, 0)])
+    (1, 300, 4, 64, 2, WN, 37), (1, 200, 4, 128, 4, WN, 50), (1, 512, 8, 128, 2, C, 0),
+    # the causal N=1024 d=64 P=2 workload's shape with one batch element (stacked length 2048)
+    (1, 1024, 16, 64, 2, C, 0)])
 def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
     from oracle import backward as bwd
     w = gi.Workload("bwd", B=B, N=N, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=90 + P)
