@@ -57,6 +57,36 @@ def forward(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, *, H, d, P, mask_mod
     return O.reshape(B, N, H * d)
 
 
+def cancellation_scale(inputs: dict, dO, *, H, d, P, mask_mode=0, window=0):
+    """The gradients of every input reached through the scores by the term P * D alone, where
+    D_r = dPbar_r . Pbar_r: the softmax derivative ("注意力机制" eqs. (5.24)-(5.31)) gives
+    dS = P * (dP - D), and D computed from a rounded attention output carries a relative
+    error that dS inherits at the size of P * D, not of dS (which may cancel to 0).  These
+    tensors set the absolute scale of that error in a tolerance; float64, keys of PARAMS
+    (zeros for the inputs the scores do not depend on)."""
+    leaves = {k: torch.as_tensor(inputs[k], dtype=torch.float64).clone().requires_grad_(True) for k in PARAMS}
+    X, W_Q, W_K, W_V = leaves["X"], leaves["W_Q"], leaves["W_K"], leaves["W_V"]
+    B, N, D_ = X.shape
+    ok = _allowed(N, P, mask_mode, window)
+
+    def pseudo(W, alpha):
+        Y = (X @ W).reshape(B, N, H, d)
+        return torch.einsum("mhj,btmc->bhjtc", alpha, Y).reshape(B, H, P * N, d)
+
+    Qb, Kb = pseudo(W_Q, leaves["alpha_Q"]), pseudo(W_K, leaves["alpha_K"])
+    Vb = pseudo(W_V, leaves["alpha_V"]).detach()
+    S = ((Qb @ Kb.transpose(-1, -2)) / math.sqrt(d)).masked_fill(~ok, float("-inf"))
+    A = torch.softmax(S, dim=-1).detach()
+    Pb = (A @ Vb).requires_grad_(True)
+    Pu = Pb.reshape(B, H, P, N, d).reshape(B, H * P, N, d)
+    O = torch.einsum("hk,bktc->bthc", leaves["R"].detach(), Pu).reshape(B, N, H * d)
+    (dPb,) = torch.autograd.grad(O, Pb, torch.as_tensor(dO, dtype=torch.float64))
+    Dr = (dPb * Pb.detach()).sum(-1, keepdim=True)
+    S_fin = S.masked_fill(~ok, 0.0)   # the masked entries carry no gradient (A = 0 there)
+    grads = torch.autograd.grad(S_fin, [leaves[k] for k in PARAMS], -(A * Dr), allow_unused=True)
+    return {k: (g.detach() if g is not None else torch.zeros_like(leaves[k])) for k, g in zip(PARAMS, grads)}
+
+
 def backward(inputs: dict, dO, *, H, d, P, mask_mode=0, window=0):
     """Gradients of sum(out * dO) for every input of Algorithm 1; float64 numpy-compatible
     tensors in, a dict of float64 tensors (same keys as PARAMS) out."""

@@ -353,7 +353,9 @@ def test_layer_stack(iha, P_local, N):
     (2, 128, 1, C, 0, 37),
     # long caches: many 128-row tiles per chunk, several chunks, a ragged last tile, and (window)
     # a first readable row that is not tile-aligned
-    (2, 128, 4, C, 0, 700), (3, 128, 2, WN, 333, 900)])
+    (2, 128, 4, C, 0, 700), (3, 128, 2, WN, 333, 900),
+    # window 1: each decoded token reads only its own P pseudo-keys
+    (2, 128, 4, WN, 1, 37), (4, 64, 2, WN, 1, 37)])
 def test_decode_matches_oracle(iha, H, d, P, mode, window, T):
     B, steps = 2, 4
     n_all = T + steps
@@ -408,7 +410,11 @@ def test_decode_from_empty_cache(iha, d, P):
 # backward pass: every gradient against the fp64 autograd oracle (oracle/backward.py)
 # ---------------------------------------------------------------------------
 
-BWD_TOL = 3e-2   # RMS(err) <= BWD_TOL * RMS(ref) per gradient tensor
+BWD_TOL = 3e-2   # RMS(err) <= BWD_TOL * RMS(ref) per gradient tensor ...
+# ... + CANCEL_TOL * RMS(the gradient reached through the scores by P * D alone): D =
+# dPbar . Pbar is formed from the bf16 attention output (relative error ~2^-8), and
+# dS = P (dP - D) inherits that error at the size of P * D even where dP - D cancels
+CANCEL_TOL = 2.0 ** -6
 
 
 @pytest.mark.parametrize("B,N,H,d,P,mode,window", [
@@ -417,7 +423,12 @@ BWD_TOL = 3e-2   # RMS(err) <= BWD_TOL * RMS(ref) per gradient tensor
     # several 128-row tiles and 64-row blocks with a ragged tail: stacked lengths 600, 800, 1024
     (1, 300, 4, 64, 2, WN, 37), (1, 200, 4, 128, 4, WN, 50), (1, 512, 8, 128, 2, C, 0),
     # the causal N=1024 d=64 P=2 workload's shape with one batch element (stacked length 2048)
-    (1, 1024, 16, 64, 2, C, 0)])
+    (1, 1024, 16, 64, 2, C, 0),
+    # degenerate cases: one token; window 1 (each pseudo-query reads its own token's P
+    # pseudo-keys); a window >= N (= causal); H*P = 128 with P = 8; one head (D = 64, narrower
+    # than one GEMM tile, and one row of the token grams)
+    (1, 1, 2, 64, 1, C, 0), (2, 60, 4, 128, 2, WN, 1), (1, 90, 2, 64, 3, WN, 500), (1, 40, 16, 64, 8, C, 0),
+    (3, 33, 1, 64, 2, C, 0)])
 def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
     from oracle import backward as bwd
     w = gi.Workload("bwd", B=B, N=N, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=90 + P)
@@ -437,12 +448,14 @@ def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
     rc, code = iha.iha_check_device_status()
     assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
     ref = bwd.backward(gi.as_f64(inp), dO.double(), H=H, d=d, P=P, mask_mode=mode, window=window)
+    scale = bwd.cancellation_scale(gi.as_f64(inp), dO.double(), H=H, d=d, P=P, mask_mode=mode, window=window)
     for k in bwd.PARAMS:
         got = out[k].double().cpu().numpy()
         r = ref[k].numpy()
         assert np.isfinite(got).all(), k
         err = rms(got - r)
-        assert err <= BWD_TOL * rms(r), f"{k}: rms err {err:.3g} vs rms ref {rms(r):.3g}"
+        bound = BWD_TOL * rms(r) + CANCEL_TOL * rms(scale[k].numpy())
+        assert err <= bound, f"{k}: rms err {err:.3g} vs rms ref {rms(r):.3g}, bound {bound:.3g}"
 
 
 @pytest.mark.parametrize("B,N,H,d,P,mode,window", [

@@ -535,3 +535,48 @@ def test_backward_oracle_matches_finite_differences(case):
         fd = (f(plus) - f(minus)) / (2 * eps)
         an = float((grads[k].numpy() * v).sum())
         assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (k, fd, an)
+
+
+def test_cancellation_scale_closed_form():
+    """One token, one head, P = 1: the softmax has one entry (p = 1), so the term P*D alone
+    is -D with D = dPbar . v, v = alpha_V x W_V, dPbar = R dO; through s = (alpha_Q x W_Q) .
+    (alpha_K x W_K) / sqrt(d) it gives dW_Q[i][c] = -D alpha_Q alpha_K x_i (x W_K)_c / sqrt(d)
+    and symmetrically for W_K, X and the alphas; the value-path inputs get nothing."""
+    import torch
+    from oracle import backward as bwd
+    rng = np.random.default_rng(5)
+    d = 6
+    p = rand_problem(rng, 1, 1, 1, d, 1)
+    dO = rng.standard_normal((1, 1, d))
+    sc = bwd.cancellation_scale(p, dO, H=1, d=d, P=1, mask_mode=1)
+    x = p["X"][0, 0]
+    aq, ak, av, r = p["alpha_Q"][0, 0, 0], p["alpha_K"][0, 0, 0], p["alpha_V"][0, 0, 0], p["R"][0, 0]
+    yq, yk, yv = x @ p["W_Q"], x @ p["W_K"], x @ p["W_V"]
+    D = float((r * dO[0, 0]) @ (av * yv))
+    g = -D / np.sqrt(d)
+    np.testing.assert_allclose(sc["W_Q"].numpy(), g * aq * ak * np.outer(x, yk), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sc["W_K"].numpy(), g * aq * ak * np.outer(x, yq), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sc["X"].numpy()[0, 0], g * aq * ak * (p["W_Q"] @ yk + p["W_K"] @ yq), rtol=1e-10,
+                               atol=1e-12)
+    np.testing.assert_allclose(float(sc["alpha_Q"].numpy()[0, 0, 0]), g * ak * float(yq @ yk), rtol=1e-10)
+    np.testing.assert_allclose(float(sc["alpha_K"].numpy()[0, 0, 0]), g * aq * float(yq @ yk), rtol=1e-10)
+    for k in ("W_V", "alpha_V", "R"):
+        assert not sc[k].numpy().any(), k
+
+
+@pytest.mark.parametrize("case", BWD_CASES)
+def test_cancellation_scale_linear_in_dO(case):
+    """The scale is linear in dO (D is) and zero for the value-path inputs at any shape."""
+    from oracle import backward as bwd
+    B, N, H, d, P, mode, w = case
+    rng = np.random.default_rng(888 + P)
+    p = rand_problem(rng, B, N, H, d, P)
+    d1, d2 = rng.standard_normal((2, B, N, H * d))
+    s1 = bwd.cancellation_scale(p, d1, H=H, d=d, P=P, mask_mode=mode, window=w)
+    s2 = bwd.cancellation_scale(p, d2, H=H, d=d, P=P, mask_mode=mode, window=w)
+    s12 = bwd.cancellation_scale(p, 2.0 * d1 - d2, H=H, d=d, P=P, mask_mode=mode, window=w)
+    for k in bwd.PARAMS:
+        np.testing.assert_allclose(s12[k].numpy(), 2.0 * s1[k].numpy() - s2[k].numpy(), rtol=1e-9,
+                                   atol=1e-9 * (1 + np.abs(s1[k].numpy()).max()))
+    for k in ("W_V", "alpha_V", "R"):
+        assert not s1[k].numpy().any(), k
