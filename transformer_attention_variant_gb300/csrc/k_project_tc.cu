@@ -16,7 +16,10 @@
 // A and B tiles, 4-stage ring), warp 1 = MMA issuer (tcgen05.mma kind::f16, M=128 N=256
 // K=16, fp32 accumulators in TMEM, double-buffered so the epilogue of one tile overlaps
 // the main loop of the next), warps 2-5 = epilogue (tcgen05.ld -> bf16 -> global; the
-// Vbar third is written as f16, the type the attention kernel's P V product uses).
+// Vbar third is written as f16, the type the attention kernel's P V product uses; in the
+// PLAIN mode each 64-column chunk is staged 128B-swizzled in shared memory and sent with one
+// TMA tensor store -- stores straight from registers, one row per lane, cost 13-15% of the
+// GEMM's time).
 #include <cuda_bf16.h>
 
 #include "iha_internal.h"
@@ -30,6 +33,9 @@ constexpr int PG_A_BYTES = PG_M * PG_K * 2;   // 16 KB
 constexpr int PG_B_BYTES = PG_N * PG_K * 2;   // 32 KB
 constexpr int PG_THREADS = 192;
 constexpr int PG_SMEM = PG_STAGES * (PG_A_BYTES + PG_B_BYTES) + 256 + 1024;
+constexpr int PG_STG_BYTES = PG_M * 128;   // one staged 64-column chunk of the plain epilogue
+constexpr int PG_SMEM_PLAIN = PG_SMEM + 2 * PG_STG_BYTES;
+static_assert(PG_SMEM_PLAIN <= 232448, "shared memory");
 
 struct ProjParams {
     __nv_bfloat16 *qkv;   // folded mode: stacked output
@@ -46,12 +52,14 @@ struct ProjParams {
 template <bool PLAIN>
 __global__ void __launch_bounds__(PG_THREADS, 1)
 proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, const ProjParams p) {
+             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+             const __grid_constant__ CUtensorMap tmY, const ProjParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + PG_STAGES * PG_A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + PG_STAGES * PG_B_BYTES);
+    uint8_t *sStg = sB + PG_STAGES * PG_B_BYTES;   // plain epilogue: 2 staged chunks
+    uint64_t *full = reinterpret_cast<uint64_t *>(sStg + (PLAIN ? 2 * PG_STG_BYTES : 0));
     uint64_t *empty = full + PG_STAGES;
     uint64_t *tfull = empty + PG_STAGES;
     uint64_t *tempty = tfull + 2;
@@ -77,6 +85,7 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         if (PLAIN) {
             tma_prefetch_desc(&tmB1);
             tma_prefetch_desc(&tmB2);
+            tma_prefetch_desc(&tmY);
         }
     }
     if (warp == 1) {
@@ -160,6 +169,8 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
         const long long HPd = (long long)p.H * p.P * p.d, Pd = (long long)p.P * p.d;
+        const bool issuer = warp == 2 && lane == 0;   // sends the staged chunks (plain mode)
+        int staged = 0;                               // chunks staged so far (plain mode)
         int it = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
@@ -167,6 +178,41 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             if (!mbar_wait(&tfull[acc], acc_phase, p.status, kSiteProjEpilogue, abort_flag)) break;
             tc_fence_after();
             const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+            if (PLAIN) {
+                // Y tile -> bf16 -> a 128B-swizzled chunk of 64 columns in shared memory (each
+                // thread writes its row) -> one TMA store per chunk (rows past M are clipped);
+                // two chunk buffers, so a chunk is converted while the previous one is sent
+                const int s = nt / p.ntps;
+                const int ncol0 = (nt % p.ntps) * PG_N;
+#pragma unroll 1
+                for (int cc = 0; cc < PG_N / 64 && ncol0 + cc * 64 < p.hd; ++cc, ++staged) {
+                    uint8_t *stg = sStg + (staged & 1) * PG_STG_BYTES;
+                    if (issuer) bulk_wait_read(1);   // the store that last read this buffer is done
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    uint32_t r[2][32];
+                    tmem_ld32(tmem_base + acc * PG_N + cc * 64 + (uint32_t(q * 32) << 16), r[0]);
+                    tmem_ld32(tmem_base + acc * PG_N + cc * 64 + 32 + (uint32_t(q * 32) << 16), r[1]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {   // 16-byte unit u of the row: columns 8u .. 8u+7
+                        const uint32_t *rr = r[u / 4] + (u % 4) * 8;
+                        *reinterpret_cast<uint4 *>(stg + row_in_tile * 128 + ((u ^ (row_in_tile & 7)) << 4)) =
+                            make_uint4(pack_bf16x2(__uint_as_float(rr[0]), __uint_as_float(rr[1])),
+                                       pack_bf16x2(__uint_as_float(rr[2]), __uint_as_float(rr[3])),
+                                       pack_bf16x2(__uint_as_float(rr[4]), __uint_as_float(rr[5])),
+                                       pack_bf16x2(__uint_as_float(rr[6]), __uint_as_float(rr[7])));
+                    }
+                    fence_proxy_async_smem();   // the staging writes before the TMA store reads them
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (issuer) {
+                        tma_store_2d(&tmY, stg, s * p.hd + ncol0 + cc * 64, mt * PG_M);
+                        bulk_commit();
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
+                continue;
+            }
             const long long m = (long long)mt * PG_M + row_in_tile;
             const bool row_ok = m < p.M;
             const long long b = m / p.N_tok, t = m % p.N_tok;
@@ -175,21 +221,6 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 uint32_t r[32];
                 tmem_ld32(tmem_base + acc * PG_N + c0 + (uint32_t(q * 32) << 16), r);
                 tmem_ld_wait();
-                if (PLAIN) {
-                    const int s = nt / p.ntps;
-                    const long long n = (long long)(nt % p.ntps) * PG_N + c0;
-                    if (row_ok && n < p.hd) {
-                        uint4 v[4];
-                        uint32_t *vw = reinterpret_cast<uint32_t *>(v);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            vw[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                        uint4 *d4 = reinterpret_cast<uint4 *>(p.y + m * (3LL * p.hd) + (long long)s * p.hd + n);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) d4[i] = v[i];
-                    }
-                    continue;
-                }
                 const long long n = (long long)nt * PG_N + c0;
                 if (row_ok && n < p.Ncols) {
                     // columns n..n+31 lie in one (s, h) block because P*d is a multiple of 32
@@ -214,6 +245,7 @@ proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
+        if (PLAIN && issuer) bulk_wait_all();   // the staged chunks are read and written before exit
     }
     tc_fence_before();
     __syncthreads();
@@ -259,7 +291,7 @@ cudaError_t launch_project(const void *X, const void *Wt, const Shape &sh, int d
     cudaError_t e = cudaFuncSetAttribute(proj_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < device_sm_count() ? p.num_tiles : device_sm_count();
-    proj_gemm_tc<false><<<grid, PG_THREADS, PG_SMEM, st>>>(tmA, tmB, tmB, tmB, p);
+    proj_gemm_tc<false><<<grid, PG_THREADS, PG_SMEM, st>>>(tmA, tmB, tmB, tmB, tmA, p);
     return cudaGetLastError();
 }
 
@@ -282,6 +314,13 @@ cudaError_t launch_project_heads(const void *X, const void *WQ, const void *WK, 
         const uint32_t box[3] = {64, PG_K, PG_N / 64};
         if (!make_tmap_bf16(&tmW[s], W[s], 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
+    CUtensorMap tmY;   // Y [M][3*hd] in 64-column x 128-row boxes (the epilogue's stores)
+    {
+        const uint64_t dims[2] = {(uint64_t)(3 * hd), (uint64_t)M};
+        const uint64_t strides[1] = {(uint64_t)(3 * hd) * 2};
+        const uint32_t box[2] = {64, PG_M};
+        if (!make_tmap_bf16(&tmY, Y, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
     ProjParams p{};
     p.y = (__nv_bfloat16 *)Y;
     p.hd = (int)hd;
@@ -295,10 +334,11 @@ cudaError_t launch_project_heads(const void *X, const void *WQ, const void *WK, 
     p.num_m_tiles = (int)((M + PG_M - 1) / PG_M);
     p.num_tiles = p.num_m_tiles * 3 * p.ntps;
     p.status = status;
-    cudaError_t e = cudaFuncSetAttribute(proj_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(proj_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM_PLAIN);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < device_sm_count() ? p.num_tiles : device_sm_count();
-    proj_gemm_tc<true><<<grid, PG_THREADS, PG_SMEM, st>>>(tmA, tmW[0], tmW[1], tmW[2], p);
+    proj_gemm_tc<true><<<grid, PG_THREADS, PG_SMEM_PLAIN, st>>>(tmA, tmW[0], tmW[1], tmW[2], tmY, p);
     return cudaGetLastError();
 }
 

@@ -215,6 +215,14 @@ __device__ __forceinline__ void tma_load_3d_mc(const CUtensorMap *map, uint64_t 
         : "memory");
 }
 
+// Tiled store shared -> global through a rank-2 tensor map (bulk groups as below).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // Tiled store shared -> global through a rank-5 tensor map, tracked by this thread's bulk
 // groups (bulk_commit / bulk_wait_*).  Elements outside the tensor are not written; no
 // coordinate may be negative.
