@@ -278,7 +278,8 @@ IHA_API int iha_decode_step(const void *x, const void *W_Q, const void *W_K, con
  * respect to iha_forward's output for the same inputs), the gradients with respect to every
  * input of Algorithm 1.  bf16 only, d in {64, 128}, H <= 16, H*P <= 128
  * (IHA_ERR_UNSUPPORTED otherwise); every mask mode.
- *   dX [B][N][H*d], dW_Q/dW_K/dW_V [H*d][H*d]: bfloat16, layouts of X and W;
+ *   dX [B][N][H*d], dW_Q/dW_K/dW_V [H*d][H*d]: bfloat16, layouts of X and W, 16-byte
+ *     aligned (IHA_ERR_INVALID_ARG otherwise; dO too);
  *   dalpha_Q/K/V [H][H][P] and dR [H][H*P]: float32, layouts of alpha and R.
  * The forward intermediates are recomputed inside the call.  workspace: NULL (allocated
  * and freed on `stream`) or iha_backward_workspace_bytes(...) bytes, 256-byte aligned. */

@@ -200,6 +200,16 @@ def test_training_pair_validation(iha):
         iha.IHA_ERR_INVALID_ARG
 
 
+def test_backward_gradient_alignment(iha):
+    fake = 1 << 40                                           # never dereferenced
+    B, N, H, d, P = 2, 64, 4, 64, 2
+    args = [fake] * 8
+    for i in range(4):   # dX, dW_Q, dW_K, dW_V are written by TMA stores
+        g = [fake] * 8
+        g[i] = fake + 8
+        assert iha.iha_backward(*args, B, N, H, d, P, 1, 0, fake, *g, 1) == iha.IHA_ERR_INVALID_ARG
+
+
 def test_backward_validation(iha):
     fake = 1 << 40                                           # never dereferenced
     B, N, H, d, P = 2, 64, 4, 64, 2

@@ -172,6 +172,12 @@ static int bwd_begin(const void *X, const void *W_Q, const void *W_K, const void
     return IHA_OK;
 }
 
+static bool grads_aligned(const void *a, const void *b, const void *c, const void *d) {
+    return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(c) |
+             reinterpret_cast<uintptr_t>(d)) &
+            15) == 0;
+}
+
 static int bwd_end(cudaError_t e, bool own, void *workspace, cudaStream_t st) {
     if (own) {
         const cudaError_t e2 = cudaFreeAsync(workspace, st);
@@ -190,6 +196,7 @@ int iha_backward(const void *X, const void *W_Q, const void *W_K, const void *W_
                  float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR, int dtype, void *stream,
                  void *workspace, size_t workspace_bytes) {
     if (!dX || !dW_Q || !dW_K || !dW_V || !dalpha_Q || !dalpha_K || !dalpha_V || !dR) return IHA_ERR_INVALID_ARG;
+    if (!grads_aligned(dX, dW_Q, dW_K, dW_V)) return IHA_ERR_INVALID_ARG;   // written by TMA stores
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool own = false;
     int rc = bwd_begin(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, dO, dtype,
@@ -228,6 +235,7 @@ int iha_backward_saved(const void *X, const void *W_Q, const void *W_K, const vo
                        float *dalpha_Q, float *dalpha_K, float *dalpha_V, float *dR, int dtype, void *stream,
                        void *workspace, size_t workspace_bytes) {
     if (!dX || !dW_Q || !dW_K || !dW_V || !dalpha_Q || !dalpha_K || !dalpha_V || !dR) return IHA_ERR_INVALID_ARG;
+    if (!grads_aligned(dX, dW_Q, dW_K, dW_V)) return IHA_ERR_INVALID_ARG;   // written by TMA stores
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool own = false;
     int rc = bwd_begin(X, W_Q, W_K, W_V, alpha_Q, alpha_K, alpha_V, R, B, N, H, d, P, mask_mode, window, dO, dtype,

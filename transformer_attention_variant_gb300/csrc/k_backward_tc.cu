@@ -41,7 +41,8 @@
 //     dX = sum_s dY_s W_s^T     (A = dY_s K-major, B = W_s K-major, 3 segments of K)
 //     dW_s = X^T dY_s           (A = X^T MN-major, B = dY_s MN-major, 3 problems)
 // as one persistent tcgen05 GEMM (M=128 N=256 K=64 tiles, 4-stage TMA ring, two TMEM
-// accumulators so that a tile's epilogue overlaps the next tile's main loop), bf16 out.
+// accumulators so that a tile's epilogue overlaps the next tile's main loop), bf16 out
+// through shared-memory staging and TMA tensor stores.
 #include <cuda_bf16.h>
 
 #include "iha_internal.h"
@@ -552,7 +553,9 @@ constexpr int BG_M = 128, BG_N = 256, BG_K = 64, BG_STAGES = 4;
 constexpr int BG_A_BYTES = BG_M * BG_K * 2;   // 16 KB
 constexpr int BG_B_BYTES = BG_N * BG_K * 2;   // 32 KB
 constexpr int BG_THREADS = 192;
-constexpr int BG_SMEM = BG_STAGES * (BG_A_BYTES + BG_B_BYTES) + 256 + 1024;
+constexpr int BG_STG_BYTES = BG_M * 128;   // one staged 64-column chunk of the epilogue
+constexpr int BG_SMEM = BG_STAGES * (BG_A_BYTES + BG_B_BYTES) + 2 * BG_STG_BYTES + 256 + 1024;
+static_assert(BG_SMEM <= 232448, "shared memory");
 
 struct BwdGemmParams {
     __nv_bfloat16 *c[3];   // outputs [M][N] row-major, one per problem
@@ -571,12 +574,14 @@ __global__ void __launch_bounds__(BG_THREADS, 1)
 bwd_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
             const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB0,
             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-            const BwdGemmParams p) {
+            const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
+            const __grid_constant__ CUtensorMap tmC2, const BwdGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + BG_STAGES * BG_A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + BG_STAGES * BG_B_BYTES);
+    uint8_t *sStg = sB + BG_STAGES * BG_B_BYTES;   // 2 staged output chunks
+    uint64_t *full = reinterpret_cast<uint64_t *>(sStg + 2 * BG_STG_BYTES);
     uint64_t *empty = full + BG_STAGES;
     uint64_t *tfull = empty + BG_STAGES;
     uint64_t *tempty = tfull + 2;
@@ -685,9 +690,13 @@ bwd_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
             mbar_wait(drain, 0, p.status, kSiteBwdGemmMma, nullptr, kWaitLimitNs);
         }
     } else {
-        // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1
+        // epilogue: warps 2..5 -> TMEM lane quarters 2, 3, 0, 1.  Each 64-column chunk of a tile
+        // is converted to bf16, staged 128B-swizzled in shared memory (each thread writes its
+        // row) and sent with one TMA tensor store (rows past M are clipped); two chunk buffers.
         const int q = warp & 3;
         const int row_in_tile = q * 32 + lane;
+        const bool issuer = warp == 2 && lane == 0;
+        int staged = 0;
         int it = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
@@ -696,26 +705,36 @@ bwd_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
             const int prob = tile / (p.num_m_tiles * p.num_n_tiles);
             const int rem = tile % (p.num_m_tiles * p.num_n_tiles);
             const int mt = rem % p.num_m_tiles, nt = rem / p.num_m_tiles;
-            const long long m = (long long)mt * BG_M + row_in_tile;
-            __nv_bfloat16 *crow = p.c[prob] + m * p.N;
+            const CUtensorMap *mc = prob == 0 ? &tmC0 : (prob == 1 ? &tmC1 : &tmC2);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BG_N; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + acc * BG_N + c0 + (uint32_t(q * 32) << 16), r);
+            for (int cc = 0; cc < BG_N / 64 && nt * BG_N + cc * 64 < p.N; ++cc, ++staged) {
+                uint8_t *stg = sStg + (staged & 1) * BG_STG_BYTES;
+                if (issuer) bulk_wait_read(1);   // the store that last read this buffer is done
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                uint32_t r[2][32];
+                tmem_ld32(tmem_base + acc * BG_N + cc * 64 + (uint32_t(q * 32) << 16), r[0]);
+                tmem_ld32(tmem_base + acc * BG_N + cc * 64 + 32 + (uint32_t(q * 32) << 16), r[1]);
                 tmem_ld_wait();
-                const int n = nt * BG_N + c0;
-                if (m < p.M && n < p.N) {   // N is a multiple of 32
-                    uint32_t w[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    uint4 *d4 = reinterpret_cast<uint4 *>(crow + n);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                for (int u = 0; u < 8; ++u) {   // 16-byte unit u of the row: columns 8u .. 8u+7
+                    const uint32_t *rr = r[u / 4] + (u % 4) * 8;
+                    *reinterpret_cast<uint4 *>(stg + row_in_tile * 128 + ((u ^ (row_in_tile & 7)) << 4)) =
+                        make_uint4(pack_bf16x2(__uint_as_float(rr[0]), __uint_as_float(rr[1])),
+                                   pack_bf16x2(__uint_as_float(rr[2]), __uint_as_float(rr[3])),
+                                   pack_bf16x2(__uint_as_float(rr[4]), __uint_as_float(rr[5])),
+                                   pack_bf16x2(__uint_as_float(rr[6]), __uint_as_float(rr[7])));
+                }
+                fence_proxy_async_smem();   // the staging writes before the TMA store reads them
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (issuer) {
+                    tma_store_2d(mc, stg, nt * BG_N + cc * 64, mt * BG_M);
+                    bulk_commit();
                 }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
+        if (issuer) bulk_wait_all();   // the staged chunks are read and written before exit
     }
     tc_fence_before();
     __syncthreads();
@@ -725,16 +744,28 @@ bwd_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CU
     }
 }
 
+// A row-major [rows][cols] bf16 output map, box [64 cols][BG_M rows] (the epilogue's stores)
+static bool out_map(CUtensorMap *m, const void *base, long long rows, long long cols) {
+    const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+    const uint64_t strides[1] = {(uint64_t)cols * 2};
+    const uint32_t box[2] = {64, BG_M};
+    return make_tmap_bf16(m, base, 2, dims, strides, box);
+}
+
 template <bool A_MN, bool B_MN>
 static cudaError_t launch_bwd_gemm_kernel(const CUtensorMap (&ta)[3], const CUtensorMap (&tb)[3], BwdGemmParams &p,
                                           cudaStream_t st) {
+    CUtensorMap tc[3];
+    for (int k = 0; k < 3; ++k)
+        if (!out_map(&tc[k], p.c[k], p.M, p.N)) return cudaErrorInvalidValue;
     p.num_m_tiles = (p.M + BG_M - 1) / BG_M;
     p.num_n_tiles = (p.N + BG_N - 1) / BG_N;
     p.num_tiles = p.nprob * p.num_m_tiles * p.num_n_tiles;
     cudaError_t e = cudaFuncSetAttribute(bwd_gemm_tc<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, BG_SMEM);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < device_sm_count() ? p.num_tiles : device_sm_count();
-    bwd_gemm_tc<A_MN, B_MN><<<grid, BG_THREADS, BG_SMEM, st>>>(ta[0], ta[1], ta[2], tb[0], tb[1], tb[2], p);
+    bwd_gemm_tc<A_MN, B_MN><<<grid, BG_THREADS, BG_SMEM, st>>>(ta[0], ta[1], ta[2], tb[0], tb[1], tb[2], tc[0], tc[1],
+                                                               tc[2], p);
     return cudaGetLastError();
 }
 
