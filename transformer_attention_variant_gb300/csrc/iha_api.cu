@@ -226,10 +226,17 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
             e = cudaMemcpyAsync(outh + r0 * row_x, static_cast<uint8_t *>(dOut) + r0 * row_x, (r1 - r0) * row_x,
                                 cudaMemcpyDeviceToHost, cs[i & 1]);
     }
-    // the call completes on st
-    for (int c = 0; c < 2 && e == cudaSuccess; ++c) {
-        e = cudaEventRecord(ev[3 + 2 * FH_CHUNKS + c], cs[c]);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[3 + 2 * FH_CHUNKS + c], 0);
+    // The call completes on st: st waits for everything queued on the copy streams -- also
+    // after an error, so that no copy still runs when the caller reuses its buffers (without
+    // the events, the host waits for the copy streams instead).
+    for (int c = 0; c < 2; ++c) {
+        const int k = 3 + 2 * FH_CHUNKS + c;
+        cudaError_t e2 = k < made ? cudaEventRecord(ev[k], cs[c]) : cudaErrorInvalidValue;
+        if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, ev[k], 0);
+        if (e2 != cudaSuccess) {
+            const cudaError_t e3 = cudaStreamSynchronize(cs[c]);
+            if (e == cudaSuccess) e = e3 != cudaSuccess ? e3 : e2;
+        }
     }
     for (int k = 0; k < made; ++k) cudaEventDestroy(ev[k]);   // released once their work is done
     return cuda_status(e);
