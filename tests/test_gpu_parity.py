@@ -389,6 +389,36 @@ def test_decode_matches_oracle(iha, H, d, P, mode, window, T):
     assert_parity(w, out_prompt.reshape(B * T, D).double().cpu().numpy(), oracle_rows(w, inp, rows=rows_p))
 
 
+@pytest.mark.parametrize("name", FULL)
+def test_decode_full_size_last_token(iha, name):
+    """The full-size workloads as `bench.py --decode` runs them: prefill N-1 tokens, then
+    decode token N-1 over the whole cache; its row against the oracle's row of the forward
+    over the whole sequence, and sampled prefill rows likewise."""
+    w = gi.WORKLOADS[name]
+    B, N, H, d, P, D = w.B, w.N, w.H, w.d, w.P, w.D
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    wts = [dinp[k] for k in ("W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")]
+    Kc = torch.zeros(B, H, N * P, d, dtype=torch.bfloat16, device="cuda:0")
+    Vc = torch.zeros(B, H, N * P, d, dtype=torch.float16, device="cuda:0")
+    X = dinp["X"]
+    out_prompt = torch.empty(B, N - 1, D, dtype=torch.bfloat16, device="cuda:0")
+    iha.check(iha.iha_prefill(X[:, :N - 1].contiguous(), *wts, B, N - 1, H, d, P, w.mask_mode, w.window, out_prompt,
+                              Kc, Vc, N, iha.IHA_DTYPE_BF16), "iha_prefill")
+    o = torch.empty(B, D, dtype=torch.bfloat16, device="cuda:0")
+    iha.check(iha.iha_decode_step(X[:, N - 1].contiguous(), *wts, B, H, d, P, w.mask_mode, w.window, Kc, Vc, N,
+                                  N - 1, o, iha.IHA_DTYPE_BF16), "iha_decode_step")
+    torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status()
+    assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
+    rows = [b * N + N - 1 for b in range(B)]
+    assert_parity(w, o.double().cpu().numpy(), oracle_rows(w, inp, rows=rows, projection="numpy"))
+    prows = [r for r in sample_rows(w) if r % N < N - 1]
+    got_p = out_prompt.double().cpu().numpy().reshape(B, N - 1, D)
+    assert_parity(w, np.stack([got_p[r // N, r % N] for r in prows]),
+                  oracle_rows(w, inp, rows=prows, projection="numpy"))
+
+
 @pytest.mark.parametrize("d,P", [(64, 2), (128, 4)])
 def test_decode_from_empty_cache(iha, d, P):
     """t = 0: the token reads only its own P pseudo-keys."""
