@@ -250,6 +250,11 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             if (it.bh < 0) break;
             const int bh = it.bh, kv_begin = it.kv_begin, nkv = it.nkv;
             const int r0 = it.qb * 2 * AT_BM;
+            // The Q tiles can only be loaded once the previous item's epilogue has sent its
+            // output through them; bring them into L2 now so that load does not wait on HBM.
+            if (leader)
+                for (int t = 0; t < 2; ++t)
+                    for (int c = 0; c < C::CHUNKS; ++c) tma_prefetch_3d(&tmQ, c * 64, r0 + t * AT_BM, bh);
             auto load_k = [&](int k) -> bool {
                 const int st = kc % C::KSTAGES;
                 if (!wait(&k_empty[st], ((kc / C::KSTAGES) & 1) ^ 1, kSiteAttnProducer)) return false;

@@ -204,6 +204,14 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap *map, uint64_t *ba
         : "memory");
 }
 
+// Prefetch a tile of a rank-3 tensor map into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // The same load delivered to the same shared-memory offset in every CTA of the cluster
 // named by cta_mask, each CTA's mbarrier at `bar`'s offset receiving the bytes it got.
 __device__ __forceinline__ void tma_load_3d_mc(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y, int z,
