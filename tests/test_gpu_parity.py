@@ -302,6 +302,30 @@ def test_forward_host_buffers(iha, B, N, H, d, P, mode, window):
         assert torch.equal(out, ref.cpu())
 
 
+def test_concurrent_streams_match_sequential(iha):
+    """Two layers of different shapes and masks run at once on two streams, each with its own
+    workspace, 8 times over: every result equals the same call run alone, bit for bit (the
+    attention launches draw their work counters from a shared ring)."""
+    ws = [W("conc_a", B=2, N=700, H=4, d=128, P=2, mask_mode=C, window=0, dtype="bf16", seed=61),
+          W("conc_b", B=1, N=900, H=8, d=64, P=4, mask_mode=WN, window=100, dtype="bf16", seed=62)]
+    dins = [to_dev(gi.make_inputs(w)) for w in ws]
+    refs = [run_gpu(iha, w, dinp=di) for w, di in zip(ws, dins)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for _ in range(8):
+        for w, di, st in zip(ws, dins, streams):
+            nb = iha.iha_workspace_bytes(w.B, w.N, w.H, w.d, w.P, iha.IHA_DTYPE_BF16)
+            buf = torch.empty(nb, dtype=torch.uint8, device="cuda:0")
+            with torch.cuda.stream(st):
+                outs.append((iha.forward(di, H=w.H, d=w.d, P=w.P, mask_mode=w.mask_mode, window=w.window,
+                                         stream=st, workspace=buf), buf))
+    torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status()
+    assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
+    for i, (o, _) in enumerate(outs):
+        assert torch.equal(o, refs[i % 2]), i
+
+
 def test_device_wait_timeout_is_reported(iha):
     """A wait that nothing will satisfy gives up after its limit, records its
     site, and the host reads IHA_ERR_TIMEOUT; the context stays usable."""
