@@ -7,16 +7,13 @@
 //   1. decode_proj:    y_s[b] = x[b] W_s (s = Q, K, V) as a split-K GEMV; W is read once.
 //   2. decode_mix:     q~/k~/v~_{h,j}[b] = sum_m alpha_s[m,h,j] y_s[b][m]; k~ and v~ go into
 //                      the cache at stacked row t*P + j, q~ into the workspace.
-//   3. decode_attn:    (d = 64; d = 128 runs decode_attn_tc, k_decode_tc.cu, on the tensor
-//                      cores) split-KV attention: a CTA takes a chunk of the cached rows of one
-//                      (b, h); a producer warp streams the chunk's K and V rows into a
-//                      6-stage shared-memory ring with bulk copies (about 96 KB in flight per
-//                      CTA); all P pseudo-queries share each row (eight lanes hold one key
-//                      row); online softmax per query; the chunk's (max, sum, unnormalised
-//                      output) go to the workspace.
+//   3. decode_attn_tc (k_decode_tc.cu): split-KV attention on the tensor cores, a CTA per
+//                      chunk of the readable cached rows of one (b, h); the chunk's (max, sum,
+//                      unnormalised output) of every query go to the workspace.
 //   4. decode_merge:   merge the chunks of every (b, h, j);
 //      decode_contract: the R contraction out[b][h][c] = sum_{h',j} R[h][h'P + j] Pbar[b][h'][j][c].
-// All four are HBM-bound: W (3 D^2 bf16) and the cached rows of K and V are the bytes.
+// The step is HBM-bound: W (3 D^2 bf16) and the cached rows of K and V are the bytes.  The
+// kernels are chained with programmatic dependent launch.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -206,210 +203,6 @@ decode_mix(const float *__restrict__ Yp, const float *__restrict__ aQ, const flo
 }
 
 // ---------------------------------------------------------------------------------------
-// 3. split-KV attention of the P pseudo-queries of token t
-// ---------------------------------------------------------------------------------------
-constexpr int DA_KT = 32;        // cached rows per ring stage
-constexpr int DA_STAGES = 5;
-constexpr int DA_CWARPS = 8;     // consumer warps; warp 8 is the producer
-constexpr int DA_THREADS = 32 * (DA_CWARPS + 1);
-
-template <int D>
-constexpr int da_smem_bytes() { return DA_STAGES * 2 * DA_KT * D * 2 + 2 * DA_STAGES * 8 + 16 + 128; }
-
-__device__ __forceinline__ float fast_ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-
-// A group of LPR = d/8 lanes holds one cached row, 8 dims (16 bytes) per lane: the group
-// reads its row's 16*LPR contiguous bytes per load (no bank conflict).
-template <int LPR, int PMAX>   // LPR = d / 8 lanes per row; PMAX = largest P
-__global__ void __launch_bounds__(DA_THREADS, PMAX <= 4 ? 2 : 1)
-decode_attn(const __nv_bfloat16 *__restrict__ qt, const __nv_bfloat16 *__restrict__ Kc, const __half *__restrict__ Vc,
-            int H, int P, long long cache_rows, long long lo, long long hi, int rows_per_chunk, float scale_log2,
-            float *__restrict__ part_ml, float *__restrict__ part_o, int *status) {
-    constexpr int DPL = 8;                        // dims per lane
-    constexpr int d = LPR * DPL;
-    constexpr int GPW = 32 / LPR;                 // rows (groups) per warp
-    constexpr int ROWB = d * 2;                   // bytes of one cached row
-    constexpr int STAGE = 2 * DA_KT * ROWB;       // K rows, then V rows
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + DA_STAGES * STAGE);
-    uint64_t *empty = full + DA_STAGES;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + DA_STAGES);
-    __shared__ float sm_ml[DA_CWARPS][PMAX][2];
-    __shared__ float sm_o[DA_CWARPS][PMAX][d];
-
-    pdl_trigger();
-    pdl_wait();   // the mixing kernel's q~ and appended cache rows
-    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, nch = gridDim.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long bh = (long long)b * H + h;
-    const long long r_begin = lo + (long long)chunk * rows_per_chunk;
-    const long long r_end = min(hi + 1, r_begin + rows_per_chunk);
-    const int nrows = (int)(r_end - r_begin);
-    const int nsub = (nrows + DA_KT - 1) / DA_KT;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < DA_STAGES; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], DA_CWARPS);
-        }
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    if (warp == DA_CWARPS) {
-        // ------------------------------- producer -----------------------------------
-        if (lane == 0) {
-            for (int i = 0; i < nsub; ++i) {
-                const int st = i % DA_STAGES;
-                if (!mbar_wait_lazy(&empty[st], ((i / DA_STAGES) & 1) ^ 1, status, kSiteDecodeProducer, abort_flag))
-                    break;
-                const int n = min(DA_KT, nrows - i * DA_KT);
-                const long long row = bh * cache_rows + r_begin + (long long)i * DA_KT;
-                mbar_arrive_expect_tx(&full[st], 2u * n * ROWB);
-                bulk_load(ring + st * STAGE, Kc + row * d, (uint32_t)(n * ROWB), &full[st]);
-                bulk_load(ring + st * STAGE + DA_KT * ROWB, Vc + row * d, (uint32_t)(n * ROWB), &full[st]);
-            }
-        }
-    } else {
-        // ------------------------------- consumers ----------------------------------
-        const int grp = lane / LPR, gl = lane % LPR;   // GPW groups of LPR lanes per warp
-        float q[PMAX][DPL];
-#pragma unroll
-        for (int j = 0; j < PMAX; ++j)
-#pragma unroll
-            for (int e = 0; e < DPL; ++e)
-                q[j][e] = j < P ? __bfloat162float(qt[((bh * P) + j) * d + gl * DPL + e]) * scale_log2 : 0.f;
-        float m[PMAX], l[PMAX], o[PMAX][DPL];
-#pragma unroll
-        for (int j = 0; j < PMAX; ++j) {
-            m[j] = -INFINITY;
-            l[j] = 0.f;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) o[j][e] = 0.f;
-        }
-        for (int i = 0; i < nsub; ++i) {
-            const int st = i % DA_STAGES;
-            // every lane waits (warp-uniform); a failed wait ends the warp's loop on all lanes
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (i / DA_STAGES) & 1, status,
-                                                               kSiteDecodeConsumer, abort_flag));
-            if (!ok) break;
-            const int n = min(DA_KT, nrows - i * DA_KT);
-            const uint8_t *ks = ring + st * STAGE, *vs = ks + DA_KT * ROWB;
-            // row groups warp, warp + DA_CWARPS, ... of the stage (GPW rows each); rows past n
-            // are skipped on every lane of their group
-            for (int qd = warp; qd < DA_KT / GPW; qd += DA_CWARPS) {
-                const int r = qd * GPW + grp;
-                const bool valid = r < n;
-                float kf[DPL], vf[DPL];
-                {
-                    const int off = r * ROWB + gl * 16;
-                    const uint4 ku = valid ? *reinterpret_cast<const uint4 *>(ks + off) : make_uint4(0, 0, 0, 0);
-                    const uint4 vu = valid ? *reinterpret_cast<const uint4 *>(vs + off) : make_uint4(0, 0, 0, 0);
-                    const uint32_t k4[4] = {ku.x, ku.y, ku.z, ku.w}, v4[4] = {vu.x, vu.y, vu.z, vu.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        kf[2 * e] = __uint_as_float(k4[e] << 16);
-                        kf[2 * e + 1] = __uint_as_float(k4[e] & 0xffff0000u);
-                        const __half2 vh = *reinterpret_cast<const __half2 *>(&v4[e]);
-                        const float2 vv = __half22float2(vh);
-                        vf[2 * e] = vv.x;
-                        vf[2 * e + 1] = vv.y;
-                    }
-                }
-                // the P scores as independent chains (queries past P have q = 0), then their
-                // reductions over the group's 8 lanes, then the online-softmax updates
-                float sc[PMAX];
-#pragma unroll
-                for (int j = 0; j < PMAX; ++j) sc[j] = 0.f;
-#pragma unroll
-                for (int e = 0; e < DPL; ++e)
-#pragma unroll
-                    for (int j = 0; j < PMAX; ++j) sc[j] = fmaf(q[j][e], kf[e], sc[j]);
-#pragma unroll
-                for (int off = LPR / 2; off >= 1; off >>= 1)
-#pragma unroll
-                    for (int j = 0; j < PMAX; ++j) sc[j] += __shfl_xor_sync(0xffffffffu, sc[j], off);
-                if (valid) {                                     // uniform over the group
-#pragma unroll
-                    for (int j = 0; j < PMAX; ++j) {
-                        if (j >= P) break;
-                        if (sc[j] > m[j]) {
-                            const float corr = fast_ex2(m[j] - sc[j]);   // m = -inf -> 0
-                            l[j] *= corr;
-#pragma unroll
-                            for (int e = 0; e < DPL; ++e) o[j][e] *= corr;
-                            m[j] = sc[j];
-                        }
-                        const float pr = fast_ex2(sc[j] - m[j]);
-                        l[j] += pr;
-#pragma unroll
-                        for (int e = 0; e < DPL; ++e) o[j][e] = fmaf(pr, vf[e], o[j][e]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);   // this warp is done with the stage
-        }
-        // merge the groups of the warp (lanes gl, gl + LPR, ... hold the same dims)
-#pragma unroll
-        for (int off = LPR; off < 32; off <<= 1) {
-#pragma unroll
-            for (int j = 0; j < PMAX; ++j) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m[j], off);
-                const float l2 = __shfl_xor_sync(0xffffffffu, l[j], off);
-                const float mn = fmaxf(m[j], m2);
-                const float c1 = m[j] == -INFINITY ? 0.f : exp2f(m[j] - mn);
-                const float c2 = m2 == -INFINITY ? 0.f : exp2f(m2 - mn);
-                l[j] = l[j] * c1 + l2 * c2;
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) {
-                    const float o2 = __shfl_xor_sync(0xffffffffu, o[j][e], off);
-                    o[j][e] = o[j][e] * c1 + o2 * c2;
-                }
-                m[j] = mn;
-            }
-        }
-        if (grp == 0) {
-#pragma unroll
-            for (int j = 0; j < PMAX; ++j) {
-                if (gl == 0) {
-                    sm_ml[warp][j][0] = m[j];
-                    sm_ml[warp][j][1] = l[j];
-                }
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) sm_o[warp][j][gl * DPL + e] = o[j][e];
-            }
-        }
-    }
-    __syncthreads();
-    // merge the consumer warps and write the chunk's partial result
-    for (int i = threadIdx.x; i < P * d; i += blockDim.x) {
-        const int j = i / d, c = i % d;
-        float mn = -INFINITY;
-        for (int w = 0; w < DA_CWARPS; ++w) mn = fmaxf(mn, sm_ml[w][j][0]);
-        float lt = 0.f, ot = 0.f;
-        for (int w = 0; w < DA_CWARPS; ++w) {
-            const float mw = sm_ml[w][j][0];
-            const float cw = mw == -INFINITY ? 0.f : exp2f(mw - mn);
-            lt += sm_ml[w][j][1] * cw;
-            ot += sm_o[w][j][c] * cw;
-        }
-        const size_t pidx = ((size_t)bh * nch + chunk) * P + j;
-        part_o[pidx * d + c] = ot;
-        if (c == 0) {
-            part_ml[pidx * 2] = mn;
-            part_ml[pidx * 2 + 1] = lt;
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------------------
 // 4a. merge the chunks of one (b, h', j): Pbar[b][h'*P + j][c], one thread per column; the
 //     chunks' partial results are read 16 at a time, all loads of a group in flight
 // ---------------------------------------------------------------------------------------
@@ -480,7 +273,7 @@ __global__ void decode_contract(const float *__restrict__ pbar, const float *__r
 // ---------------------------------------------------------------------------------------
 bool decode_tc_supported(int d, int P, const void *Kc, const void *Vc);
 int decode_tc_chunks(int B, int H, long long rows, int max_chunks, int &rows_per_chunk);
-cudaError_t launch_decode_attn_tc(const void *qt, const void *Kc, const void *Vc, int B, int H, int P,
+cudaError_t launch_decode_attn_tc(const void *qt, const void *Kc, const void *Vc, int B, int H, int d, int P,
                                   long long cache_rows, long long lo, long long hi, int nch, int rows_per_chunk,
                                   float *part_ml, float *part_o, cudaStream_t st, int *status);
 
@@ -565,52 +358,16 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
     long long lo = 0;
     if (mask_mode == 2) lo = (t - window + 1) * P > 0 ? (t - window + 1) * P : 0;
     const long long rows = hi - lo + 1;
-    if (decode_tc_supported(d, P, Kc, Vc)) {
-        // d = 128: the tensor-core kernel (k_decode_tc.cu)
-        int rpc = 0;
-        const int nch = decode_tc_chunks(B, H, rows, DC_NCH_MAX, rpc);
-        e = launch_decode_attn_tc(qt, Kc, Vc, B, H, P, cache_rows, lo, hi, nch, rpc, part_ml, part_o, st, status);
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(decode_merge, dim3(B * H, P), dim3(d), 0, st, (const float *)part_ml, (const float *)part_o, H,
-                       d, P, nch, pbar);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(decode_contract, dim3(B, H), dim3(d), 0, st, (const float *)pbar, R, H, d, P,
-                          (__nv_bfloat16 *)out);
-    }
-    // one wave of resident CTAs: chunks per (b, h) = resident CTAs / (B * H)
-    int occ = 1;
-    if (d == 128) {
-        e = cudaFuncSetAttribute(decode_attn<16, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, da_smem_bytes<128>());
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_attn<16, 4>, DA_THREADS, da_smem_bytes<128>());
-    } else {
-        e = cudaFuncSetAttribute(decode_attn<8, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, da_smem_bytes<64>());
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_attn<8, 8>, DA_THREADS, da_smem_bytes<64>());
-    }
-    if (e != cudaSuccess) return e;
-    if (occ < 1) occ = 1;
-    long long nch = ((long long)occ * device_sm_count()) / ((long long)B * H);
-    if (nch > (rows + 63) / 64) nch = (rows + 63) / 64;
-    if (nch > DC_NCH_MAX) nch = DC_NCH_MAX;
-    if (nch < 1) nch = 1;
-    const int rpc = (int)((rows + nch - 1) / nch);
-    nch = (rows + rpc - 1) / rpc;
-    const float sl2 = 1.4426950408889634f / sqrtf((float)d);
-    const dim3 g3((unsigned)nch, H, B);
-    if (d == 128) {
-        e = launch_pdl(decode_attn<16, 4>, g3, dim3(DA_THREADS), da_smem_bytes<128>(), st, (const __nv_bfloat16 *)qt,
-                       (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P, cache_rows, lo, hi, rpc, sl2, part_ml,
-                       part_o, status);
-    } else {
-        e = launch_pdl(decode_attn<8, 8>, g3, dim3(DA_THREADS), da_smem_bytes<64>(), st, (const __nv_bfloat16 *)qt,
-                       (const __nv_bfloat16 *)Kc, (const __half *)Vc, H, P, cache_rows, lo, hi, rpc, sl2, part_ml,
-                       part_o, status);
-    }
+    // 3. attention over the readable cached rows [lo, hi] on the tensor cores (k_decode_tc.cu),
+    //    one wave of CTAs over the chunks of every (b, h)
+    if (!decode_tc_supported(d, P, Kc, Vc)) return cudaErrorInvalidValue;   // checked by the entry point
+    int rpc = 0;
+    const int nch = decode_tc_chunks(B, H, rows, DC_NCH_MAX, rpc);
+    e = launch_decode_attn_tc(qt, Kc, Vc, B, H, d, P, cache_rows, lo, hi, nch, rpc, part_ml, part_o, st, status);
     if (e != cudaSuccess) return e;
     // 4. merge the chunks, then the contraction
     e = launch_pdl(decode_merge, dim3(B * H, P), dim3(d), 0, st, (const float *)part_ml, (const float *)part_o, H, d,
-                   P, (int)nch, pbar);
+                   P, nch, pbar);
     if (e != cudaSuccess) return e;
     return launch_pdl(decode_contract, dim3(B, H), dim3(d), 0, st, (const float *)pbar, R, H, d, P,
                       (__nv_bfloat16 *)out);

@@ -1,5 +1,5 @@
-// k_decode_tc.cu -- the attention of one decoding step on the tcgen05 tensor cores (d = 128,
-// P <= 4): the P pseudo-queries of the new token t against the cached pseudo-keys and
+// k_decode_tc.cu -- the attention of one decoding step on the tcgen05 tensor cores (d = 128
+// with P <= 4, d = 64 with P <= 8): the P pseudo-queries of the new token t against the cached pseudo-keys and
 // pseudo-values it may read ("Interleaved Head Attention" section 4, Algorithm 1, step
 // "注意力計算" for the rows of token t; the mask is by original position, so every
 // pseudo-query of t reads the same cached rows [lo, hi]).
@@ -7,7 +7,7 @@
 // A CTA takes a chunk of the readable rows of one (b, h) and walks it in tiles of 128 rows:
 //   S^T  = K_tile Q^T     (M = 128 cached rows, N = 16 -- the P queries padded with zero
 //                          rows, K = d; bf16, fp32 in TMEM)
-//   O^T_tile = V_tile^T P^T (M = d = 128, N = 16, K = 128 rows; f16 V and P)
+//   O^T_tile = V_tile^T P^T (M = 128 >= d, N = 16, K = 128 rows; f16 V and P)
 // so every cached row costs the tensor cores a few cycles and the softmax warps a handful
 // of instructions per tile: the kernel streams K and V at HBM speed instead of spending
 // ~65 SIMT instructions per row on dot products and lane reductions.
@@ -33,16 +33,24 @@
 namespace iha {
 
 constexpr int DT_ROWS = 128;    // cached rows per tile
-constexpr int DT_D = 128;       // head width this kernel serves
-constexpr int DT_N = 16;        // queries per MMA (P <= 4, zero-padded)
-constexpr int DT_PMAX = 4;
+constexpr int DT_N = 16;        // queries per MMA (P <= 8, zero-padded)
 constexpr int DT_STAGES = 3;
 constexpr int DT_THREADS = 192;
-constexpr int DT_KV_BYTES = DT_ROWS * DT_D * 2;          // one K or V tile: 32 KB
-constexpr int DT_STAGE_BYTES = 2 * DT_KV_BYTES;
-constexpr int DT_Q_BYTES = DT_N * DT_D * 2;              // 4 KB
 constexpr int DT_PT_BYTES = DT_N * DT_ROWS * 2;          // one P^T buffer: 4 KB
-constexpr int DT_SMEM = DT_STAGES * DT_STAGE_BYTES + DT_Q_BYTES + 2 * DT_PT_BYTES + 512 + 1024;
+constexpr int DT_CHUNK = DT_ROWS * 128;                  // one 64-column chunk of a tile: 16 KB
+
+// d = 128 (P <= 4) or d = 64 (P <= 8).  The output product always has M = 128 rows, two
+// 64-row d-chunks DT_CHUNK apart in shared memory: for d = 64 a stage is K, V and a block of
+// zeros after V, so that the second chunk reads zeros and the rows past d of O^T are 0.
+template <int DH>
+struct DtCfg {
+    static constexpr int PMAX = DH == 128 ? 4 : 8;
+    static constexpr int KV_BYTES = DT_ROWS * DH * 2;                           // 32 KB or 16 KB
+    static constexpr int STAGE_BYTES = DH == 128 ? 2 * KV_BYTES : 3 * KV_BYTES;   // K, V (, zeros)
+    static constexpr int Q_BYTES = DT_N * DH * 2;
+    static constexpr int SMEM = DT_STAGES * STAGE_BYTES + Q_BYTES + 2 * DT_PT_BYTES + 512 + 1024;
+    static_assert(SMEM <= 232448, "shared memory");
+};
 
 struct DecodeTcParams {
     const __nv_bfloat16 *qt;   // [B][H][P][d]
@@ -60,6 +68,15 @@ __device__ __forceinline__ float dt_ex2(float x) {
     return y;
 }
 
+// The first N columns (N = 4 or 8: the queries a kernel instance serves) of this warp's lane
+// quarter.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+    static_assert(N == 4 || N == 8, "4 or 8 columns");
+    if constexpr (N == 4) tmem_ld4(taddr, r);
+    else tmem_ld8(taddr, r);
+}
+
 // Byte offset of element (row r, column k) in a K-major SW128 tile of 16-bit values whose
 // rows hold 64 elements per 128-byte chunk and whose chunks are `chunk_bytes` apart.
 __device__ __forceinline__ uint32_t sw128_off(int r, int k, int chunk_bytes) {
@@ -67,14 +84,17 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int k, int chunk_bytes) {
     return c * chunk_bytes + (r >> 3) * 1024 + (r & 7) * 128 + ((((kc >> 3) ^ (r & 7))) << 4) + (kc & 7) * 2;
 }
 
+template <int DH>
 __global__ void __launch_bounds__(DT_THREADS, 1)
 decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const DecodeTcParams p) {
+    using C = DtCfg<DH>;
+    constexpr int DT_PMAX = C::PMAX;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sKV = smem;                                       // [stage][K tile | V tile]
-    uint8_t *sQ = sKV + DT_STAGES * DT_STAGE_BYTES;            // B operand of S: [16 q][128 d]
-    uint8_t *sPT = sQ + DT_Q_BYTES;                            // 2 x B operand of O: [16 q][128 rows]
+    uint8_t *sQ = sKV + DT_STAGES * C::STAGE_BYTES;            // B operand of S: [16 q][d]
+    uint8_t *sPT = sQ + C::Q_BYTES;                            // 2 x B operand of O: [16 q][128 rows]
     float *red = reinterpret_cast<float *>(sPT + 2 * DT_PT_BYTES);   // [2][4 warps][DT_PMAX]
     uint64_t *bars = reinterpret_cast<uint64_t *>(red + 2 * 4 * DT_PMAX);
     uint64_t *kv_full = bars;                  // [DT_STAGES]
@@ -95,14 +115,19 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const int P = p.P;
 
     pdl_trigger();
-    // Q (bf16) and zeroed P^T buffers: the rows past P stay zero
-    for (int i = threadIdx.x; i < (DT_Q_BYTES + 2 * DT_PT_BYTES) / 16; i += blockDim.x)
+    // Q (bf16) and zeroed P^T buffers: the rows past P stay zero; for d = 64 the zero block of
+    // every stage (never written by TMA)
+    for (int i = threadIdx.x; i < (C::Q_BYTES + 2 * DT_PT_BYTES) / 16; i += blockDim.x)
         reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0, 0, 0, 0);
+    if (DH == 64)
+        for (int i = threadIdx.x; i < DT_STAGES * (DT_CHUNK / 16); i += blockDim.x)
+            reinterpret_cast<uint4 *>(sKV + (i / (DT_CHUNK / 16)) * C::STAGE_BYTES + 2 * C::KV_BYTES)[i % (DT_CHUNK / 16)] =
+                make_uint4(0, 0, 0, 0);
     pdl_wait();   // the mixing kernel's q~ and appended cache rows
     __syncthreads();
-    for (int i = threadIdx.x; i < P * DT_D; i += blockDim.x) {
-        const int q = i / DT_D, c = i % DT_D;
-        *reinterpret_cast<__nv_bfloat16 *>(sQ + sw128_off(q, c, DT_N * 128)) = p.qt[(bh * P + q) * DT_D + c];
+    for (int i = threadIdx.x; i < P * DH; i += blockDim.x) {
+        const int q = i / DH, c = i % DH;
+        *reinterpret_cast<__nv_bfloat16 *>(sQ + sw128_off(q, c, DT_N * 128)) = p.qt[(bh * P + q) * DH + c];
     }
     fence_proxy_async_smem();   // generic writes of Q and P^T before the tensor core reads them
     if (threadIdx.x == 0) {
@@ -140,11 +165,11 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                                     abort_flag))
                     break;
                 const int row0 = (int)(r_begin + (long long)i * DT_ROWS);
-                uint8_t *dst = sKV + st * DT_STAGE_BYTES;
-                mbar_arrive_expect_tx(&kv_full[st], DT_STAGE_BYTES);
-                for (int c = 0; c < DT_D / 64; ++c) {
-                    tma_load_3d(&tmK, &kv_full[st], dst + c * (DT_ROWS * 128), c * 64, row0, (int)bh);
-                    tma_load_3d(&tmV, &kv_full[st], dst + DT_KV_BYTES + c * (DT_ROWS * 128), c * 64, row0, (int)bh);
+                uint8_t *dst = sKV + st * C::STAGE_BYTES;
+                mbar_arrive_expect_tx(&kv_full[st], 2 * C::KV_BYTES);
+                for (int c = 0; c < DH / 64; ++c) {
+                    tma_load_3d(&tmK, &kv_full[st], dst + c * DT_CHUNK, c * 64, row0, (int)bh);
+                    tma_load_3d(&tmV, &kv_full[st], dst + C::KV_BYTES + c * DT_CHUNK, c * 64, row0, (int)bh);
                 }
                 ++issued;
             }
@@ -156,18 +181,19 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // ------------------------------- MMA issuer ---------------------------------
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(DT_ROWS, DT_N, 0, 0);   // K rows x Q: both K-major
-            constexpr uint32_t idesc_o = idesc_f16_f32(DT_D, DT_N, 1, 0);       // V^T (MN-major) x P^T
+            constexpr uint32_t idesc_o = idesc_f16_f32(128, DT_N, 1, 0);        // V^T (MN-major) x P^T
             const uint32_t q0 = smem_u32(sQ), pt0 = smem_u32(sPT), kv0 = smem_u32(sKV);
             bool ok = true;
             auto issue_pv = [&](int j) -> bool {
                 const int bj = j & 1, st = j % DT_STAGES;
                 if (!mbar_wait(&p_full[bj], (j >> 1) & 1, p.status, kSiteDecodeTcMma, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t v0 = kv0 + st * DT_STAGE_BYTES + DT_KV_BYTES;
+                const uint32_t v0 = kv0 + st * C::STAGE_BYTES + C::KV_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < DT_ROWS / 16; ++kk) {
-                    // A = V^T: 16 cached rows of 128-byte d-chunks 16 KB apart (leading offset)
-                    const uint64_t a = sdesc_sw128(v0 + kk * 2048, DT_ROWS * 128, 1024);
+                    // A = V^T: 16 cached rows of 128-byte d-chunks 16 KB apart (leading offset;
+                    // for d = 64 the second chunk is the zero block)
+                    const uint64_t a = sdesc_sw128(v0 + kk * 2048, DT_CHUNK, 1024);
                     const uint64_t bd = sdesc_sw128(pt0 + bj * DT_PT_BYTES + (kk / 4) * (DT_N * 128) + (kk % 4) * 32, 16,
                                                     1024);
                     mma_ss(tmem + 32 + bj * 16, a, bd, idesc_o, kk > 0 ? 1u : 0u);
@@ -183,10 +209,10 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     break;
                 }
                 tc_fence_after();
-                const uint32_t k0 = kv0 + st * DT_STAGE_BYTES;
+                const uint32_t k0 = kv0 + st * C::STAGE_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < DT_D / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(k0 + (kk / 4) * (DT_ROWS * 128) + (kk % 4) * 32, 16, 1024);
+                for (int kk = 0; kk < DH / 16; ++kk) {
+                    const uint64_t a = sdesc_sw128(k0 + (kk / 4) * DT_CHUNK + (kk % 4) * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(q0 + (kk / 4) * (DT_N * 128) + (kk % 4) * 32, 16, 1024);
                     mma_ss(tmem + bi * 16, a, bd, idesc_s, kk > 0 ? 1u : 0u);
                 }
@@ -215,8 +241,8 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         auto fold = [&](int j, const float (&f)[DT_PMAX]) -> bool {
             if (!mbar_wait(&o_full[j & 1], (j >> 1) & 1, p.status, kSiteDecodeTc, abort_flag)) return false;
             tc_fence_after();
-            uint32_t u[4];
-            tmem_ld4(tmem + lane_addr + 32 + (j & 1) * 16, u);
+            uint32_t u[DT_PMAX];
+            tmem_ld_cols<DT_PMAX>(tmem + lane_addr + 32 + (j & 1) * 16, u);
             tmem_ld_wait();
 #pragma unroll
             for (int q = 0; q < DT_PMAX; ++q) o[q] = fmaf(o[q], f[q], __uint_as_float(u[q]));
@@ -225,10 +251,10 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         for (int i = 0; i < ntiles; ++i) {
             const int bi = i & 1;
             ok = ok && mbar_wait(&s_full[bi], (i >> 1) & 1, p.status, kSiteDecodeTc, abort_flag);
-            uint32_t u[4] = {0u, 0u, 0u, 0u};
+            uint32_t u[DT_PMAX] = {};
             if (ok) {
                 tc_fence_after();
-                tmem_ld4(tmem + lane_addr + bi * 16, u);
+                tmem_ld_cols<DT_PMAX>(tmem + lane_addr + bi * 16, u);
                 tmem_ld_wait();
             }
             const long long row = r_begin + (long long)i * DT_ROWS + i_row;
@@ -294,7 +320,7 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         asm volatile("bar.sync 1, 128;" ::: "memory");
         for (int q = 0; q < P; ++q) {
             const size_t pidx = ((size_t)bh * nch + chunk) * P + q;
-            p.part_o[pidx * DT_D + i_row] = ok ? o[q] : 0.f;
+            if (i_row < DH) p.part_o[pidx * DH + i_row] = ok ? o[q] : 0.f;
             if (i_row == 0) {
                 p.part_ml[pidx * 2] = ok ? m[q] : -INFINITY;
                 p.part_ml[pidx * 2 + 1] =
@@ -311,8 +337,8 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 }
 
 bool decode_tc_supported(int d, int P, const void *Kc, const void *Vc) {
-    return d == DT_D && P <= DT_PMAX && (reinterpret_cast<uintptr_t>(Kc) & 15) == 0 &&
-           (reinterpret_cast<uintptr_t>(Vc) & 15) == 0;
+    return ((d == 128 && P <= DtCfg<128>::PMAX) || (d == 64 && P <= DtCfg<64>::PMAX)) &&
+           (reinterpret_cast<uintptr_t>(Kc) & 15) == 0 && (reinterpret_cast<uintptr_t>(Vc) & 15) == 0;
 }
 
 // Chunks per (b, h): one wave of CTAs (one per SM), whole tiles per chunk.
@@ -327,14 +353,17 @@ int decode_tc_chunks(int B, int H, long long rows, int max_chunks, int &rows_per
     return (int)((rows + rows_per_chunk - 1) / rows_per_chunk);
 }
 
-cudaError_t launch_decode_attn_tc(const void *qt, const void *Kc, const void *Vc, int B, int H, int P,
-                                  long long cache_rows, long long lo, long long hi, int nch, int rows_per_chunk,
-                                  float *part_ml, float *part_o, cudaStream_t st, int *status) {
+template <int DH>
+static cudaError_t launch_decode_attn_tc_d(const void *qt, const void *Kc, const void *Vc, int B, int H, int P,
+                                          long long cache_rows, long long lo, long long hi, int nch,
+                                          int rows_per_chunk, float *part_ml, float *part_o, cudaStream_t st,
+                                          int *status) {
+    using C = DtCfg<DH>;
     const long long BH = (long long)B * H;
     if (cache_rows >= (1LL << 31) || BH >= (1LL << 31)) return cudaErrorInvalidValue;
     CUtensorMap tmK, tmV;
-    const uint64_t dims[3] = {(uint64_t)DT_D, (uint64_t)cache_rows, (uint64_t)BH};
-    const uint64_t strides[2] = {(uint64_t)DT_D * 2, (uint64_t)cache_rows * DT_D * 2};
+    const uint64_t dims[3] = {(uint64_t)DH, (uint64_t)cache_rows, (uint64_t)BH};
+    const uint64_t strides[2] = {(uint64_t)DH * 2, (uint64_t)cache_rows * DH * 2};
     const uint32_t box[3] = {64, DT_ROWS, 1};
     if (!make_tmap_bf16(&tmK, Kc, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (!make_tmap_bf16(&tmV, Vc, 3, dims, strides, box, /*f16=*/true)) return cudaErrorInvalidValue;
@@ -345,24 +374,36 @@ cudaError_t launch_decode_attn_tc(const void *qt, const void *Kc, const void *Vc
     p.lo = lo;
     p.hi = hi;
     p.rows_per_chunk = rows_per_chunk;
-    p.scale_log2 = 1.4426950408889634f / sqrtf((float)DT_D);
+    p.scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
     p.part_ml = part_ml;
     p.part_o = part_o;
     p.status = status;
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, DT_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(decode_attn_tc<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     // programmatic stream serialization: the launch and prologue overlap the mixing kernel
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)nch, H, B);
     cfg.blockDim = dim3(DT_THREADS);
-    cfg.dynamicSmemBytes = DT_SMEM;
+    cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_attn_tc, tmK, tmV, p);
+    return cudaLaunchKernelEx(&cfg, decode_attn_tc<DH>, tmK, tmV, p);
+}
+
+cudaError_t launch_decode_attn_tc(const void *qt, const void *Kc, const void *Vc, int B, int H, int d, int P,
+                                  long long cache_rows, long long lo, long long hi, int nch, int rows_per_chunk,
+                                  float *part_ml, float *part_o, cudaStream_t st, int *status) {
+    if (d == 128)
+        return launch_decode_attn_tc_d<128>(qt, Kc, Vc, B, H, P, cache_rows, lo, hi, nch, rows_per_chunk, part_ml,
+                                            part_o, st, status);
+    if (d == 64)
+        return launch_decode_attn_tc_d<64>(qt, Kc, Vc, B, H, P, cache_rows, lo, hi, nch, rows_per_chunk, part_ml,
+                                           part_o, st, status);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace iha
