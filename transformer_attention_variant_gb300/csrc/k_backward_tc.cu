@@ -373,17 +373,25 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
 #pragma unroll
                 for (int c4 = 0; c4 < BA_BLK / 4; ++c4) {
                     const float4 l = l4[c4];
-                    pv[4 * c4 + 0] = ba_exp2(fmaf(pv[4 * c4 + 0], sl2, -l.x));
-                    pv[4 * c4 + 1] = ba_exp2(fmaf(pv[4 * c4 + 1], sl2, -l.y));
-                    pv[4 * c4 + 2] = ba_exp2(fmaf(pv[4 * c4 + 2], sl2, -l.z));
-                    pv[4 * c4 + 3] = ba_exp2(fmaf(pv[4 * c4 + 3], sl2, -l.w));
+                    float x0, x1, x2, x3;   // exponents by packed fp32x2 FMAs
+                    ffma2(x0, x1, pv[4 * c4 + 0], pv[4 * c4 + 1], sl2, sl2, -l.x, -l.y);
+                    ffma2(x2, x3, pv[4 * c4 + 2], pv[4 * c4 + 3], sl2, sl2, -l.z, -l.w);
+                    pv[4 * c4 + 0] = ba_exp2(x0);
+                    pv[4 * c4 + 1] = ba_exp2(x1);
+                    pv[4 * c4 + 2] = ba_exp2(x2);
+                    pv[4 * c4 + 3] = ba_exp2(x3);
                     pw[2 * c4] = pack_bf16x2(pv[4 * c4], pv[4 * c4 + 1]);
                     pw[2 * c4 + 1] = pack_bf16x2(pv[4 * c4 + 2], pv[4 * c4 + 3]);
                 }
                 tmem_st32(sc, pw);   // P^T over the S columns (dP is in other columns)
             } else {
 #pragma unroll
-                for (int c = 0; c < BA_BLK; ++c) pv[c] = ba_exp2(fmaf(pv[c], sl2, -lse_r));
+                for (int c = 0; c < BA_BLK; c += 2) {
+                    float x0, x1;
+                    ffma2(x0, x1, pv[c], pv[c + 1], sl2, sl2, -lse_r, -lse_r);
+                    pv[c] = ba_exp2(x0);
+                    pv[c + 1] = ba_exp2(x1);
+                }
             }
             if (!mbar_wait(&dp_full[grp], jj & 1, p.status, kSiteBwdSoftmax, abort_flag)) {
                 ok = false;
@@ -401,14 +409,22 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
 #pragma unroll
                     for (int c4 = 0; c4 < BA_BLK / 4; ++c4) {
                         const float4 dd = d4[c4];
-                        dw[2 * c4] = pack_bf16x2(pv[4 * c4] * (dp[4 * c4] - dd.x), pv[4 * c4 + 1] * (dp[4 * c4 + 1] - dd.y));
-                        dw[2 * c4 + 1] =
-                            pack_bf16x2(pv[4 * c4 + 2] * (dp[4 * c4 + 2] - dd.z), pv[4 * c4 + 3] * (dp[4 * c4 + 3] - dd.w));
+                        float t0, t1, t2, t3;   // dp - D, then p (dp - D), by packed fp32x2 operations
+                        fadd2(t0, t1, dp[4 * c4], dp[4 * c4 + 1], -dd.x, -dd.y);
+                        fadd2(t2, t3, dp[4 * c4 + 2], dp[4 * c4 + 3], -dd.z, -dd.w);
+                        ffma2(t0, t1, pv[4 * c4], pv[4 * c4 + 1], t0, t1, 0.f, 0.f);
+                        ffma2(t2, t3, pv[4 * c4 + 2], pv[4 * c4 + 3], t2, t3, 0.f, 0.f);
+                        dw[2 * c4] = pack_bf16x2(t0, t1);
+                        dw[2 * c4 + 1] = pack_bf16x2(t2, t3);
                     }
                 } else {
 #pragma unroll
-                    for (int c2 = 0; c2 < BA_BLK / 2; ++c2)
-                        dw[c2] = pack_bf16x2(pv[2 * c2] * (dp[2 * c2] - D_r), pv[2 * c2 + 1] * (dp[2 * c2 + 1] - D_r));
+                    for (int c2 = 0; c2 < BA_BLK / 2; ++c2) {
+                        float t0, t1;
+                        fadd2(t0, t1, dp[2 * c2], dp[2 * c2 + 1], -D_r, -D_r);
+                        ffma2(t0, t1, pv[2 * c2], pv[2 * c2 + 1], t0, t1, 0.f, 0.f);
+                        dw[c2] = pack_bf16x2(t0, t1);
+                    }
                 }
             }
             tmem_st32(sc + 64, dw);
