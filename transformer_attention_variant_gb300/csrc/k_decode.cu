@@ -10,8 +10,8 @@
 //   3. decode_attn_tc (k_decode_tc.cu): split-KV attention on the tensor cores, a CTA per
 //                      chunk of the readable cached rows of one (b, h); the chunk's (max, sum,
 //                      unnormalised output) of every query go to the workspace.
-//   4. decode_merge:   merge the chunks of every (b, h, j);
-//      decode_contract: the R contraction out[b][h][c] = sum_{h',j} R[h][h'P + j] Pbar[b][h'][j][c].
+//   4. decode_combine: merge the chunks of every (b, h', j) and apply the R contraction
+//                      out[b][h][c] = sum_{h',j} R[h][h'P + j] Pbar[b][h'][j][c] in one pass.
 // The step is HBM-bound: W (3 D^2 bf16) and the cached rows of K and V are the bytes.  The
 // kernels are chained with programmatic dependent launch.
 #include <cuda_bf16.h>
@@ -203,69 +203,96 @@ decode_mix(const float *__restrict__ Yp, const float *__restrict__ aQ, const flo
 }
 
 // ---------------------------------------------------------------------------------------
-// 4a. merge the chunks of one (b, h', j): Pbar[b][h'*P + j][c], one thread per column; the
-//     chunks' partial results are read 16 at a time, all loads of a group in flight
+// 4. chunk merge and R contraction in one pass.  With w = 2^(m_ch - M) over the chunks of one
+//    pseudo-query row k = (h', j) (M the largest chunk max) and L_k = sum_ch w l_ch,
+//      out[b][h][c] = sum_k R[h][k] Pbar_k[c] = sum_{k, ch} (R[h][k] w / L_k) o_{k,ch}[c],
+//    which is linear in the chunks' partial outputs.  A CTA per (b, h, 32 columns): R[h][:]
+//    is an input, so it goes to shared memory before the wait for the attention; then one warp
+//    per row k turns the (max, sum) pairs into those coefficients, each stored beside the index
+//    of its partial-output row, and DCB_THREADS / 32 groups (warps) reduce those rows with
+//    them, DCB_UNROLL loads of a thread in flight at once.
 // ---------------------------------------------------------------------------------------
-constexpr int DM_CHUNK_GROUP = 16;
-__global__ void decode_merge(const float *__restrict__ part_ml, const float *__restrict__ part_o, int H, int d, int P,
-                             int nch, float *__restrict__ pbar) {
+constexpr int DCB_THREADS = 1024, DCB_COLS = 32, DCB_UNROLL = 16, DK_HPMAX = 256;
+constexpr size_t dcb_smem_bytes(int terms) { return ((size_t)2 * terms + DK_HPMAX + DCB_THREADS) * 4; }
+__global__ void __launch_bounds__(DCB_THREADS)
+decode_combine(const float *__restrict__ part_ml, const float *__restrict__ part_o, const float *__restrict__ R,
+               int H, int d, int P, int nch, __nv_bfloat16 *__restrict__ out) {
+    extern __shared__ float cb_sm[];
     pdl_trigger();
-    pdl_wait();   // the attention's partial results
-    const int bh = blockIdx.x, j = blockIdx.y, c = threadIdx.x;
-    const size_t base = (size_t)bh * nch;
-    float mt = -INFINITY, lt = 0.f, ot = 0.f;   // running merge (max, sum, output) in log2 units
-    for (int c0 = 0; c0 < nch; c0 += DM_CHUNK_GROUP) {
-        float m[DM_CHUNK_GROUP], l[DM_CHUNK_GROUP], o[DM_CHUNK_GROUP];
-#pragma unroll
-        for (int u = 0; u < DM_CHUNK_GROUP; ++u) {
-            const bool in = c0 + u < nch;
-            const size_t pidx = (base + c0 + u) * P + j;
-            m[u] = in ? part_ml[pidx * 2] : -INFINITY;
-            l[u] = in ? part_ml[pidx * 2 + 1] : 0.f;
-            o[u] = in ? part_o[pidx * d + c] : 0.f;
-        }
-        float mg = mt;
-#pragma unroll
-        for (int u = 0; u < DM_CHUNK_GROUP; ++u) mg = fmaxf(mg, m[u]);
-        if (mg == -INFINITY) continue;
-        const float f = exp2f(mt - mg);   // mt = -inf -> 0
-        lt *= f;
-        ot *= f;
-#pragma unroll
-        for (int u = 0; u < DM_CHUNK_GROUP; ++u) {
-            const float cw = m[u] == -INFINITY ? 0.f : exp2f(m[u] - mg);
-            lt = fmaf(l[u], cw, lt);
-            ot = fmaf(o[u], cw, ot);
-        }
-        mt = mg;
-    }
-    pbar[((size_t)bh * P + j) * d + c] = lt > 0.f ? ot / lt : 0.f;   // [b][h'][j][c] = [b][h'*P + j][c]
-}
-
-// ---------------------------------------------------------------------------------------
-// 4b. R contraction: out[b][h][c] = sum_k R[h][k] Pbar[b][k][c], one CTA per (b, h); R[h][:]
-//     goes to shared memory, and a thread's H*P loads are issued 64 at a time
-// ---------------------------------------------------------------------------------------
-constexpr int DK_GROUP = 64, DK_HPMAX = 256;
-__global__ void decode_contract(const float *__restrict__ pbar, const float *__restrict__ R, int H, int d, int P,
-                                __nv_bfloat16 *__restrict__ out) {
-    pdl_trigger();
-    const int b = blockIdx.x, h = blockIdx.y, c = threadIdx.x, HP = H * P;
-    __shared__ float rs[DK_HPMAX];
-    for (int i = threadIdx.x; i < HP; i += blockDim.x) rs[i] = R[(size_t)h * HP + i];   // an input: no wait
+    const int b = blockIdx.x, h = blockIdx.y, c0 = blockIdx.z * DCB_COLS;
+    const int HP = H * P, T = HP * nch;
+    float *coef = cb_sm;                                           // [HP][nch]
+    int *row = reinterpret_cast<int *>(cb_sm + T);                 // [HP][nch]: (b, h', ch, j) row of part_o
+    float *rs = cb_sm + 2 * T;                                     // [DK_HPMAX]: R[h][:]
+    float *red = rs + DK_HPMAX;                                    // [DCB_THREADS]
+    for (int k = threadIdx.x; k < HP; k += DCB_THREADS) rs[k] = R[(size_t)h * HP + k];
     __syncthreads();
-    pdl_wait();   // the merged Pbar
-    const float *pb = pbar + (size_t)b * HP * d;
-    float v = 0.f;
-    for (int k0 = 0; k0 < HP; k0 += DK_GROUP) {
-        float xv[DK_GROUP];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();   // the attention's partial results
+    constexpr int RPW = 4;   // rows of a warp whose (max, sum) loads are in flight at once
+    for (int k0 = warp; k0 < HP; k0 += 32 * RPW) {
+        float m[RPW][2], l[RPW][2];
 #pragma unroll
-        for (int u = 0; u < DK_GROUP; ++u) xv[u] = k0 + u < HP ? pb[(size_t)(k0 + u) * d + c] : 0.f;
+        for (int i = 0; i < RPW; ++i) {
+            const int k = k0 + 32 * i, base = (b * H + k / P) * nch * P + k % P;   // + ch * P: (b, h', ch, j)
 #pragma unroll
-        for (int u = 0; u < DK_GROUP; ++u)
-            if (k0 + u < HP) v = fmaf(rs[k0 + u], xv[u], v);
+            for (int u = 0; u < 2; ++u) {
+                const int ch = lane + 32 * u;   // nch <= 64
+                const bool in = k < HP && ch < nch;
+                m[i][u] = in ? part_ml[(size_t)(base + ch * P) * 2] : -INFINITY;
+                l[i][u] = in ? part_ml[(size_t)(base + ch * P) * 2 + 1] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            const int k = k0 + 32 * i;
+            if (k >= HP) break;   // warp-uniform
+            const int base = (b * H + k / P) * nch * P + k % P;
+            float mg = fmaxf(m[i][0], m[i][1]);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
+            float w[2], L = 0.f;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                w[u] = m[i][u] == -INFINITY ? 0.f : exp2f(m[i][u] - mg);   // an empty chunk weighs nothing
+                L = fmaf(l[i][u], w[u], L);
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+            const float r = L > 0.f ? rs[k] / L : 0.f;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int ch = lane + 32 * u;
+                if (ch < nch) {
+                    coef[k * nch + ch] = w[u] * r;
+                    row[k * nch + ch] = base + ch * P;
+                }
+            }
+        }
     }
-    out[((size_t)b * H + h) * d + c] = __float2bfloat16_rn(v);
+    __syncthreads();
+    constexpr int G = DCB_THREADS / DCB_COLS;
+    const int g = threadIdx.x / DCB_COLS, c = c0 + threadIdx.x % DCB_COLS;   // c0 + 32 <= d
+    float acc = 0.f;
+    for (int t0 = g; t0 < T; t0 += G * DCB_UNROLL) {
+        float xv[DCB_UNROLL];
+#pragma unroll
+        for (int u = 0; u < DCB_UNROLL; ++u) {
+            const int t = t0 + u * G;
+            xv[u] = t < T ? part_o[(size_t)row[t] * d + c] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < DCB_UNROLL; ++u)
+            if (t0 + u * G < T) acc = fmaf(coef[t0 + u * G], xv[u], acc);
+    }
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    if (threadIdx.x < DCB_COLS) {
+        float v = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) v += red[gg * DCB_COLS + threadIdx.x];
+        out[((size_t)b * H + h) * d + c0 + threadIdx.x] = __float2bfloat16_rn(v);
+    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -304,8 +331,7 @@ size_t decode_workspace_bytes(int B, int H, int d, int P) {
     auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
     const size_t D = (size_t)H * d;
     return al((size_t)DC_KS * B * 3 * D * 4) + al((size_t)B * H * P * d * 2) +
-           al((size_t)B * H * DC_NCH_MAX * P * 2 * 4) + al((size_t)B * H * DC_NCH_MAX * P * d * 4) +
-           al((size_t)B * H * P * d * 4);
+           al((size_t)B * H * DC_NCH_MAX * P * 2 * 4) + al((size_t)B * H * DC_NCH_MAX * P * d * 4);
 }
 
 cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const void *WV, const float *aQ,
@@ -322,8 +348,6 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
     float *part_ml = reinterpret_cast<float *>(w);
     w += al((size_t)B * H * DC_NCH_MAX * P * 2 * 4);
     float *part_o = reinterpret_cast<float *>(w);
-    w += al((size_t)B * H * DC_NCH_MAX * P * d * 4);
-    float *pbar = reinterpret_cast<float *>(w);
     const long long cache_rows = cache_tokens * P;
 
     // 1. projections
@@ -365,12 +389,13 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
     const int nch = decode_tc_chunks(B, H, rows, DC_NCH_MAX, rpc);
     e = launch_decode_attn_tc(qt, Kc, Vc, B, H, d, P, cache_rows, lo, hi, nch, rpc, part_ml, part_o, st, status);
     if (e != cudaSuccess) return e;
-    // 4. merge the chunks, then the contraction
-    e = launch_pdl(decode_merge, dim3(B * H, P), dim3(d), 0, st, (const float *)part_ml, (const float *)part_o, H, d,
-                   P, nch, pbar);
+    // 4. merge the chunks and contract with R
+    if (d % DCB_COLS != 0 || (long long)B * H * nch * P >= (1LL << 31)) return cudaErrorInvalidValue;
+    const size_t smem4 = dcb_smem_bytes(H * P * nch);
+    e = cudaFuncSetAttribute(decode_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem4);
     if (e != cudaSuccess) return e;
-    return launch_pdl(decode_contract, dim3(B, H), dim3(d), 0, st, (const float *)pbar, R, H, d, P,
-                      (__nv_bfloat16 *)out);
+    return launch_pdl(decode_combine, dim3(B, H, d / DCB_COLS), dim3(DCB_THREADS), smem4, st,
+                      (const float *)part_ml, (const float *)part_o, R, H, d, P, nch, (__nv_bfloat16 *)out);
 }
 
 }  // namespace iha
