@@ -460,6 +460,37 @@ def test_decode_from_empty_cache(iha, d, P):
     assert_parity(w, o.double().cpu().numpy(), oracle_rows(w, inp))
 
 
+@pytest.mark.parametrize("d,P,fill", [(128, 4, "nan"), (64, 2, "inf"), (128, 2, "nan")])
+def test_decode_ignores_unwritten_cache_rows(iha, d, P, fill):
+    """Cache rows past the current token may hold any bits (a cache allocated without
+    initialisation): NaN or Inf there, read by the last tile of a chunk and masked out,
+    must not reach the output."""
+    B, H, T, steps = 2, 2, 300, 2
+    n_all = T + steps
+    w = gi.Workload("decode_fill", B=B, N=n_all, H=H, d=d, P=P, mask_mode=C, window=0, dtype="bf16", seed=81)
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    wts = [dinp[k] for k in ("W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")]
+    cap = n_all + 40
+    Kc = torch.full((B, H, cap * P, d), float(fill), dtype=torch.bfloat16, device="cuda:0")
+    Vc = torch.full((B, H, cap * P, d), float(fill), dtype=torch.float16, device="cuda:0")
+    X = dinp["X"]
+    out_prompt = torch.empty(B, T, w.D, dtype=torch.bfloat16, device="cuda:0")
+    iha.check(iha.iha_prefill(X[:, :T].contiguous(), *wts, B, T, H, d, P, C, 0, out_prompt, Kc, Vc, cap,
+                              iha.IHA_DTYPE_BF16), "iha_prefill")
+    dec = []
+    for s in range(steps):
+        o = torch.empty(B, w.D, dtype=torch.bfloat16, device="cuda:0")
+        iha.check(iha.iha_decode_step(X[:, T + s].contiguous(), *wts, B, H, d, P, C, 0, Kc, Vc, cap, T + s, o,
+                                      iha.IHA_DTYPE_BF16), "iha_decode_step")
+        dec.append(o)
+    torch.cuda.synchronize()
+    got = torch.stack(dec, 1).reshape(B * steps, w.D).double().cpu().numpy()
+    assert np.isfinite(got).all()
+    rows = [b * n_all + t for b in range(B) for t in range(T, n_all)]
+    assert_parity(w, got, oracle_rows(w, inp, rows=rows))
+
+
 # ---------------------------------------------------------------------------
 # backward pass: every gradient against the fp64 autograd oracle (oracle/backward.py)
 # ---------------------------------------------------------------------------

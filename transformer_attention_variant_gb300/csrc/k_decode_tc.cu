@@ -1,7 +1,7 @@
 // k_decode_tc.cu -- the attention of one decoding step on the tcgen05 tensor cores (d = 128
 // with P <= 4, d = 64 with P <= 8): the P pseudo-queries of the new token t against the cached pseudo-keys and
-// pseudo-values it may read ("Interleaved Head Attention" section 4, Algorithm 1, step
-// "注意力計算" for the rows of token t; the mask is by original position, so every
+// pseudo-values it may read ("Interleaved Head Attention" section 4, Algorithm 1, the
+// attention step for the rows of token t; the mask is by original position, so every
 // pseudo-query of t reads the same cached rows [lo, hi]).
 //
 // A CTA takes a chunk of the readable rows of one (b, h) and walks it in tiles of 128 rows:
@@ -20,8 +20,15 @@
 // double-buffered shared-memory B operand.  Each tile's O^T goes to its own TMEM columns
 // (two buffers), and thread i folds it into its register copy of output column i,
 // o_q = o_q * 2^(m_q(prev) - m_q) + O^T_tile[i][q], one tile behind the MMA -- no rescaling
-// of TMEM.  The chunk's (m, l, o) go to the workspace in the layout of the SIMT kernel, and
-// the same merge kernel combines the chunks.
+// of TMEM.  The chunk's (m, l, o) go to the workspace, and decode_combine (k_decode.cu)
+// merges the chunks.
+//
+// Rows of a tile past the chunk's end are masked out of the softmax (p = 0), and their V rows
+// in shared memory are cleared before the output product: a cache row that has not been
+// written yet may hold any bits, and 0 * NaN would reach the output.  Everything up to the
+// first K/V loads runs before the wait for the mixing kernel (dependent launch); a tile is
+// loaded before that wait only if every row the chunk reads from it predates token t, since
+// the mixing kernel writes token t's rows while this kernel may already be running.
 // TMEM: S buffers at columns 0 and 16, O^T buffers at 32 and 48 (64 columns).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -123,13 +130,6 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         for (int i = threadIdx.x; i < DT_STAGES * (DT_CHUNK / 16); i += blockDim.x)
             reinterpret_cast<uint4 *>(sKV + (i / (DT_CHUNK / 16)) * C::STAGE_BYTES + 2 * C::KV_BYTES)[i % (DT_CHUNK / 16)] =
                 make_uint4(0, 0, 0, 0);
-    pdl_wait();   // the mixing kernel's q~ and appended cache rows
-    __syncthreads();
-    for (int i = threadIdx.x; i < P * DH; i += blockDim.x) {
-        const int q = i / DH, c = i % DH;
-        *reinterpret_cast<__nv_bfloat16 *>(sQ + sw128_off(q, c, DT_N * 128)) = p.qt[(bh * P + q) * DH + c];
-    }
-    fence_proxy_async_smem();   // generic writes of Q and P^T before the tensor core reads them
     if (threadIdx.x == 0) {
         for (int s = 0; s < DT_STAGES; ++s) {
             mbar_init(&kv_full[s], 1);
@@ -153,24 +153,46 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // one stage of the K/V ring: tile i of the chunk (a fresh stage needs no empty wait)
+    auto load_tile = [&](int i) {
+        const int st = i % DT_STAGES;
+        const int row0 = (int)(r_begin + (long long)i * DT_ROWS);
+        uint8_t *dst = sKV + st * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * C::KV_BYTES);
+        for (int c = 0; c < DH / 64; ++c) {
+            tma_load_3d(&tmK, &kv_full[st], dst + c * DT_CHUNK, c * 64, row0, (int)bh);
+            tma_load_3d(&tmV, &kv_full[st], dst + C::KV_BYTES + c * DT_CHUNK, c * 64, row0, (int)bh);
+        }
+    };
+    // tiles whose readable rows all predate token t (rows hi-P+1 .. hi are token t's) go out
+    // before the wait for the mixing kernel
+    int early = 0;
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        const long long first_new = p.hi - P + 1;
+        while (early < DT_STAGES && early < ntiles &&
+               min(r_begin + (long long)(early + 1) * DT_ROWS, r_end) <= first_new)
+            load_tile(early++);
+    }
+    pdl_wait();   // the mixing kernel's q~ and appended cache rows
+    for (int i = threadIdx.x; i < P * DH; i += blockDim.x) {
+        const int q = i / DH, c = i % DH;
+        *reinterpret_cast<__nv_bfloat16 *>(sQ + sw128_off(q, c, DT_N * 128)) = p.qt[(bh * P + q) * DH + c];
+    }
+    fence_proxy_async_smem();   // generic writes of Q, P^T and the zero blocks before the tensor core reads them
+    __syncthreads();
+
     if (warp == 4) {
         // ------------------------------- TMA producer -------------------------------
         if (lane == 0) {
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            int issued = 0;
-            for (int i = 0; i < ntiles; ++i) {
+            int issued = early;
+            for (int i = early; i < ntiles; ++i) {
                 const int st = i % DT_STAGES;
                 if (!mbar_wait_lazy(&kv_empty[st], ((i / DT_STAGES) & 1) ^ 1, p.status, kSiteDecodeTcProducer,
                                     abort_flag))
                     break;
-                const int row0 = (int)(r_begin + (long long)i * DT_ROWS);
-                uint8_t *dst = sKV + st * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(&kv_full[st], 2 * C::KV_BYTES);
-                for (int c = 0; c < DH / 64; ++c) {
-                    tma_load_3d(&tmK, &kv_full[st], dst + c * DT_CHUNK, c * 64, row0, (int)bh);
-                    tma_load_3d(&tmV, &kv_full[st], dst + C::KV_BYTES + c * DT_CHUNK, c * 64, row0, (int)bh);
-                }
+                load_tile(i);
                 ++issued;
             }
             for (int k = issued - DT_STAGES > 0 ? issued - DT_STAGES : 0; k < issued; ++k)
@@ -292,7 +314,14 @@ decode_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     *reinterpret_cast<__half *>(sPT + bi * DT_PT_BYTES + sw128_off(q, i_row, DT_N * 128)) =
                         __float2half_rn(pq);
             }
-            fence_proxy_async_smem();   // P^T writes before the tensor core reads them
+            if (!valid) {   // this row's V: cleared, so that p = 0 meets zeros, whatever the cache held
+                uint4 *vrow = reinterpret_cast<uint4 *>(sKV + (i % DT_STAGES) * C::STAGE_BYTES + C::KV_BYTES + i_row * 128);
+#pragma unroll
+                for (int c = 0; c < DH / 64; ++c)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) vrow[c * (DT_CHUNK / 16) + e] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();   // P^T and cleared V rows before the tensor core reads them
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[bi]);
