@@ -252,7 +252,8 @@ IHA_API int iha_forward_stack(const void *X, int num_layers,
  *   K_cache [B][H][cache_tokens*P][d] bfloat16, V_cache same shape float16: stacked row
  *     t*P + j holds pseudo-key/value j of token t (the layout of Kbar/Vbar in iha_project);
  *     both 16-byte aligned for iha_decode_step, as are W_Q, W_K, W_V (IHA_ERR_INVALID_ARG
- *     otherwise).
+ *     otherwise).  Rows of tokens not yet appended may hold any bits (the caches need no
+ *     initialisation): they never reach an output.
  *
  * iha_prefill: iha_forward_ex over X [B][N][H*d] (the prompt) that also writes the prompt's
  *   pseudo-keys/values into rows 0 .. N*P-1 of the caches (cache_tokens >= N). */
