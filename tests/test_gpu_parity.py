@@ -378,6 +378,8 @@ def test_layer_stack(iha, P_local, N):
     # long caches: many 128-row tiles per chunk, several chunks, a ragged last tile, and (window)
     # a first readable row that is not tile-aligned
     (2, 128, 4, C, 0, 700), (3, 128, 2, WN, 333, 900),
+    # more than 32 chunks per head (36 one-tile chunks: the chunk merge's second lane half)
+    (2, 64, 4, C, 0, 1150),
     # window 1: each decoded token reads only its own P pseudo-keys
     (2, 128, 4, WN, 1, 37), (4, 64, 2, WN, 1, 37)])
 def test_decode_matches_oracle(iha, H, d, P, mode, window, T):
