@@ -267,7 +267,9 @@ def test_caller_workspace_and_default_stream_entry(iha):
     dinp = to_dev(gi.make_inputs(w))
     ref = run_gpu(iha, w, dinp=dinp)
     nbytes = iha.iha_workspace_bytes(w.B, w.N, w.H, w.d, w.P, iha.IHA_DTYPE_BF16)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
+    # every byte NaN (bf16, f16 and fp32 alike): a read of workspace the call did not write
+    # first would reach the output
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda:0")
     out = iha.forward(dinp, H=w.H, d=w.d, P=w.P, mask_mode=w.mask_mode, window=w.window, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
@@ -292,7 +294,7 @@ def test_forward_host_buffers(iha, B, N, H, d, P, mode, window):
     out = torch.empty(w.B, w.N, w.D, dtype=torch.bfloat16).pin_memory()
     s = torch.cuda.Stream()
     nbytes = iha.iha_host_buffer_bytes(w.B, w.N, w.H, w.d, w.P, iha.IHA_DTYPE_BF16)
-    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
+    buf = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda:0")   # NaN bytes: nothing read unwritten
     for dev_buf in (None, buf):
         out.zero_()
         rc = iha.iha_forward_host(hin["X"], hin["W_Q"], hin["W_K"], hin["W_V"], hin["alpha_Q"], hin["alpha_K"],
@@ -524,7 +526,8 @@ def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
     D = w.D
     g = torch.Generator().manual_seed(1234 + N)
     dO = torch.randn(B, N, D, generator=g).to(torch.bfloat16)
-    dev = lambda shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device="cuda:0")
+    # NaN-filled outputs: an element the call leaves unwritten fails the finiteness check
+    dev = lambda shape, dt=torch.bfloat16: torch.full(shape, float("nan"), dtype=dt, device="cuda:0")
     out = {"X": dev((B, N, D)), "W_Q": dev((D, D)), "W_K": dev((D, D)), "W_V": dev((D, D)),
            "alpha_Q": dev((H, H, P), torch.float32), "alpha_K": dev((H, H, P), torch.float32),
            "alpha_V": dev((H, H, P), torch.float32), "R": dev((H, H * P), torch.float32)}
@@ -558,17 +561,18 @@ def test_training_pair_matches_recompute(iha, B, N, H, d, P, mode, window):
     g = torch.Generator().manual_seed(99 + N)
     dO = torch.randn(B, N, D, generator=g).to(torch.bfloat16).to("cuda:0").contiguous()
     nb = iha.iha_backward_workspace_bytes(B, N, H, d, P, iha.IHA_DTYPE_BF16)
-    ws = torch.empty(nb, dtype=torch.uint8, device="cuda:0")
-    out = torch.empty(B, N, D, dtype=torch.bfloat16, device="cuda:0")
+    ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda:0")   # NaN bytes: nothing read unwritten
+    out = torch.full((B, N, D), float("nan"), dtype=torch.bfloat16, device="cuda:0")
     args = [dinp[k] for k in bwd.PARAMS] + [B, N, H, d, P, mode, window]
     iha.check(iha.iha_forward_train(*args, out, iha.IHA_DTYPE_BF16, None, ws, nb), "iha_forward_train")
 
-    def grads():
-        return {"X": torch.empty(B, N, D, dtype=torch.bfloat16, device="cuda:0"),
-                **{k: torch.empty(D, D, dtype=torch.bfloat16, device="cuda:0") for k in ("W_Q", "W_K", "W_V")},
-                **{k: torch.empty(H, H, P, dtype=torch.float32, device="cuda:0")
+    def grads():   # NaN-filled: an element the calls leave unwritten fails the equality below
+        nan = float("nan")
+        return {"X": torch.full((B, N, D), nan, dtype=torch.bfloat16, device="cuda:0"),
+                **{k: torch.full((D, D), nan, dtype=torch.bfloat16, device="cuda:0") for k in ("W_Q", "W_K", "W_V")},
+                **{k: torch.full((H, H, P), nan, dtype=torch.float32, device="cuda:0")
                    for k in ("alpha_Q", "alpha_K", "alpha_V")},
-                "R": torch.empty(H, H * P, dtype=torch.float32, device="cuda:0")}
+                "R": torch.full((H, H * P), nan, dtype=torch.float32, device="cuda:0")}
     g_saved, g_full = grads(), grads()
     iha.check(iha.iha_backward_saved(*args, dO, *(g_saved[k] for k in bwd.PARAMS), iha.IHA_DTYPE_BF16, None, ws,
                                      nb), "iha_backward_saved")
