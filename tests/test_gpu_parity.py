@@ -468,7 +468,7 @@ def test_decode_from_empty_cache(iha, d, P):
 def test_decode_ignores_unwritten_cache_rows(iha, d, P, fill):
     """Cache rows past the current token may hold any bits (a cache allocated without
     initialisation): NaN or Inf there, read by the last tile of a chunk and masked out,
-    must not reach the output."""
+    must not reach the output; nor may NaN bytes in a caller-provided workspace."""
     B, H, T, steps = 2, 2, 300, 2
     n_all = T + steps
     w = gi.Workload("decode_fill", B=B, N=n_all, H=H, d=d, P=P, mask_mode=C, window=0, dtype="bf16", seed=81)
@@ -482,11 +482,14 @@ def test_decode_ignores_unwritten_cache_rows(iha, d, P, fill):
     out_prompt = torch.empty(B, T, w.D, dtype=torch.bfloat16, device="cuda:0")
     iha.check(iha.iha_prefill(X[:, :T].contiguous(), *wts, B, T, H, d, P, C, 0, out_prompt, Kc, Vc, cap,
                               iha.IHA_DTYPE_BF16), "iha_prefill")
+    # the caller's workspace starts as NaN bytes too: nothing in it may be read before it is written
+    nws = iha.iha_decode_workspace_bytes(B, H, d, P)
+    ws = torch.full((nws,), 0xFF, dtype=torch.uint8, device="cuda:0")
     dec = []
     for s in range(steps):
-        o = torch.empty(B, w.D, dtype=torch.bfloat16, device="cuda:0")
+        o = torch.full((B, w.D), float("nan"), dtype=torch.bfloat16, device="cuda:0")
         iha.check(iha.iha_decode_step(X[:, T + s].contiguous(), *wts, B, H, d, P, C, 0, Kc, Vc, cap, T + s, o,
-                                      iha.IHA_DTYPE_BF16), "iha_decode_step")
+                                      iha.IHA_DTYPE_BF16, None, ws, nws), "iha_decode_step")
         dec.append(o)
     torch.cuda.synchronize()
     got = torch.stack(dec, 1).reshape(B * steps, w.D).double().cpu().numpy()
