@@ -489,7 +489,9 @@ def run_stack(args, w):
                                    "window": L["window"] or None} for L in layers],
                        "l2": "flushed between steps (256 MiB write outside the timed events)"},
             "tflops_algorithmic": flops / (ms * 1e-3) / 1e12,
-            "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / peaks["bf16"],
+            "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": peaks["bf16"],
+                         "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / peaks["bf16"], "traffic": None,
+                         "note": "whole stack: the layers' algorithmic flops over the stack's time"},
             "gpu_launches": 4 * len(layers) * args.steps, "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
