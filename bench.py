@@ -253,6 +253,115 @@ def config_of(w, l2):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+class ForwardStep:
+    """One forward step of workload w through the library's step entry points, on one
+    stream: the route's steps 1+2 (project heads then mix, or fold then project), the
+    attention, the contraction; each kernel bracketed by CUDA events on that stream."""
+
+    def __init__(self, iha, w, host, dev, stream):
+        self.iha, self.w, self.dev, self.stream = iha, w, dev, stream
+        self.dt = iha.IHA_DTYPE_BF16 if w.dtype == "bf16" else iha.IHA_DTYPE_F32
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.d = {k: v.to(dev).contiguous() for k, v in host.items()}
+        self.route = iha.iha_projection_route(w.H, w.d, w.P, self.dt)
+        if self.route == 1:
+            self.Wt = torch.empty(w.B * w.N, 3 * w.D, dtype=tdt, device=dev)        # head projections Y
+        else:
+            self.Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=tdt, device=dev)  # folded weights
+        self.QKV = torch.empty(3, w.B, w.H, w.N * w.P, w.d, dtype=tdt, device=dev)
+        self.Pbar = torch.empty(w.B, w.N, w.H, w.P, w.d, dtype=tdt, device=dev)
+        self.out = torch.empty(w.B, w.N, w.D, dtype=tdt, device=dev)
+        self.names = (["project_heads", "mix", "attention", "contract"] if self.route == 1
+                      else ["fold", "project", "attention", "contract"])
+
+    def launches(self):
+        iha, w, d, dt, s = self.iha, self.w, self.d, self.dt, self.stream
+        if self.route == 1:
+            yield lambda: iha.check(iha.iha_project_heads(d["X"], d["W_Q"], d["W_K"], d["W_V"], w.B, w.N, w.H, w.d,
+                                                          dt, self.Wt, s), "project_heads")
+            yield lambda: iha.check(iha.iha_mix_heads(self.Wt, d["alpha_Q"], d["alpha_K"], d["alpha_V"], w.B, w.N,
+                                                      w.H, w.d, w.P, dt, self.QKV, s), "mix")
+        else:
+            yield lambda: iha.check(iha.iha_fold_weights(d["W_Q"], d["W_K"], d["W_V"], d["alpha_Q"], d["alpha_K"],
+                                                         d["alpha_V"], w.H, w.d, w.P, dt, self.Wt, s), "fold")
+            yield lambda: iha.check(iha.iha_project(d["X"], self.Wt, w.B, w.N, w.H, w.d, w.P, dt, self.QKV, s),
+                                    "project")
+        yield lambda: iha.check(iha.iha_attention(self.QKV, w.B, w.N, w.H, w.d, w.P, w.mask_mode, w.window, dt,
+                                                  self.Pbar, s), "attention")
+        yield lambda: iha.check(iha.iha_contract(self.Pbar, d["R"], w.B, w.N, w.H, w.d, w.P, dt, self.out, s),
+                                "contract")
+
+    def run(self, ev=None):
+        for j, launch in enumerate(self.launches()):
+            if ev is not None:
+                ev[j].record(self.stream)
+            launch()
+        if ev is not None:
+            ev[len(self.names)].record(self.stream)
+
+    def time(self, steps, warmup, flush, dist=None, clocks=None):
+        """Warm-up, then `steps` timed steps with L2 flushed between them (outside the events).
+        Returns (mean step ms, {kernel: mean ms}, wall seconds of the timed region)."""
+        iha, stream, dev = self.iha, self.stream, self.dev
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                flush.fill_(1)
+                self.run()
+        torch.cuda.synchronize(dev)
+        rc, code = iha.iha_check_device_status(stream)
+        iha.check(rc, f"device status after warm-up ({code:#x})")
+        n = len(self.names)
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        with (clocks if clocks is not None else _NoClock()):
+            t_wall0 = time.perf_counter()
+            with torch.cuda.stream(stream):
+                for i in range(steps):
+                    flush.fill_(i & 0xFF)          # evict L2 between steps (outside the events)
+                    self.run(events[i])
+            torch.cuda.synchronize(dev)
+            t_wall = time.perf_counter() - t_wall0
+        barrier(dist)
+        rc, code = iha.iha_check_device_status(stream)
+        iha.check(rc, f"device status after timed steps ({code:#x})")
+        k_ms = {nm: sum(ev[j].elapsed_time(ev[j + 1]) for ev in events) / steps for j, nm in enumerate(self.names)}
+        step_ms = sum(ev[0].elapsed_time(ev[n]) for ev in events) / steps
+        return step_ms, k_ms, t_wall
+
+
+class _NoClock:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+# the other workloads of the target, timed in the same run (ms per step, kernel times and
+# the attention kernel's fraction of peak), beside the headline workload's line
+SIDE_WORKLOADS = ["bf16_causal_n1024", "bf16_window1024_n4096", "bf16_window4096_n16384"]
+
+
+def side_workloads(iha, args, dev, stream, flush, peaks, skip):
+    res = {}
+    for name in SIDE_WORKLOADS:
+        if name == skip:
+            continue
+        w = gi.WORKLOADS[name]
+        fs = ForwardStep(iha, w, gi.make_inputs(w), dev, stream)
+        ms, k_ms, _ = fs.time(args.steps, args.warmup, flush)
+        wk = work(w)
+        tf = wk["attn"] / (k_ms["attention"] * 1e-3) / 1e12
+        res[name] = {"value": wk["pseudo_tokens"] / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "kernel_ms": k_ms,
+                     "attention_tflops_exact_pairs": tf, "attention_frac": tf / peaks["bf16"],
+                     "forward_tflops_algorithmic": wk["algorithmic"] / (ms * 1e-3) / 1e12,
+                     "steps": args.steps, "config": config_of(w, "flushed between steps")}
+        del fs
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args, w):
     rank, world, local, dist = dist_setup(args.gpus)
     import transformer_attention_variant_gb300 as iha
@@ -262,82 +371,15 @@ def run_gpu(args, w):
     wk = work(w)
     dt = iha.IHA_DTYPE_BF16 if w.dtype == "bf16" else iha.IHA_DTYPE_F32
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-    es = 2 if w.dtype == "bf16" else 4
 
     host = gi.make_inputs(w)
-    d = {k: v.to(dev).contiguous() for k, v in host.items()}
-    # steps 1+2 take the same route as iha_forward_ex: fold + project, or project heads + mix
-    route = iha.iha_projection_route(w.H, w.d, w.P, dt)
-    if route == 1:
-        Wt = torch.empty(w.B * w.N, 3 * w.D, dtype=tdt, device=dev)        # head projections Y
-    else:
-        Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=tdt, device=dev)  # folded weights
-    QKV = torch.empty(3, w.B, w.H, w.N * w.P, w.d, dtype=tdt, device=dev)
-    Pbar = torch.empty(w.B, w.N, w.H, w.P, w.d, dtype=tdt, device=dev)
-    out = torch.empty(w.B, w.N, w.D, dtype=tdt, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
-
-    def step(ev=None):
-        s = stream
-        if ev is not None:
-            ev[0].record(s)
-        if route == 1:
-            iha.check(iha.iha_project_heads(d["X"], d["W_Q"], d["W_K"], d["W_V"], w.B, w.N, w.H, w.d, dt, Wt, s),
-                      "project_heads")
-        else:
-            iha.check(iha.iha_fold_weights(d["W_Q"], d["W_K"], d["W_V"], d["alpha_Q"], d["alpha_K"], d["alpha_V"],
-                                           w.H, w.d, w.P, dt, Wt, s), "fold")
-        if ev is not None:
-            ev[1].record(s)
-        if route == 1:
-            iha.check(iha.iha_mix_heads(Wt, d["alpha_Q"], d["alpha_K"], d["alpha_V"], w.B, w.N, w.H, w.d, w.P, dt,
-                                        QKV, s), "mix")
-        else:
-            iha.check(iha.iha_project(d["X"], Wt, w.B, w.N, w.H, w.d, w.P, dt, QKV, s), "project")
-        if ev is not None:
-            ev[2].record(s)
-        iha.check(iha.iha_attention(QKV, w.B, w.N, w.H, w.d, w.P, w.mask_mode, w.window, dt, Pbar, s), "attention")
-        if ev is not None:
-            ev[3].record(s)
-        iha.check(iha.iha_contract(Pbar, d["R"], w.B, w.N, w.H, w.d, w.P, dt, out, s), "contract")
-        if ev is not None:
-            ev[4].record(s)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            flush.fill_(1)
-            step()
-    torch.cuda.synchronize(dev)
-    rc, code = iha.iha_check_device_status(stream)
-    iha.check(rc, f"device status after warm-up ({code:#x})")
-
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    barrier(dist)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        t_wall0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                flush.fill_(i & 0xFF)          # evict L2 between steps (outside the events)
-                step(events[i])
-        torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall0
-    barrier(dist)
-    rc, code = iha.iha_check_device_status(stream)
-    iha.check(rc, f"device status after timed steps ({code:#x})")
-
-    names = ["project_heads", "mix", "attention", "contract"] if route == 1 else ["fold", "project", "attention",
-                                                                                 "contract"]
-    k_ms = {n: [] for n in names}
-    step_ms = []
-    for ev in events:
-        for j, n in enumerate(names):
-            k_ms[n].append(ev[j].elapsed_time(ev[j + 1]))
-        step_ms.append(ev[0].elapsed_time(ev[4]))
-    mean_step = sum(step_ms) / len(step_ms)
+    fs = ForwardStep(iha, w, host, dev, stream)
+    route, names = fs.route, fs.names
+    clk = ClockSampler(local)
+    mean_step, kmean, t_wall = fs.time(args.steps, args.warmup, flush, dist=dist, clocks=clk)
     mean_step = max_over_ranks(mean_step, dist, dev)
-    kmean = {n: sum(v) / len(v) for n, v in k_ms.items()}
     value = job_value(world, wk["pseudo_tokens"], mean_step)
 
     # roofline of the dominant kernel
@@ -380,7 +422,7 @@ def run_gpu(args, w):
         "kernel_ms": kmean,
         "projection_route": "project heads + mix" if route == 1 else "fold alpha into W + project",
         "roofline": roof,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": len(names) * args.steps,
         "wall_s_timed_region": t_wall,
         "clocks": clk.summary(),
     }
@@ -390,7 +432,8 @@ def run_gpu(args, w):
         hin = {k: v.contiguous().pin_memory() for k, v in host.items()}
         hout = torch.empty(w.B, w.N, w.D, dtype=tdt).pin_memory()
         nbytes = iha.iha_host_buffer_bytes(w.B, w.N, w.H, w.d, w.P, dt)
-        del QKV, Pbar, Wt
+        del fs
+        torch.cuda.empty_cache()
         dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         h2d = sum(v.numel() * v.element_size() for v in hin.values())
         d2h = hout.numel() * hout.element_size()
@@ -415,6 +458,12 @@ def run_gpu(args, w):
         line["e2e"] = {"value": job_value(world, wk["pseudo_tokens"], e2e_s * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3, "steps": n_e2e,
                        "call": "iha_forward_host (pinned host buffers, preallocated device buffer)"}
+
+    if args.side_workloads and world == 1 and args.workload == DEFAULT_WORKLOAD and args.N is None:
+        if not args.no_e2e:
+            del dbuf
+            torch.cuda.empty_cache()
+        line["workloads"] = side_workloads(iha, args, dev, stream, flush, peaks, skip=w.name)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -748,6 +797,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=48, help="oracle sample size per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
+    ap.add_argument("--no-side-workloads", dest="side_workloads", action="store_false",
+                    help="do not time the other target workloads (the 'workloads' object of the line)")
     ap.add_argument("--stack", action="store_true",
                     help="time the four-local + one-global layer stack on the workload's shape instead")
     ap.add_argument("--decode", action="store_true",

@@ -37,6 +37,11 @@
  *     Argument errors are detected on the host before anything is launched.
  *     A device-side bounded wait that expires (IHA_ERR_TIMEOUT) is recorded in a
  *     per-device status word and reported by iha_check_device_status().
+ *   - The library looks up the device addresses of its per-device state (the
+ *     status word, the attention work-counter ring, the array behind
+ *     iha_forward_noalloc) on first use on each device and keeps them for the
+ *     life of the process.  cudaDeviceReset() invalidates them: no call may
+ *     follow a device reset in the same process.
  */
 #ifndef IHA_H
 #define IHA_H
@@ -60,6 +65,9 @@ extern "C" {
 #define IHA_ERR_WORKSPACE 3     /* caller workspace smaller than iha_workspace_bytes() */
 #define IHA_ERR_CUDA 4          /* a CUDA call or launch failed */
 #define IHA_ERR_TIMEOUT 5       /* a device-side bounded wait expired */
+#define IHA_ERR_BUILD 6         /* the library's kernels do not match this device, or a
+                                   warp-specialised kernel was compiled to another register
+                                   count than its register split needs: rebuild */
 
 #define IHA_DTYPE_F32 0
 #define IHA_DTYPE_BF16 1
@@ -96,7 +104,8 @@ IHA_API int iha_forward_ex(const void *X, const void *W_Q, const void *W_K, cons
 
 /* Bytes of device workspace one call needs (0 if the sizes are invalid): the folded
  * weights (or, on the unfolded route, the head projections Y) + stacked Qbar, Kbar, Vbar
- * + Pbar, each 256-byte aligned. */
+ * + Pbar, each 256-byte aligned, + a 256-byte control slot (the call's own attention work
+ * counter, reset on the stream by every call). */
 IHA_API size_t iha_workspace_bytes(int B, int N, int H, int d, int P, int dtype);
 
 /* A static, human-readable name for a status code (never NULL). */
@@ -211,10 +220,12 @@ IHA_API int iha_mix_heads(const void *Y, const float *alpha_Q, const float *alph
                           int B, int N, int H, int d, int P, int dtype, void *QKV, void *stream);
 
 /* Step 3: masked softmax attention over each head's stacked sequence.
- * QKV as written by iha_project; Pbar [B][N][H][P][d].  For bf16 each call takes one of
- * 1024 device work counters in turn (zeroed on `stream` before the kernel), so at most 1024
- * calls may be executing or queued on different streams at once; calls on one stream are
- * ordered and never collide. */
+ * QKV as written by iha_project; Pbar [B][N][H][P][d].  This entry point has no workspace,
+ * so for bf16 each call takes the next of 1024 library-owned work counters (zeroed on
+ * `stream` before the kernel): at most 1024 calls may be executing or queued on different
+ * streams at once, and a CUDA graph that captured this call uses the same counter on every
+ * replay, so replays of it must not overlap.  Calls on one stream are ordered and never
+ * collide.  The whole-pass entry points keep their counter in their own workspace. */
 IHA_API int iha_attention(const void *QKV, int B, int N, int H, int d, int P,
                   int mask_mode, int window, int dtype, void *Pbar, void *stream);
 

@@ -43,6 +43,7 @@ def test_error_strings(iha):
     assert iha.iha_error_string(iha.IHA_OK) == "ok"
     assert "invalid" in iha.iha_error_string(iha.IHA_ERR_INVALID_ARG)
     assert "timed out" in iha.iha_error_string(iha.IHA_ERR_TIMEOUT)
+    assert "rebuild" in iha.iha_error_string(iha.IHA_ERR_BUILD)
     assert iha.iha_error_string(12345) == "unknown status"
 
 
@@ -53,7 +54,8 @@ def test_workspace_bytes(iha):
     for dtype, es in ((iha.IHA_DTYPE_BF16, 2), (iha.IHA_DTYPE_F32, 4)):
         # first region: head projections Y on the unfolded route, folded weights otherwise
         first = 3 * B * N * D * es if iha.iha_projection_route(H, d, P, dtype) == 1 else 3 * H * P * d * D * es
-        expect = al(first) + al(3 * B * H * N * P * d * es) + al(B * N * H * P * d * es)
+        # + the 256-byte control slot (the call's attention work counter)
+        expect = al(first) + al(3 * B * H * N * P * d * es) + al(B * N * H * P * d * es) + 256
         assert iha.iha_workspace_bytes(B, N, H, d, P, dtype) == expect
     assert iha.iha_workspace_bytes(0, N, H, d, P, 1) == 0
     assert iha.iha_workspace_bytes(B, N, H, 96, P, 1) == 0       # bf16 needs d in {64, 128}
@@ -232,3 +234,36 @@ def test_backward_validation(iha):
     assert call(H=20) == iha.IHA_ERR_UNSUPPORTED
     assert call(dO=fake + 8) == iha.IHA_ERR_INVALID_ARG                 # dO is read by TMA: 16-byte aligned
     assert call(ws=fake, wsb=256) == iha.IHA_ERR_WORKSPACE
+
+
+def test_register_contracts_hold_in_this_build(iha):
+    """The setmaxnreg kernels were compiled to the register count their split assumes
+    (the build already refuses otherwise; this reads the same ptxas reports)."""
+    import __graft_entry__
+    b = __graft_entry__._build_module()
+    b.check_register_contracts()
+    for frag, (src, const) in b.REG_CONTRACTS.items():
+        log = open(os.path.join(b.BUILD, src[:-3] + ".ptxas.txt")).read()
+        regs = {k: v for k, v in b._kernel_registers(log).items() if frag in k}
+        assert regs and set(regs.values()) == {b._declared_regs(src, const)}
+
+
+def test_register_contract_check_rejects_a_mismatch(tmp_path, monkeypatch):
+    """A kernel compiled to another register count makes the build fail, naming it."""
+    import __graft_entry__
+    b = __graft_entry__._build_module()
+    (tmp_path / "k_fake.ptxas.txt").write_text(
+        "ptxas info    : Compiling entry function '_ZN3iha7fake_wsEv' for 'sm_103a'\n"
+        "ptxas info    : Used 128 registers, used 16 barriers\n")
+    csrc = tmp_path / "csrc"
+    csrc.mkdir()
+    (csrc / "k_fake.cu").write_text("constexpr int FAKE_LAUNCH_REGS = 168;\n")
+    monkeypatch.setattr(b, "BUILD", str(tmp_path))
+    monkeypatch.setattr(b, "CSRC", str(csrc))
+    monkeypatch.setattr(b, "REG_CONTRACTS", {"fake_ws": ("k_fake.cu", "FAKE_LAUNCH_REGS")})
+    with pytest.raises(RuntimeError, match="_ZN3iha7fake_wsEv: 128 registers"):
+        b.check_register_contracts()
+    (tmp_path / "k_fake.ptxas.txt").write_text(
+        "ptxas info    : Compiling entry function '_ZN3iha7fake_wsEv' for 'sm_103a'\n"
+        "ptxas info    : Used 168 registers, used 16 barriers\n")
+    b.check_register_contracts()

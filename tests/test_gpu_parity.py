@@ -126,13 +126,33 @@ def test_edge_shapes_every_element(iha, w):
 # full-size workloads: sampled rows
 # ---------------------------------------------------------------------------
 
-def sample_rows(w):
+def sample_rows(w, seed=0):
+    """Flat output rows (b*N + t) to compare at full size: fixed edge tokens (first and
+    last tokens, tile and window edges) of the first and last batch element, plus one
+    random token of every 128-row stacked query tile (128/P tokens) of EVERY batch
+    element, so that each attention work item of every head has rows under test."""
     toks = {0, 1, 2, 63, 64, 127, 128, 129, 255, 256, w.N // 2, w.N // 2 + 1, w.N - 2, w.N - 1}
     if w.mask_mode == WN:
         toks |= {w.window - 1, w.window, w.window + 1, 2 * w.window}
-    toks = sorted(t for t in toks if 0 <= t < w.N)
-    bs = sorted({0, w.B - 1})
-    return [b * w.N + t for b in bs for t in toks]
+    toks = {t for t in toks if 0 <= t < w.N}
+    rng = np.random.default_rng(1000 + seed)
+    per_tile = max(1, 128 // w.P)   # tokens per 128-row stacked tile
+    rows = set()
+    for b in range(w.B):
+        tile_toks = {int(t0 + rng.integers(0, min(per_tile, w.N - t0))) for t0 in range(0, w.N, per_tile)}
+        edge = toks if b in (0, w.B - 1) else set()
+        rows |= {b * w.N + t for t in tile_toks | edge}
+    return sorted(rows)
+
+
+def one_hot_contraction(H, P, k):
+    """R [H][H*P] picking pseudo-block j = (h + k) mod P of head h itself: output head h is
+    then exactly that pseudo-head's attention output (no other pseudo-head mixed in), and
+    over k = 0..P-1 every (h, j) is picked once."""
+    R = torch.zeros(H, H * P, dtype=torch.float32)
+    for h in range(H):
+        R[h, h * P + (h + k) % P] = 1.0
+    return R
 
 
 FULL = ["bf16_window1024_n4096", "bf16_causal_p4_n8192", "bf16_window4096_n16384"]
@@ -140,14 +160,39 @@ FULL = ["bf16_window1024_n4096", "bf16_causal_p4_n8192", "bf16_window4096_n16384
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled_rows(iha, name):
+    """The launch configuration the benchmark times: one token of every stacked query
+    tile of every batch element against the oracle, and a second call bit-identical."""
     w = gi.WORKLOADS[name]
     inp = gi.make_inputs(w)
-    got = run_gpu(iha, w, inp).double().cpu().numpy().reshape(w.B * w.N, w.D)
+    dinp = to_dev(inp)
+    out = run_gpu(iha, w, dinp=dinp)
+    again = run_gpu(iha, w, dinp=dinp)
+    assert torch.equal(out, again), f"{name}: two calls on the same inputs differ"
+    got = out.double().cpu().numpy().reshape(w.B * w.N, w.D)
     rows = sample_rows(w)
     ref = oracle_rows(w, inp, rows=rows, projection="numpy")
     assert_parity(w, got[rows], ref)
     # properties that hold at every row
     assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_single_pseudo_head_outputs(iha, name):
+    """R picks one pseudo-block per head (one_hot_contraction), so every compared output
+    element is one attention output element of one pseudo-head, undiluted by the
+    contraction over H*P pseudo-heads; run for k = 0..P-1, each (h, j) of every sampled
+    tile is compared once."""
+    w = gi.WORKLOADS[name]
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    for k in range(w.P):
+        R = one_hot_contraction(w.H, w.P, k)
+        inp["R"] = R
+        dinp["R"] = R.to("cuda:0")
+        got = run_gpu(iha, w, dinp=dinp).double().cpu().numpy().reshape(w.B * w.N, w.D)
+        rows = sample_rows(w, seed=k + 1)
+        ref = oracle_rows(w, inp, rows=rows, projection="numpy")
+        assert_parity(w, got[rows], ref)
 
 
 def test_full_size_mha_special_case(iha):

@@ -21,6 +21,7 @@ IHA_ERR_UNSUPPORTED = 2
 IHA_ERR_WORKSPACE = 3
 IHA_ERR_CUDA = 4
 IHA_ERR_TIMEOUT = 5
+IHA_ERR_BUILD = 6
 
 IHA_DTYPE_F32 = 0
 IHA_DTYPE_BF16 = 1

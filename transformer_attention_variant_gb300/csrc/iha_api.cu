@@ -79,7 +79,7 @@ static int validate_mask(int mask_mode, int window) {
 }
 
 struct WsLayout {
-    size_t wt, qkv, pbar, total;
+    size_t wt, qkv, pbar, ctr, total;
 };
 
 static WsLayout ws_layout(const Shape &sh, int dtype) {
@@ -90,11 +90,12 @@ static WsLayout ws_layout(const Shape &sh, int dtype) {
                                                    : (size_t)sh.wt_rows() * (size_t)sh.D() * es;
     w.qkv = align256(first);
     w.pbar = w.qkv + align256(3 * (size_t)sh.qkv_elems() * es);
-    w.total = w.pbar + align256((size_t)sh.B * sh.N * sh.H * sh.P * sh.d * es);
+    w.ctr = w.pbar + align256((size_t)sh.B * sh.N * sh.H * sh.P * sh.d * es);
+    w.total = w.ctr + kCtrlBytes;   // the call's own attention work counter
     return w;
 }
 
-static int cuda_status(cudaError_t e) { return e == cudaSuccess ? IHA_OK : IHA_ERR_CUDA; }
+static int cuda_status(cudaError_t e) { return status_from_cuda(e); }
 
 static int run_forward(const void *X, const void *WQ, const void *WK, const void *WV, const float *aQ,
                        const float *aK, const float *aV, const float *R, const Shape &sh, int mask_mode, int window,
@@ -110,6 +111,7 @@ static int run_forward(const void *X, const void *WQ, const void *WK, const void
     int *status = status_ptr();
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     void *Wt = ws + lay.wt, *QKV = ws + lay.qkv, *Pbar = ws + lay.pbar;
+    unsigned int *ticket = reinterpret_cast<unsigned int *>(ws + lay.ctr);
     cudaError_t e;
     if (unfolded_route(sh, dtype)) {
         e = launch_project_heads(X, WQ, WK, WV, sh, Wt, st, status);   // Y in the first region
@@ -118,7 +120,7 @@ static int run_forward(const void *X, const void *WQ, const void *WK, const void
         e = launch_fold(WQ, WK, WV, aQ, aK, aV, sh, dtype, Wt, st);
         if (e == cudaSuccess) e = launch_project(X, Wt, sh, dtype, QKV, st, status);
     }
-    if (e == cudaSuccess) e = launch_attention(QKV, sh, mask_mode, window, dtype, Pbar, st, status);
+    if (e == cudaSuccess) e = launch_attention(QKV, sh, mask_mode, window, dtype, Pbar, st, status, ticket);
     if (e == cudaSuccess) e = launch_contract(Pbar, R, sh, dtype, out, st, status);
     if (own) {
         const cudaError_t e2 = cudaFreeAsync(workspace, st);
@@ -165,6 +167,7 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
     const WsLayout lay = ws_layout(sh, IHA_DTYPE_BF16);
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     uint8_t *Y = w8 + lay.wt, *QKV = w8 + lay.qkv, *Pbar = w8 + lay.pbar;
+    unsigned int *ticket = reinterpret_cast<unsigned int *>(w8 + lay.ctr);
     int *status = status_ptr();
     // events: 0 start, 1-2 W ready (one per copy stream), 3.. X chunks, then contraction chunks,
     // then the two copy streams' last copies
@@ -212,7 +215,8 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
                                      Shape{1, (int)(r1 - r0), sh.H, sh.d, sh.P}, Y + r0 * row_y, st, status);
     }
     if (e == cudaSuccess) e = launch_mix(Y, daQ, daK, daV, sh, QKV, st, status);
-    if (e == cudaSuccess) e = launch_attention(QKV, sh, mask_mode, window, IHA_DTYPE_BF16, Pbar, st, status);
+    if (e == cudaSuccess)
+        e = launch_attention(QKV, sh, mask_mode, window, IHA_DTYPE_BF16, Pbar, st, status, ticket);
     // contraction chunk by chunk, each chunk's output copied down as soon as it is done
     for (int i = 0; i < FH_CHUNKS && e == cudaSuccess; ++i) {
         long long r0, r1;
@@ -276,6 +280,7 @@ const char *iha_error_string(int status) {
         case IHA_ERR_WORKSPACE: return "workspace too small or misaligned";
         case IHA_ERR_CUDA: return "CUDA error";
         case IHA_ERR_TIMEOUT: return "device wait timed out";
+        case IHA_ERR_BUILD: return "library build does not match this device or a kernel's register contract: rebuild";
         default: return "unknown status";
     }
 }

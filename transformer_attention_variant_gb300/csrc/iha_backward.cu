@@ -35,7 +35,7 @@ cudaError_t launch_bwd_dw_tc(const void *X, const void *const dY[3], long long T
                              cudaStream_t st, int *status);
 
 struct BwdLayout {
-    size_t y, qkv, vb, pbar, lse, dpst, dv, ds, dy, part, total;
+    size_t y, qkv, vb, pbar, lse, dpst, dv, ds, dy, part, ctr, total;
     size_t ld_bytes;   // lse and D: [B*H][bwd_ld_stride(L)] floats each
 };
 
@@ -58,6 +58,7 @@ static BwdLayout bwd_layout(const Shape &sh) {
     l.ds = o;   o += al256(3 * T * HP * sh.d * 2);
     l.dy = o;   o += al256(3 * T * D * 2);
     l.part = o; o += al256(bwd_gram_part_floats((long long)T, sh.H, (int)HP) * 4);
+    l.ctr = o;  o += kCtrlBytes;   // the forward attention's work counter
     l.total = o;
     return l;
 }
@@ -101,7 +102,8 @@ static cudaError_t bwd_forward_pieces(const void *X, const void *W_Q, const void
     if (e == cudaSuccess) e = launch_project_heads(X, W_Q, W_K, W_V, sh, Y, st, status);
     if (e == cudaSuccess) e = launch_mix(Y, alpha_Q, alpha_K, alpha_V, sh, QKV, st, status);
     if (e == cudaSuccess)
-        e = launch_attention_lse(QKV, sh, mask_mode, window, IHA_DTYPE_BF16, Pbar, lse, ld, st, status);
+        e = launch_attention_lse(QKV, sh, mask_mode, window, IHA_DTYPE_BF16, Pbar, lse, ld, st, status,
+                                 reinterpret_cast<unsigned int *>(ws + lay.ctr));
     // Vbar again, in bf16: the V third of Y mixed with alpha_V
     if (e == cudaSuccess)
         e = launch_mix_sets(Y + (size_t)2 * D * 2, alpha_V, alpha_V, alpha_V, sh, 1, Vb, st, status, 3, -1);
@@ -183,7 +185,7 @@ static int bwd_end(cudaError_t e, bool own, void *workspace, cudaStream_t st) {
         const cudaError_t e2 = cudaFreeAsync(workspace, st);
         if (e == cudaSuccess) e = e2;
     }
-    return e == cudaSuccess ? IHA_OK : IHA_ERR_CUDA;
+    return status_from_cuda(e);
 }
 
 }  // namespace iha

@@ -44,7 +44,7 @@ int iha_decode_step(const void *x, const void *W_Q, const void *W_K, const void 
         const cudaError_t e2 = cudaFreeAsync(workspace, st);
         if (e == cudaSuccess) e = e2;
     }
-    return e == cudaSuccess ? IHA_OK : IHA_ERR_CUDA;
+    return status_from_cuda(e);
 }
 
 }  // extern "C"

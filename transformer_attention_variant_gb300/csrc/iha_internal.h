@@ -5,7 +5,30 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "iha.h"
+
 namespace iha {
+
+// A CUDA error as an IHA status: kernel images that do not match the device or their
+// register contract (see check_register_contract) are IHA_ERR_BUILD, anything else
+// IHA_ERR_CUDA.
+inline int status_from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return IHA_OK;
+    if (e == cudaErrorInvalidKernelImage || e == cudaErrorNoKernelImageForDevice) return IHA_ERR_BUILD;
+    return IHA_ERR_CUDA;
+}
+
+// Warp-specialised kernels that move registers between warpgroups (setmaxnreg) assume
+// they were compiled to exactly `regs` registers per thread: a warpgroup asking for more
+// than the launch provided would wait forever.  The build checks this from the ptxas
+// report; this guard turns a library built any other way into an error before launch.
+template <typename Kernel>
+inline cudaError_t check_register_contract(Kernel kern, int regs) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    return fa.numRegs == regs ? cudaSuccess : cudaErrorInvalidKernelImage;
+}
 
 // Wait-site codes written to the status word (low 12 bits) when a bounded wait expires.
 enum WaitSite {
@@ -88,11 +111,17 @@ cudaError_t launch_mix_sets(const void *Y, const float *aQ, const float *aK, con
 // Attention that also writes each stacked row's log2 softmax normaliser (bf16 only) into
 // lse[b*H + h][lse_stride] (lse_stride >= N*P).
 cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
-                                 void *Pbar, float *lse, int lse_stride, cudaStream_t st, int *status);
+                                 void *Pbar, float *lse, int lse_stride, cudaStream_t st, int *status,
+                                 unsigned int *ticket = nullptr);
 
 // Step 3: masked softmax attention per head over the stacked sequence -> Pbar [B][N][H][P][d].
+// ticket: the launch's work counter (one unsigned int of the caller's workspace, zeroed on
+// `st` before the kernel), or NULL to take the next one of a ring of library-owned counters.
 cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
-                             void *Pbar, cudaStream_t st, int *status);
+                             void *Pbar, cudaStream_t st, int *status, unsigned int *ticket = nullptr);
+
+// Bytes of the control slot every workspace ends with (the attention's work counter).
+constexpr size_t kCtrlBytes = 256;
 
 // Step 4: out[b][t][h][:] = sum_i R[h][i] Pbar[b][t][i][:], i = h'*P + j.
 cudaError_t launch_contract(const void *Pbar, const float *R, const Shape &sh, int dtype, void *out,

@@ -51,7 +51,7 @@ constexpr int AT_BM = 128;         // query rows per tile
 constexpr int AT_BN = 128;         // key rows per tile
 constexpr int AT_THREADS = 384;    // 2 softmax warpgroups + 1 warpgroup (producer, MMA, 2 idle)
 // Register split (setmaxnreg): the kernel is compiled to exactly AT_LAUNCH_REGS per thread
-// (384 x 168 = 64512 registers allocated at launch); the producer/MMA warpgroup gives
+// (384 x 168 = 64512 registers allocated at launch; the build checks the count); the producer/MMA warpgroup gives
 // registers back, the softmax warpgroups take them: 128 x 72 + 256 x 216 = 64512.
 constexpr int AT_LAUNCH_REGS = 168, AT_REGS_SOFTMAX = 216, AT_REGS_CONTROL = 72;
 static_assert(128 * AT_REGS_CONTROL + 256 * AT_REGS_SOFTMAX <= AT_THREADS * AT_LAUNCH_REGS, "register split");
@@ -639,21 +639,25 @@ attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 cudaError_t launch_attention_f32(const void *QKV, const Shape &sh, int mask_mode, int window, void *Pbar,
                                  cudaStream_t st);
 
-// A work counter for one launch, set to 0 on the launch's stream.  Launches take the
-// AT_TICKETS counters in turn, so up to AT_TICKETS launches may run at once.
-static unsigned int *attn_ticket(cudaStream_t st, cudaError_t &e) {
+// The work counter of one launch, set to 0 on the launch's stream: the caller's own (a slot
+// of its workspace) when it has one; otherwise the next of AT_TICKETS library-owned
+// counters, taken in turn, so that up to AT_TICKETS such launches may run at once.
+static unsigned int *attn_ticket(unsigned int *own, cudaStream_t st, cudaError_t &e) {
     static std::atomic<unsigned> next{0};
-    unsigned int *base = nullptr;
-    e = cudaGetSymbolAddress(reinterpret_cast<void **>(&base), g_attn_tickets);
-    if (e != cudaSuccess) return nullptr;
-    unsigned int *t = base + next.fetch_add(1u) % AT_TICKETS;
+    unsigned int *t = own;
+    if (!t) {
+        unsigned int *base = nullptr;
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&base), g_attn_tickets);
+        if (e != cudaSuccess) return nullptr;
+        t = base + next.fetch_add(1u) % AT_TICKETS;
+    }
     e = cudaMemsetAsync(t, 0, sizeof(unsigned int), st);
     return e == cudaSuccess ? t : nullptr;
 }
 
 template <int DH>
 static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mode, int window, void *Pbar,
-                                  float *lse, int lse_stride, cudaStream_t st, int *status) {
+                                  float *lse, int lse_stride, cudaStream_t st, int *status, unsigned int *ticket) {
     using C = AttnCfg<DH>;
     const long long L = sh.L(), BH = (long long)sh.B * sh.H;
     const __nv_bfloat16 *base = (const __nv_bfloat16 *)QKV;
@@ -694,11 +698,8 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     p.status = status;
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    // the register split above is only valid for exactly AT_LAUNCH_REGS registers per thread
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attn_fwd_tc<DH>);
+    e = check_register_contract(attn_fwd_tc<DH>, AT_LAUNCH_REGS);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs != AT_LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     p.num_heads = (int)BH;
     {
         const long long kv_bytes_per_head = 2LL * L * DH * 2;   // K and V of one (b, h)
@@ -710,25 +711,25 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     // persistent: one CTA per SM, each looping over work items
     const long long items = BH * p.num_qblocks;
     const unsigned grid = (unsigned)(items < device_sm_count() ? items : device_sm_count());
-    p.ticket = attn_ticket(st, e);
+    p.ticket = attn_ticket(ticket, st, e);
     if (!p.ticket) return e;
     attn_fwd_tc<DH><<<grid, AT_THREADS, C::SMEM, st>>>(tm[0], tm[1], tm[2], tmO, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
-                                 void *Pbar, float *lse, int lse_stride, cudaStream_t st, int *status);
-
 cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype, void *Pbar,
-                             cudaStream_t st, int *status) {
-    return launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, nullptr, 0, st, status);
+                             cudaStream_t st, int *status, unsigned int *ticket) {
+    return launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, nullptr, 0, st, status, ticket);
 }
 
 cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
-                                 void *Pbar, float *lse, int lse_stride, cudaStream_t st, int *status) {
+                                 void *Pbar, float *lse, int lse_stride, cudaStream_t st, int *status,
+                                 unsigned int *ticket) {
     if (dtype == 0) return launch_attention_f32(QKV, sh, mask_mode, window, Pbar, st);
-    if (sh.d == 128) return launch_attn_tc<128>(QKV, sh, mask_mode, window, Pbar, lse, lse_stride, st, status);
-    if (sh.d == 64) return launch_attn_tc<64>(QKV, sh, mask_mode, window, Pbar, lse, lse_stride, st, status);
+    if (sh.d == 128)
+        return launch_attn_tc<128>(QKV, sh, mask_mode, window, Pbar, lse, lse_stride, st, status, ticket);
+    if (sh.d == 64)
+        return launch_attn_tc<64>(QKV, sh, mask_mode, window, Pbar, lse, lse_stride, st, status, ticket);
     return cudaErrorInvalidValue;
 }
 

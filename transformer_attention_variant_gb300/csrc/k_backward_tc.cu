@@ -28,12 +28,8 @@
 // and D by bulk copy, on the same barrier); warp 9 = MMA issuer.  The MMA order S(i),
 // dP(i), [wait P(i-1)] acc(i-1), S(i+1), ... keeps the tensor pipe busy while a block's
 // exponentials run.
-// CTAs may run in clusters of BA_CLUSTER adjacent resident tiles that stream the same
-// blocks: each CTA loads a slice of every block and multicasts it to the cluster, and a
-// ring slot is refilled only after the MMA warps of all the cluster's CTAs have released
-// it.  Measured on the causal P=4 N=8192 and windowed N=4096 layers, clusters of 2 and 4
-// were 1-5% slower than single CTAs (the score products, not L2 streaming, bound these
-// kernels), so BA_CLUSTER is 1.
+// Each CTA loads every streamed block for itself; CTAs of neighbouring tiles read the same
+// blocks, which L2 serves (the score products, not L2 streaming, bound these kernels).
 // TMEM: buffer b: S at 128b, dP at 128b+64 (P^T / dS overwrite their first 32 columns as
 // bf16 pairs); accumulators at 256 (dK or dQ) and 256+d (dV).  512 columns.
 //
@@ -57,7 +53,6 @@ namespace iha {
 constexpr int BA_ROWS = 128;       // resident rows per CTA
 constexpr int BA_BLK = 64;         // streamed rows per block
 constexpr int BA_STAGES = 4;       // moving-block ring
-constexpr int BA_CLUSTER = 1;      // CTAs (adjacent resident tiles) sharing each streamed block
 constexpr int BA_THREADS = 384;
 constexpr int BA_LAUNCH_REGS = 168, BA_REGS_SOFTMAX = 216, BA_REGS_CONTROL = 72;
 static_assert(128 * BA_REGS_CONTROL + 256 * BA_REGS_SOFTMAX <= BA_THREADS * BA_LAUNCH_REGS, "register split");
@@ -107,19 +102,15 @@ __device__ __forceinline__ void ba_query_interval(const BwdAttnParams &p, int c,
     if (p.mask_mode == 2) hi = min(hi, (t + p.window) * p.P - 1);
 }
 
-// The resident tile of this CTA and the blocks its cluster streams: [mb0, mb0 + nmov).
-// A cluster holds CS adjacent tiles (the grid is padded to a multiple of CS; padding tiles
-// have no rows) and streams the union of their ranges.  Both interval ends are
-// nondecreasing in the row, so that union runs from the first row's lower end to the last
-// row's upper end.
-template <bool KV, int CS>
+// The resident tile of this CTA and the blocks it streams: [mb0, mb0 + nmov).  Both
+// interval ends are nondecreasing in the row, so the union of the tile's rows' ranges runs
+// from the first row's lower end to the last row's upper end.
+template <bool KV>
 __device__ __forceinline__ void ba_range(const BwdAttnParams &p, int &tile, int &mb0, int &nmov) {
     // KV: early key tiles are read by the most queries (causal), Q: late query tiles read
-    // the most keys -- heaviest clusters first
-    const int ncl = (int)gridDim.x / CS, c = (int)blockIdx.x / CS;
-    const int cl = KV ? c : ncl - 1 - c;
-    tile = cl * CS + (int)blockIdx.x % CS;
-    const int r0 = cl * CS * BA_ROWS, r1 = min((cl + 1) * CS * BA_ROWS - 1, p.L - 1);
+    // the most keys -- heaviest tiles first
+    tile = KV ? (int)blockIdx.x : (int)gridDim.x - 1 - (int)blockIdx.x;
+    const int r0 = tile * BA_ROWS, r1 = min((tile + 1) * BA_ROWS - 1, p.L - 1);
     int lo0, hi0, lo1, hi1;
     if (KV) {
         ba_query_interval(p, r0, lo0, hi0);
@@ -139,10 +130,8 @@ __device__ __forceinline__ float ba_exp2(float x) {
 }
 
 // tmS1/tmS2: resident operands of the score and dP products (KV: K, V; Q: Q, dPbar), box
-// 128 rows; tmM1/tmM2: streamed (KV: Q, dPbar; Q: K, V), box 64/CS rows: each CTA of a
-// cluster loads one slice of every streamed block and multicasts it to all CS CTAs, so the
-// cluster reads each block from L2 once.  All [B*H][L][d] bf16.
-template <int DH, bool KV, int CS>
+// 128 rows; tmM1/tmM2: streamed (KV: Q, dPbar; Q: K, V), box 64 rows.  All [B*H][L][d] bf16.
+template <int DH, bool KV>
 __global__ void __launch_bounds__(BA_THREADS, 1)
 bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmS2,
             const __grid_constant__ CUtensorMap tmM1, const __grid_constant__ CUtensorMap tmM2,
@@ -168,15 +157,14 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
     const int warp = warp_id(), lane = lane_id();
     const int bh = blockIdx.y;
     int tile, mb0, nmov;
-    ba_range<KV, CS>(p, tile, mb0, nmov);
-    constexpr uint16_t kAll = (1u << CS) - 1;   // every CTA of the cluster
+    ba_range<KV>(p, tile, mb0, nmov);
     const int row0 = tile * BA_ROWS;
 
     if (threadIdx.x == 0) {
         mbar_init(stat_full, 1);
         for (int s = 0; s < BA_STAGES; ++s) {
             mbar_init(&mov_full[s], 1);
-            mbar_init(&mov_empty[s], CS);   // released by the MMA warp of every CTA of the cluster
+            mbar_init(&mov_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
@@ -202,7 +190,6 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    cluster_sync();   // every CTA's barriers are initialised before any multicast reaches them
 
     if (warp >= 8) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BA_REGS_CONTROL));
@@ -220,7 +207,6 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
                 }
             }
             int issued = 0;
-            const int slice = (int)cluster_ctarank() * (BA_BLK / CS);   // this CTA's rows of each block
             for (int i = 0; i < nmov; ++i) {
                 const int st = i % BA_STAGES;
                 if (!wait(&mov_empty[st], ((i / BA_STAGES) & 1) ^ 1)) break;
@@ -234,17 +220,16 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
                         bulk_load(ld, p.lse + (size_t)bh * p.ld + rb, BA_BLK * 4, &mov_full[st]);
                         bulk_load(ld + BA_BLK, p.Dv + (size_t)bh * p.ld + rb, BA_BLK * 4, &mov_full[st]);
                     }
-                    uint8_t *dst = sM + st * 2 * C::MOV_BYTES + slice * 128;
+                    uint8_t *dst = sM + st * 2 * C::MOV_BYTES;
                     for (int c = 0; c < C::CHUNKS; ++c) {
-                        tma_load_3d_mc(&tmM1, &mov_full[st], dst + c * (BA_BLK * 128), c * 64, rb + slice, bh, kAll);
-                        tma_load_3d_mc(&tmM2, &mov_full[st], dst + C::MOV_BYTES + c * (BA_BLK * 128), c * 64,
-                                       rb + slice, bh, kAll);
+                        tma_load_3d(&tmM1, &mov_full[st], dst + c * (BA_BLK * 128), c * 64, rb, bh);
+                        tma_load_3d(&tmM2, &mov_full[st], dst + C::MOV_BYTES + c * (BA_BLK * 128), c * 64, rb, bh);
                     }
                 }
                 ++issued;
             }
-            // every copy into this CTA (its own slices and the other CTAs') has landed before
-            // the CTA may exit (the normal path has consumed them all already)
+            // every copy into this CTA has landed before the CTA may exit (the normal path has
+            // consumed them all already)
             for (int k = issued - BA_STAGES > 0 ? issued - BA_STAGES : 0; k < issued; ++k)
                 mbar_wait(&mov_full[k % BA_STAGES], (k / BA_STAGES) & 1, p.status, kSiteBwdProducer, nullptr,
                           kWaitLimitNs);
@@ -311,7 +296,7 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
                     tc_fence_after();
                     if (leader) {
                         issue_acc(j);
-                        mma_commit_mc(&mov_empty[j % BA_STAGES], kAll);
+                        mma_commit(&mov_empty[j % BA_STAGES]);
                         if (j == nmov - 1) mma_commit(acc_full);
                     }
                 }
@@ -470,7 +455,6 @@ bwd_attn_tc(const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CU
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();   // no CTA leaves while another may still multicast into it or release its slots
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -481,26 +465,15 @@ template <int DH, bool KV>
 static cudaError_t launch_bwd_attn_kernel(const CUtensorMap (&tm)[4], const BwdAttnParams &p, int BH,
                                           cudaStream_t st) {
     using C = BwdAttnCfg<DH>;
-    constexpr int CS = BA_CLUSTER;
-    auto kern = bwd_attn_tc<DH, KV, CS>;
+    auto kern = bwd_attn_tc<DH, KV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess) e = check_register_contract(kern, BA_LAUNCH_REGS);
     if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != BA_LAUNCH_REGS) return cudaErrorInvalidConfiguration;   // the register split needs it
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.ntiles + CS - 1) / CS * CS), (unsigned)BH);
+    cfg.gridDim = dim3((unsigned)p.ntiles, (unsigned)BH);
     cfg.blockDim = dim3(BA_THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     if (KV) e = cudaLaunchKernelEx(&cfg, kern, tm[1], tm[2], tm[0], tm[3], p);
     else e = cudaLaunchKernelEx(&cfg, kern, tm[0], tm[3], tm[1], tm[2], p);
     if (e != cudaSuccess) return e;
@@ -521,15 +494,14 @@ cudaError_t launch_bwd_attention_tc(const void *Q, const void *K, const void *Vb
     const long long L = sh.L(), BH = (long long)sh.B * sh.H;
     if (BH > 65535) return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(lse) & 15) || (reinterpret_cast<uintptr_t>(Dv) & 15)) return cudaErrorInvalidValue;
-    static_assert(BA_BLK % (8 * BA_CLUSTER) == 0, "slices are whole 8-row swizzle atoms");
-    // maps [0] Q, [1] K, [2] Vb, [3] dPst with 128-row boxes (resident) and one cluster
-    // member's slice of a streamed block
+    // maps [0] Q, [1] K, [2] Vb, [3] dPst with 128-row boxes (resident) and 64-row boxes
+    // (a streamed block)
     const void *src[4] = {Q, K, Vb, dPst};
     CUtensorMap big[4], small[4];
     for (int s = 0; s < 4; ++s) {
         const uint64_t dims[3] = {(uint64_t)sh.d, (uint64_t)L, (uint64_t)BH};
         const uint64_t strides[2] = {(uint64_t)sh.d * 2, (uint64_t)L * sh.d * 2};
-        const uint32_t box_b[3] = {64, BA_ROWS, 1}, box_s[3] = {64, BA_BLK / BA_CLUSTER, 1};
+        const uint32_t box_b[3] = {64, BA_ROWS, 1}, box_s[3] = {64, BA_BLK, 1};
         if (!make_tmap_bf16(&big[s], src[s], 3, dims, strides, box_b)) return cudaErrorInvalidValue;
         if (!make_tmap_bf16(&small[s], src[s], 3, dims, strides, box_s)) return cudaErrorInvalidValue;
     }

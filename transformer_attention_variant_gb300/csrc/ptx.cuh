@@ -212,17 +212,6 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, i
                  : "memory");
 }
 
-// The same load delivered to the same shared-memory offset in every CTA of the cluster
-// named by cta_mask, each CTA's mbarrier at `bar`'s offset receiving the bytes it got.
-__device__ __forceinline__ void tma_load_3d_mc(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y, int z,
-                                               uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
-        : "memory");
-}
-
 // Tiled store shared -> global through a rank-2 tensor map (bulk groups as below).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0, int c1) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -295,15 +284,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// The same, arriving on the mbarrier at `bar`'s offset in every CTA of cta_mask.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // ------------------------------------------------------------------------------------
 // programmatic dependent launch: a kernel launched with programmatic stream serialization
 // may start while its predecessor on the stream runs; pdl_wait() returns once the
@@ -312,20 +292,6 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) 
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-// ------------------------------------------------------------------------------------
-// thread-block clusters
-// ------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Every thread of every CTA of the cluster: writes before it (barrier inits included) are
-// visible cluster-wide after it.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D:
 //   [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format (1 = bf16),
