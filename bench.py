@@ -4,7 +4,8 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl re
 
 One step = one pass of the whole hot path over one batch of synthetic input:
 projection + pseudo-head mixing into the stacked layout (the library's route for the
-shape: project all heads then mix, or fold alpha into W then project) -> attention
+shape: the head projections with the mixing in the GEMM epilogue, or fold alpha into W
+then project) -> attention
 over the stacked sequence -> R contraction, launched through the library's step
 entry points on one stream, each kernel bracketed by CUDA events on that stream.
 L2 is flushed (256 MiB write) between steps, outside the timed events.
@@ -79,11 +80,11 @@ def work(w):
     es = 2
     bytes_contract = es * (B * N * H * P * d + B * N * D)
     bytes_fold = es * (3 * D * D + 3 * H * P * d * D)
-    bytes_mix = es * (B * N * 3 * D + 3 * B * H * N * P * d)   # read Y, write Qbar/Kbar/Vbar
+    bytes_slice = es * 2 * 3 * D * D                            # read W_Q/W_K/W_V, write them slice-major
     return dict(pairs=pairs, attn=attn, proj_folded=proj_folded, proj_heads=proj_heads,
                 algorithmic=proj_heads + mixing + attn + contract,
                 executed_folded=proj_folded + attn + contract, executed_unfolded=proj_heads + mixing + attn + contract,
-                bytes_contract=bytes_contract, bytes_fold=bytes_fold, bytes_mix=bytes_mix, pseudo_tokens=B * P * N)
+                bytes_contract=bytes_contract, bytes_fold=bytes_fold, bytes_slice=bytes_slice, pseudo_tokens=B * P * N)
 
 
 # ---------------------------------------------------------------------------
@@ -264,23 +265,23 @@ class ForwardStep:
         tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         self.d = {k: v.to(dev).contiguous() for k, v in host.items()}
         self.route = iha.iha_projection_route(w.H, w.d, w.P, self.dt)
-        if self.route == 1:
-            self.Wt = torch.empty(w.B * w.N, 3 * w.D, dtype=tdt, device=dev)        # head projections Y
-        else:
-            self.Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=tdt, device=dev)  # folded weights
+        if self.route == 1:   # slice-major weights
+            self.Wt = torch.empty(iha.iha_sliced_weights_bytes(w.H, w.d, self.dt), dtype=torch.uint8, device=dev)
+        else:                 # folded weights
+            self.Wt = torch.empty(3 * w.H * w.P * w.d, w.D, dtype=tdt, device=dev)
         self.QKV = torch.empty(3, w.B, w.H, w.N * w.P, w.d, dtype=tdt, device=dev)
         self.Pbar = torch.empty(w.B, w.N, w.H, w.P, w.d, dtype=tdt, device=dev)
         self.out = torch.empty(w.B, w.N, w.D, dtype=tdt, device=dev)
-        self.names = (["project_heads", "mix", "attention", "contract"] if self.route == 1
+        self.names = (["slice_weights", "project_mix", "attention", "contract"] if self.route == 1
                       else ["fold", "project", "attention", "contract"])
 
     def launches(self):
         iha, w, d, dt, s = self.iha, self.w, self.d, self.dt, self.stream
         if self.route == 1:
-            yield lambda: iha.check(iha.iha_project_heads(d["X"], d["W_Q"], d["W_K"], d["W_V"], w.B, w.N, w.H, w.d,
-                                                          dt, self.Wt, s), "project_heads")
-            yield lambda: iha.check(iha.iha_mix_heads(self.Wt, d["alpha_Q"], d["alpha_K"], d["alpha_V"], w.B, w.N,
-                                                      w.H, w.d, w.P, dt, self.QKV, s), "mix")
+            yield lambda: iha.check(iha.iha_slice_weights(d["W_Q"], d["W_K"], d["W_V"], w.H, w.d, dt, self.Wt, s),
+                                    "slice_weights")
+            yield lambda: iha.check(iha.iha_project_mix(d["X"], self.Wt, d["alpha_Q"], d["alpha_K"], d["alpha_V"],
+                                                        w.B, w.N, w.H, w.d, w.P, dt, self.QKV, s), "project_mix")
         else:
             yield lambda: iha.check(iha.iha_fold_weights(d["W_Q"], d["W_K"], d["W_V"], d["alpha_Q"], d["alpha_K"],
                                                          d["alpha_V"], w.H, w.d, w.P, dt, self.Wt, s), "fold")
@@ -392,14 +393,14 @@ def run_gpu(args, w):
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
                 else "fallback 1.9 PFLOP/s"}
         traffic_key = "attention"
-    elif dom in ("project", "project_heads"):
+    elif dom in ("project", "project_mix"):
         ach = (wk["proj_folded"] if dom == "project" else wk["proj_heads"]) / (kmean[dom] * 1e-3) / 1e12
         roof = {"kernel": "proj_gemm_tc", "bound": "tensor", "achieved": ach, "peak": peaks["bf16"],
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16"],
                 "frac_of_sustained": ach / peaks["bf16_sustained"], "peak_source": peaks["source"]}
         traffic_key = "project"
     else:
-        b = {"contract": wk["bytes_contract"], "fold": wk["bytes_fold"], "mix": wk["bytes_mix"]}[dom]
+        b = {"contract": wk["bytes_contract"], "fold": wk["bytes_fold"], "slice_weights": wk["bytes_slice"]}[dom]
         ach = b / (kmean[dom] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": ach / peaks["hbm"], "peak_source": peaks["source"]}
@@ -416,11 +417,12 @@ def run_gpu(args, w):
             "forward_algorithmic": wk["algorithmic"] / (mean_step * 1e-3) / 1e12,
             "forward_executed": (wk["executed_unfolded"] if route == 1 else wk["executed_folded"])
             / (mean_step * 1e-3) / 1e12,
-            "projection_gemm": (wk["proj_heads"] / (kmean["project_heads"] * 1e-3) if route == 1
+            "projection_gemm": (wk["proj_heads"] / (kmean["project_mix"] * 1e-3) if route == 1
                                 else wk["proj_folded"] / (kmean["project"] * 1e-3)) / 1e12,
         },
         "kernel_ms": kmean,
-        "projection_route": "project heads + mix" if route == 1 else "fold alpha into W + project",
+        "projection_route": ("head projections with the mixing in the GEMM epilogue" if route == 1
+                             else "fold alpha into W + project"),
         "roofline": roof,
         "gpu_launches": len(names) * args.steps,
         "wall_s_timed_region": t_wall,

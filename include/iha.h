@@ -103,7 +103,7 @@ IHA_API int iha_forward_ex(const void *X, const void *W_Q, const void *W_K, cons
                    int dtype, void *stream, void *workspace, size_t workspace_bytes);
 
 /* Bytes of device workspace one call needs (0 if the sizes are invalid): the folded
- * weights (or, on the unfolded route, the head projections Y) + stacked Qbar, Kbar, Vbar
+ * weights (the slice-major weights on the unfolded route) + stacked Qbar, Kbar, Vbar
  * + Pbar, each 256-byte aligned, + a 256-byte control slot (the call's own attention work
  * counter, reset on the stream by every call). */
 IHA_API size_t iha_workspace_bytes(int B, int N, int H, int d, int P, int dtype);
@@ -201,8 +201,9 @@ IHA_API int iha_project(const void *X, const void *Wt, int B, int N, int H, int 
                 int dtype, void *QKV, void *stream);
 
 /* Which way steps 1+2 run for this shape (what iha_forward_ex does):
- *   1 = unfolded: iha_project_heads then iha_mix_heads (bf16, P >= 2, H <= 16, H*P <= 128 --
- *       the projection GEMM then does 1/P of the folded GEMM's work);
+ *   1 = unfolded: iha_slice_weights then iha_project_mix, the head projections with the
+ *       mixing in the GEMM epilogue (bf16, P >= 2, H <= 16, H*P <= 128 -- the GEMM does 1/P
+ *       of the folded GEMM's work, and the head projections never reach memory);
  *   0 = folded:   iha_fold_weights then iha_project;
  *  -1 = invalid sizes or dtype. */
 IHA_API int iha_projection_route(int H, int d, int P, int dtype);
@@ -212,6 +213,23 @@ IHA_API int iha_projection_route(int H, int d, int P, int dtype);
  * m*d + c holds (X W_s^(m))[t][c]).  The weights are read as stored. */
 IHA_API int iha_project_heads(const void *X, const void *W_Q, const void *W_K, const void *W_V,
                               int B, int N, int H, int d, int dtype, void *Y, void *stream);
+
+/* Steps 1+2 and the stacking in one kernel (bf16 only, H <= 16, H*P <= 128, d in {64, 128};
+ * IHA_ERR_UNSUPPORTED otherwise): the head projections X W_s^(m) on the tensor cores with the
+ * mixing S~_{h,j} = sum_m alpha_s[m,h,j] (X W_s^(m)) in fp32 in the GEMM epilogue, written into
+ * QKV (layout as for iha_project; 32-byte aligned, IHA_ERR_INVALID_ARG otherwise).  It reads
+ * the weights slice-major, as iha_slice_weights writes them:
+ *   Wp [3][D][S]: for s = Q, K, V, column sl*C + m*CW + c of row k holds W_s[k][m*d + sl*CW + c],
+ *   CW = the widest of 64, 32, 16 with H*CW <= 256 and CW <= d, C = H*CW rounded up to a
+ *   multiple of 64 (padding columns zero), S = (d/CW)*C; iha_sliced_weights_bytes(H, d, dtype)
+ *   bytes, 16-byte aligned.
+ * iha_forward_ex runs iha_slice_weights then iha_project_mix when iha_projection_route() is 1. */
+IHA_API size_t iha_sliced_weights_bytes(int H, int d, int dtype);
+IHA_API int iha_slice_weights(const void *W_Q, const void *W_K, const void *W_V, int H, int d, int dtype,
+                              void *Wp, void *stream);
+IHA_API int iha_project_mix(const void *X, const void *Wp,
+                            const float *alpha_Q, const float *alpha_K, const float *alpha_V,
+                            int B, int N, int H, int d, int P, int dtype, void *QKV, void *stream);
 
 /* Steps 1+2, second half, and the stacking (bf16 only, H <= 16, H*P <= 128): the mixing
  * S~_{h,j} = sum_m alpha_s[m,h,j] (X W_s^(m)) of Y into QKV (layout as for iha_project).

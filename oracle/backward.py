@@ -94,3 +94,37 @@ def backward(inputs: dict, dO, *, H, d, P, mask_mode=0, window=0):
     out = forward(*(leaves[k] for k in PARAMS), H=H, d=d, P=P, mask_mode=mask_mode, window=window)
     grads = torch.autograd.grad(out, [leaves[k] for k in PARAMS], torch.as_tensor(dO, dtype=torch.float64))
     return {k: g.detach() for k, g in zip(PARAMS, grads)}
+
+
+def gram_term_scale(inputs: dict, dO, *, H, d, P, mask_mode=0, window=0):
+    """The size of the individual terms of the four gradients that are sums over every token
+    and column of a product of two stored tensors (chain rule through Algorithm 1's mixing and
+    contraction steps):
+        dalpha_s[m,h,j] = sum_{t,c} (X W_s^(m))[t,c] * dS~_s[h,j][t,c]
+        dR[h, h'P+j]    = sum_{t,c} dO_h[t,c] * P_{h',j}[t,c]
+    For each output element, sqrt(sum over (t,c) of term^2): the standard deviation of the sum's
+    error when each term carries an independent relative error of 1 (the factors are stored in
+    bfloat16).  Where the terms cancel, the result can be far smaller than this scale, and a
+    tolerance relative to the result alone is ill-conditioned.  float64; keys alpha_Q, alpha_K,
+    alpha_V, R (the other keys are not such sums and are absent)."""
+    f = {k: torch.as_tensor(inputs[k], dtype=torch.float64) for k in PARAMS}
+    X = f["X"]
+    B, N, D_ = X.shape
+    ok = _allowed(N, P, mask_mode, window)
+    Y = {s: (X @ f["W_" + s]).reshape(B, N, H, d) for s in ("Q", "K", "V")}
+    mixed = {s: torch.einsum("mhj,btmc->bhjtc", f["alpha_" + s], Y[s]).reshape(B, H, P * N, d).requires_grad_(True)
+             for s in ("Q", "K", "V")}
+    S = (mixed["Q"] @ mixed["K"].transpose(-1, -2)) / math.sqrt(d)
+    A = torch.softmax(S.masked_fill(~ok, float("-inf")), dim=-1)
+    Pb = A @ mixed["V"]
+    Pu = Pb.reshape(B, H, P, N, d).reshape(B, H * P, N, d)
+    O = torch.einsum("hk,bktc->bthc", f["R"], Pu).reshape(B, N, H * d)
+    dOt = torch.as_tensor(dO, dtype=torch.float64)
+    g = torch.autograd.grad(O, [mixed[s] for s in ("Q", "K", "V")], dOt)
+    out = {}
+    for s, gs in zip(("Q", "K", "V"), g):
+        dS = gs.detach().reshape(B, H, P, N, d)                    # [b, h, j, t, c]
+        out["alpha_" + s] = torch.einsum("btmc,bhjtc->mhj", Y[s] ** 2, dS ** 2).sqrt()
+    Pd = Pu.detach().reshape(B, H * P, N, d)
+    out["R"] = torch.einsum("bthc,bktc->hk", dOt.reshape(B, N, H, d) ** 2, Pd ** 2).sqrt()
+    return out

@@ -52,8 +52,9 @@ def test_workspace_bytes(iha):
     D = H * d
     al = lambda x: (x + 255) // 256 * 256
     for dtype, es in ((iha.IHA_DTYPE_BF16, 2), (iha.IHA_DTYPE_F32, 4)):
-        # first region: head projections Y on the unfolded route, folded weights otherwise
-        first = 3 * B * N * D * es if iha.iha_projection_route(H, d, P, dtype) == 1 else 3 * H * P * d * D * es
+        # first region: folded weights, or the slice-major weights on the unfolded route
+        # (W_Q, W_K, W_V reordered: 3 D x D, no padding at 16 heads)
+        first = 3 * D * D * es if iha.iha_projection_route(H, d, P, dtype) == 1 else 3 * H * P * d * D * es
         # + the 256-byte control slot (the call's attention work counter)
         expect = al(first) + al(3 * B * H * N * P * d * es) + al(B * N * H * P * d * es) + 256
         assert iha.iha_workspace_bytes(B, N, H, d, P, dtype) == expect
@@ -102,6 +103,15 @@ def test_step_entry_points_reject_bad_arguments(iha):
     assert iha.iha_project_heads(FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 64, 0, FAKE) == 2
     assert iha.iha_mix_heads(FAKE, FAKE, FAKE, FAKE, 1, 8, 32, 64, 2, 1, FAKE) == 2
     assert iha.iha_mix_heads(FAKE, FAKE, FAKE, None, 1, 8, 2, 64, 2, 1, FAKE) == 1
+    assert iha.iha_project_mix(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 64, 2, 1, FAKE) == 1
+    assert iha.iha_project_mix(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 32, 64, 2, 1, FAKE) == 2   # H > 16
+    assert iha.iha_project_mix(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 64, 2, 0, FAKE) == 2    # fp32
+    assert iha.iha_project_mix(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 64, 2, 1, FAKE + 16) == 1   # QKV not 32-aligned
+    assert iha.iha_slice_weights(FAKE, None, FAKE, 2, 64, 1, FAKE) == 1
+    assert iha.iha_slice_weights(FAKE, FAKE, FAKE, 32, 64, 1, FAKE) == 2
+    assert iha.iha_sliced_weights_bytes(16, 128, 1) == 3 * 2048 * 2048 * 2   # 16 heads: no padding
+    assert iha.iha_sliced_weights_bytes(5, 64, 1) == 3 * 320 * 2 * 192 * 2   # 5 x 32 columns padded to 192
+    assert iha.iha_sliced_weights_bytes(16, 128, 0) == 0
     assert iha.iha_fold_weights(None, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 64, 2, 1, FAKE) == 1
     assert iha.iha_project(FAKE, FAKE, 1, 8, 2, 64, 0, 1, FAKE) == 1
     assert iha.iha_attention(FAKE, 1, 8, 2, 64, 2, 2, 0, 1, FAKE) == 1

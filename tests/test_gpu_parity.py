@@ -260,8 +260,9 @@ def test_repeated_tokens_gpu(iha):
 
 @pytest.mark.parametrize("P", [1, 2, 3])
 def test_step_entry_points_match_forward(iha, P):
-    """Both ways of computing steps 1+2 (fold alpha into W, or project the heads and mix)
-    match the oracle; the route iha_forward_ex takes gives its bits exactly."""
+    """Every way of computing steps 1+2 (fold alpha into W; project the heads, then mix; the
+    projection with the mixing in its epilogue) matches the oracle; the route iha_forward_ex
+    takes gives its bits exactly."""
     w = W("steps", B=2, N=260, H=4, d=64, P=P, mask_mode=WN, window=40, dtype="bf16", seed=43)
     inp = gi.make_inputs(w)
     dinp = to_dev(inp)
@@ -271,7 +272,7 @@ def test_step_entry_points_match_forward(iha, P):
     assert route == (1 if P >= 2 else 0)
     s = torch.cuda.current_stream()
     ora = oracle_rows(w, inp)
-    for r in (0, 1):
+    for r in (0, 1, 2):
         QKV = torch.empty(3, w.B, w.H, w.N * w.P, w.d, dtype=torch.bfloat16, device="cuda:0")
         Pbar = torch.empty(w.B, w.N, w.H, w.P, w.d, dtype=torch.bfloat16, device="cuda:0")
         out = torch.empty_like(ref)
@@ -280,6 +281,11 @@ def test_step_entry_points_match_forward(iha, P):
             iha.check(iha.iha_fold_weights(dinp["W_Q"], dinp["W_K"], dinp["W_V"], dinp["alpha_Q"],
                                            dinp["alpha_K"], dinp["alpha_V"], w.H, w.d, w.P, dt, Wt, s))
             iha.check(iha.iha_project(dinp["X"], Wt, w.B, w.N, w.H, w.d, w.P, dt, QKV, s))
+        elif r == 2:
+            Wp = torch.empty(iha.iha_sliced_weights_bytes(w.H, w.d, dt), dtype=torch.uint8, device="cuda:0")
+            iha.check(iha.iha_slice_weights(dinp["W_Q"], dinp["W_K"], dinp["W_V"], w.H, w.d, dt, Wp, s))
+            iha.check(iha.iha_project_mix(dinp["X"], Wp, dinp["alpha_Q"], dinp["alpha_K"], dinp["alpha_V"], w.B, w.N,
+                                          w.H, w.d, w.P, dt, QKV, s))
         else:
             Y = torch.empty(w.B * w.N, 3 * w.D, dtype=torch.bfloat16, device="cuda:0")
             iha.check(iha.iha_project_heads(dinp["X"], dinp["W_Q"], dinp["W_K"], dinp["W_V"], w.B, w.N, w.H,
@@ -296,7 +302,7 @@ def test_step_entry_points_match_forward(iha, P):
         iha.check(iha.iha_contract(Pbar, dinp["R"], w.B, w.N, w.H, w.d, w.P, dt, out, s))
         torch.cuda.synchronize()
         assert_parity(w, out.double().cpu().numpy(), ora)
-        if r == route:
+        if (r == 2 and route == 1) or (r == 0 and route == 0):
             assert torch.equal(out, ref)
         if r == 0:
             # the folded weights are the mixing sum (checked in float64 on a slice)
@@ -305,6 +311,45 @@ def test_step_entry_points_match_forward(iha, P):
             col = sum(f["alpha_K"][m, h, j] * f["W_K"][:, m * w.d + c] for m in range(w.H))
             row = Wt[1 * w.H * w.P * w.d + h * w.P * w.d + j * w.d + c].double().cpu().numpy()
             np.testing.assert_allclose(row, col, rtol=1e-2, atol=1e-2 * np.abs(col).max())
+
+
+@pytest.mark.parametrize("B,N,H,d,P", [
+    (1, 200, 16, 128, 4),   # 16-column slices (32-byte swizzle), the workloads' head count
+    (2, 130, 16, 64, 2),    # ragged last token tile
+    (1, 77, 8, 128, 2),     # 32-column slices (64-byte swizzle)
+    (1, 300, 5, 64, 3),     # N = 160, H*P = 15 (not a multiple of 4)
+    (2, 65, 3, 128, 3),     # 64-column slices (128-byte swizzle), N = 192
+    (1, 40, 1, 64, 4),      # one head
+    (1, 1, 4, 128, 2),      # a single token
+    # whole 32-token groups: results leave through shared-memory staging and TMA stores
+    (1, 256, 16, 128, 4), (2, 96, 16, 64, 2), (1, 64, 8, 128, 2), (3, 32, 4, 64, 1), (1, 64, 2, 128, 8)])
+def test_project_mix_matches_definition(iha, B, N, H, d, P):
+    """iha_project_mix writes S~_{h,j} = sum_m alpha_s[m,h,j] X W_s^(m) (Algorithm 1, the mixing
+    step) at stacked row t*P + j of head h, for every element: against the sums in float64,
+    within the rounding of the stored type (bf16 Qbar/Kbar, f16 Vbar)."""
+    w = W("pm", B=B, N=N, H=H, d=d, P=P, mask_mode=C, window=0, dtype="bf16", seed=46)
+    inp = gi.make_inputs(w)
+    dinp = to_dev(inp)
+    QKV = torch.full((3, B, H, N * P, d), float("nan"), dtype=torch.bfloat16, device="cuda:0")
+    dt = iha.IHA_DTYPE_BF16
+    Wp = torch.full((iha.iha_sliced_weights_bytes(H, d, dt),), 0xFF, dtype=torch.uint8, device="cuda:0")
+    iha.check(iha.iha_slice_weights(dinp["W_Q"], dinp["W_K"], dinp["W_V"], H, d, dt, Wp, None))
+    iha.check(iha.iha_project_mix(dinp["X"], Wp, dinp["alpha_Q"], dinp["alpha_K"], dinp["alpha_V"], B, N, H, d, P,
+                                  dt, QKV, None))
+    torch.cuda.synchronize()
+    rc, code = iha.iha_check_device_status()
+    assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
+    f = gi.as_f64(inp)
+    X = f["X"].reshape(B, N, H * d)
+    for si, (wn, an) in enumerate((("W_Q", "alpha_Q"), ("W_K", "alpha_K"), ("W_V", "alpha_V"))):
+        Yh = (X @ f[wn]).reshape(B, N, H, d)                      # X W_s^(m), head m
+        ref = np.einsum("mhj,bnmc->bhnjc", f[an], Yh).reshape(B, H, N * P, d)
+        got = QKV[si].view(torch.float16) if si == 2 else QKV[si]
+        got = got.double().cpu().numpy()
+        assert np.isfinite(got).all(), f"set {si}: unwritten elements"
+        err = np.abs(got - ref)
+        bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -12 * np.abs(ref).max()
+        assert (err <= bound).all(), f"set {si}: worst excess {float((err - bound).max()):.3e}"
 
 
 def test_caller_workspace_and_default_stream_entry(iha):
@@ -552,6 +597,12 @@ BWD_TOL = 3e-2   # RMS(err) <= BWD_TOL * RMS(ref) per gradient tensor ...
 # dPbar . Pbar is formed from the bf16 attention output (relative error ~2^-8), and
 # dS = P (dP - D) inherits that error at the size of P * D even where dP - D cancels
 CANCEL_TOL = 2.0 ** -6
+# ... and, for the four gradients that are sums over all tokens and columns of a product of two
+# bf16-stored tensors (dalpha_Q/K/V, dR), + GRAM_TOL * RMS(sqrt(sum of the squared terms)): the
+# terms can cancel to a result far below their size, so an error relative to the result alone
+# is ill-conditioned there; per-term relative errors of about 2^-8 (bf16 storage of both
+# factors) give a sum error of about 2^-8 * sqrt(sum term^2), allowed four times over
+GRAM_TOL = 2.0 ** -6
 
 
 @pytest.mark.parametrize("B,N,H,d,P,mode,window", [
@@ -587,12 +638,15 @@ def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
     assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
     ref = bwd.backward(gi.as_f64(inp), dO.double(), H=H, d=d, P=P, mask_mode=mode, window=window)
     scale = bwd.cancellation_scale(gi.as_f64(inp), dO.double(), H=H, d=d, P=P, mask_mode=mode, window=window)
+    terms = bwd.gram_term_scale(gi.as_f64(inp), dO.double(), H=H, d=d, P=P, mask_mode=mode, window=window)
     for k in bwd.PARAMS:
         got = out[k].double().cpu().numpy()
         r = ref[k].numpy()
         assert np.isfinite(got).all(), k
         err = rms(got - r)
         bound = BWD_TOL * rms(r) + CANCEL_TOL * rms(scale[k].numpy())
+        if k in terms:
+            bound += GRAM_TOL * rms(terms[k].numpy())
         assert err <= bound, f"{k}: rms err {err:.3g} vs rms ref {rms(r):.3g}, bound {bound:.3g}"
 
 

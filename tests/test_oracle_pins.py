@@ -580,3 +580,43 @@ def test_cancellation_scale_linear_in_dO(case):
                                    atol=1e-9 * (1 + np.abs(s1[k].numpy()).max()))
     for k in ("W_V", "alpha_V", "R"):
         assert not s1[k].numpy().any(), k
+
+
+def test_gram_term_scale_closed_form_and_bounds():
+    """gram_term_scale, the tolerance scale of the four token-sum gradients:
+    - one token, one head, P = 1, d columns: dR = sum_c dO_c Pbar_c with Pbar = v (the one
+      readable value, p = 1) = alpha_V x W_V, so its scale is sqrt(sum_c (dO_c v_c)^2); dalpha_V
+      = sum_c (x W_V)_c dv_c with dv = R dO, scale sqrt(sum_c ((x W_V)_c R dO_c)^2);
+    - at any shape each gradient is at most sqrt(number of terms) times its scale
+      (Cauchy-Schwarz), the scale is linear in |dO| and, for dR, independent of R."""
+    from oracle import backward as bwd
+    rng = np.random.default_rng(17)
+    d = 5
+    p = rand_problem(rng, 1, 1, 1, d, 1)
+    dO = rng.standard_normal((1, 1, d))
+    sc = bwd.gram_term_scale(p, dO, H=1, d=d, P=1, mask_mode=1)
+    x = p["X"][0, 0]
+    yv = x @ p["W_V"]
+    v = p["alpha_V"][0, 0, 0] * yv
+    r = p["R"][0, 0]
+    np.testing.assert_allclose(float(sc["R"].numpy()[0, 0]), np.sqrt(np.sum((dO[0, 0] * v) ** 2)), rtol=1e-12)
+    np.testing.assert_allclose(float(sc["alpha_V"].numpy()[0, 0, 0]), np.sqrt(np.sum((yv * r * dO[0, 0]) ** 2)),
+                               rtol=1e-12)
+    for case in BWD_CASES[:3]:
+        B, N, H, d, P, mode, w = case
+        rng = np.random.default_rng(99 + N)
+        p = rand_problem(rng, B, N, H, d, P)
+        dO = rng.standard_normal((B, N, H * d))
+        sc = bwd.gram_term_scale(p, dO, H=H, d=d, P=P, mask_mode=mode, window=w)
+        ref = bwd.backward(p, dO, H=H, d=d, P=P, mask_mode=mode, window=w)
+        n = B * N * d
+        for k, s in sc.items():
+            assert (np.abs(ref[k].numpy()) <= np.sqrt(n) * s.numpy() * (1 + 1e-9) + 1e-12).all(), k
+        sc3 = bwd.gram_term_scale(p, -3.0 * dO, H=H, d=d, P=P, mask_mode=mode, window=w)
+        for k in sc:
+            np.testing.assert_allclose(sc3[k].numpy(), 3.0 * sc[k].numpy(), rtol=1e-10, atol=1e-300)
+        p2 = dict(p)
+        p2["R"] = 2.0 * p["R"]
+        sc_r = bwd.gram_term_scale(p2, dO, H=H, d=d, P=P, mask_mode=mode, window=w)
+        np.testing.assert_allclose(sc_r["R"].numpy(), sc["R"].numpy(), rtol=1e-10, atol=1e-300)
+        np.testing.assert_allclose(sc_r["alpha_V"].numpy(), 2.0 * sc["alpha_V"].numpy(), rtol=1e-10, atol=1e-300)

@@ -36,7 +36,8 @@ EXPORTED = ("iha_forward", "iha_forward_ex", "iha_workspace_bytes", "iha_error_s
             "iha_contract", "iha_forward_noalloc", "iha_projection_route", "iha_project_heads",
             "iha_mix_heads", "iha_stack_workspace_bytes", "iha_forward_stack", "iha_prefill",
             "iha_decode_workspace_bytes", "iha_decode_step", "iha_backward_workspace_bytes", "iha_backward",
-            "iha_forward_train", "iha_backward_saved")
+            "iha_forward_train", "iha_backward_saved", "iha_project_mix", "iha_slice_weights",
+            "iha_sliced_weights_bytes")
 
 IHA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -85,6 +86,12 @@ def _load():
     lib.iha_project_heads.restype = i
     lib.iha_mix_heads.argtypes = [vp] + [fp] * 3 + [i] * 6 + [vp, vp]
     lib.iha_mix_heads.restype = i
+    lib.iha_project_mix.argtypes = [vp, vp] + [fp] * 3 + [i] * 6 + [vp, vp]
+    lib.iha_project_mix.restype = i
+    lib.iha_slice_weights.argtypes = [vp] * 3 + [i] * 3 + [vp, vp]
+    lib.iha_slice_weights.restype = i
+    lib.iha_sliced_weights_bytes.argtypes = [i] * 3
+    lib.iha_sliced_weights_bytes.restype = sz
     lib.iha_forward_noalloc.argtypes = [vp] * 4 + [fp] * 4 + shape + [i, i, vp, i, vp]
     lib.iha_forward_noalloc.restype = i
     ip = ctypes.POINTER(i)
@@ -187,6 +194,19 @@ def iha_projection_route(H, d, P, dtype) -> int:
 
 def iha_project_heads(X, W_Q, W_K, W_V, B, N, H, d, dtype, Y, stream=None) -> int:
     return _lib.iha_project_heads(_p(X), _p(W_Q), _p(W_K), _p(W_V), B, N, H, d, dtype, _p(Y), _s(stream))
+
+
+def iha_sliced_weights_bytes(H, d, dtype) -> int:
+    return int(_lib.iha_sliced_weights_bytes(H, d, dtype))
+
+
+def iha_slice_weights(W_Q, W_K, W_V, H, d, dtype, Wp, stream=None) -> int:
+    return _lib.iha_slice_weights(_p(W_Q), _p(W_K), _p(W_V), H, d, dtype, _p(Wp), _s(stream))
+
+
+def iha_project_mix(X, Wp, alpha_Q, alpha_K, alpha_V, B, N, H, d, P, dtype, QKV, stream=None) -> int:
+    return _lib.iha_project_mix(_p(X), _p(Wp), _p(alpha_Q), _p(alpha_K), _p(alpha_V), B, N, H, d, P, dtype,
+                                _p(QKV), _s(stream))
 
 
 def iha_mix_heads(Y, alpha_Q, alpha_K, alpha_V, B, N, H, d, P, dtype, QKV, stream=None) -> int:

@@ -36,6 +36,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompil
 REG_CONTRACTS = {
     "attn_fwd_tc": ("k_attention_tc.cu", "AT_LAUNCH_REGS"),
     "bwd_attn_tc": ("k_backward_tc.cu", "BA_LAUNCH_REGS"),
+    "proj_mix_tc": ("k_project_mix_tc.cu", "PM_LAUNCH_REGS"),
 }
 
 

@@ -85,9 +85,8 @@ struct WsLayout {
 static WsLayout ws_layout(const Shape &sh, int dtype) {
     const size_t es = elem_size(dtype);
     WsLayout w;
-    w.wt = 0;   // folded weights Wt, or the head projections Y on the unfolded route
-    const size_t first = unfolded_route(sh, dtype) ? (size_t)sh.B * sh.N * 3 * (size_t)sh.D() * es
-                                                   : (size_t)sh.wt_rows() * (size_t)sh.D() * es;
+    w.wt = 0;   // folded weights Wt, or the slice-major weights Wp on the unfolded route
+    const size_t first = unfolded_route(sh, dtype) ? sliced_weights_bytes(sh) : (size_t)sh.wt_rows() * (size_t)sh.D() * es;
     w.qkv = align256(first);
     w.pbar = w.qkv + align256(3 * (size_t)sh.qkv_elems() * es);
     w.ctr = w.pbar + align256((size_t)sh.B * sh.N * sh.H * sh.P * sh.d * es);
@@ -114,8 +113,9 @@ static int run_forward(const void *X, const void *WQ, const void *WK, const void
     unsigned int *ticket = reinterpret_cast<unsigned int *>(ws + lay.ctr);
     cudaError_t e;
     if (unfolded_route(sh, dtype)) {
-        e = launch_project_heads(X, WQ, WK, WV, sh, Wt, st, status);   // Y in the first region
-        if (e == cudaSuccess) e = launch_mix(Wt, aQ, aK, aV, sh, QKV, st, status);
+        e = launch_slice_weights(WQ, WK, WV, sh, Wt, st);
+        if (e == cudaSuccess)
+            e = launch_project_mix(X, Wt, aQ, aK, aV, sh, 0, (long long)sh.B * sh.N, QKV, nullptr, st, status);
     } else {
         e = launch_fold(WQ, WK, WV, aQ, aK, aV, sh, dtype, Wt, st);
         if (e == cudaSuccess) e = launch_project(X, Wt, sh, dtype, QKV, st, status);
@@ -150,8 +150,8 @@ static cudaStream_t *copy_streams() {
 }
 
 // iha_forward_host on the unfolded bf16 route with the copies overlapped with the work:
-// W and X go up on the two copy streams, X in FH_CHUNKS token chunks, and the head projection
-// of a chunk starts as soon as that chunk (and W) has landed; the contraction runs in token
+// W and X go up on the two copy streams, X in FH_CHUNKS token chunks, and the projection and
+// mixing of a chunk start as soon as that chunk (and W and alpha) have landed; the contraction runs in token
 // chunks and each chunk's output goes down while the next is computed.  `st` waits for both
 // copy streams at the end, so the call completes on `st` as the plain sequence does.
 constexpr int FH_CHUNKS = 4;
@@ -163,10 +163,10 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
     if (!cs) return IHA_ERR_CUDA;
     const long long T = (long long)sh.B * sh.N, D = sh.D();
     const size_t wb = (size_t)D * D * 2, ab = (size_t)sh.H * sh.H * sh.P * sizeof(float);
-    const size_t row_x = (size_t)D * 2, row_y = 3 * (size_t)D * 2, row_p = (size_t)sh.H * sh.P * sh.d * 2;
+    const size_t row_x = (size_t)D * 2, row_p = (size_t)sh.H * sh.P * sh.d * 2;
     const WsLayout lay = ws_layout(sh, IHA_DTYPE_BF16);
     uint8_t *w8 = static_cast<uint8_t *>(ws);
-    uint8_t *Y = w8 + lay.wt, *QKV = w8 + lay.qkv, *Pbar = w8 + lay.pbar;
+    uint8_t *Wp = w8 + lay.wt, *QKV = w8 + lay.qkv, *Pbar = w8 + lay.pbar;
     unsigned int *ticket = reinterpret_cast<unsigned int *>(w8 + lay.ctr);
     int *status = status_ptr();
     // events: 0 start, 1-2 W ready (one per copy stream), 3.. X chunks, then contraction chunks,
@@ -203,18 +203,17 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
                                 cudaMemcpyHostToDevice, cs[i & 1]);
         if (e == cudaSuccess) e = cudaEventRecord(ev[3 + i], cs[i & 1]);
     }
-    // head projections chunk by chunk
+    // projection and mixing chunk by chunk, straight into the stacked layout
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[1], 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[2], 0);
+    if (e == cudaSuccess) e = launch_slice_weights(dWQ, dWK, dWV, sh, Wp, st);
     for (int i = 0; i < FH_CHUNKS && e == cudaSuccess; ++i) {
         long long r0, r1;
         chunk(i, r0, r1);
         e = cudaStreamWaitEvent(st, ev[3 + i], 0);
         if (e == cudaSuccess && r1 > r0)
-            e = launch_project_heads(static_cast<uint8_t *>(dX) + r0 * row_x, dWQ, dWK, dWV,
-                                     Shape{1, (int)(r1 - r0), sh.H, sh.d, sh.P}, Y + r0 * row_y, st, status);
+            e = launch_project_mix(dX, Wp, daQ, daK, daV, sh, r0, r1 - r0, QKV, nullptr, st, status);
     }
-    if (e == cudaSuccess) e = launch_mix(Y, daQ, daK, daV, sh, QKV, st, status);
     if (e == cudaSuccess)
         e = launch_attention(QKV, sh, mask_mode, window, IHA_DTYPE_BF16, Pbar, st, status, ticket);
     // contraction chunk by chunk, each chunk's output copied down as soon as it is done
@@ -463,6 +462,34 @@ int iha_project_heads(const void *X, const void *W_Q, const void *W_K, const voi
     if (dtype != IHA_DTYPE_BF16) return IHA_ERR_UNSUPPORTED;
     return cuda_status(launch_project_heads(X, W_Q, W_K, W_V, Shape{B, N, H, d, 1}, Y,
                                             static_cast<cudaStream_t>(stream), status_ptr()));
+}
+
+size_t iha_sliced_weights_bytes(int H, int d, int dtype) {
+    if (validate_shape(1, 1, H, d, 1, dtype) != IHA_OK || dtype != IHA_DTYPE_BF16) return 0;
+    const Shape sh{1, 1, H, d, 1};
+    return project_mix_supported(sh) ? sliced_weights_bytes(sh) : 0;
+}
+
+int iha_slice_weights(const void *W_Q, const void *W_K, const void *W_V, int H, int d, int dtype, void *Wp,
+                      void *stream) {
+    if (!W_Q || !W_K || !W_V || !Wp) return IHA_ERR_INVALID_ARG;
+    if (iha_sliced_weights_bytes(H, d, dtype) == 0) return IHA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(W_Q) | reinterpret_cast<uintptr_t>(W_K) | reinterpret_cast<uintptr_t>(W_V) |
+         reinterpret_cast<uintptr_t>(Wp)) & 15)
+        return IHA_ERR_INVALID_ARG;
+    return cuda_status(launch_slice_weights(W_Q, W_K, W_V, Shape{1, 1, H, d, 1}, Wp, static_cast<cudaStream_t>(stream)));
+}
+
+int iha_project_mix(const void *X, const void *Wp, const float *alpha_Q, const float *alpha_K, const float *alpha_V,
+                    int B, int N, int H, int d, int P, int dtype, void *QKV, void *stream) {
+    if (!X || !Wp || !alpha_Q || !alpha_K || !alpha_V || !QKV) return IHA_ERR_INVALID_ARG;
+    const int rc = validate_shape(B, N, H, d, P, dtype);
+    if (rc != IHA_OK) return rc;
+    const Shape sh{B, N, H, d, P};
+    if (dtype != IHA_DTYPE_BF16 || !project_mix_supported(sh)) return IHA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(QKV) & 31) || (reinterpret_cast<uintptr_t>(Wp) & 15)) return IHA_ERR_INVALID_ARG;
+    return cuda_status(launch_project_mix(X, Wp, alpha_Q, alpha_K, alpha_V, sh, 0, (long long)B * N, QKV, nullptr,
+                                          static_cast<cudaStream_t>(stream), status_ptr()));
 }
 
 int iha_mix_heads(const void *Y, const float *alpha_Q, const float *alpha_K, const float *alpha_V, int B, int N, int H,

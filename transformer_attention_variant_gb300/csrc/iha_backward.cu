@@ -4,7 +4,8 @@
 // pieces in the backward workspace) + iha_backward_saved (the gradients from them).
 //
 // Step order (one stream, bf16 tensors, fp32 arithmetic):
-//   forward pieces:  Y = X [W_Q|W_K|W_V];  Q~K~V~ = mix(Y);  Pbar, lse = attention(Q~, K~, V~)
+//   forward pieces:  Y = X [W_Q|W_K|W_V] and Q~K~V~ = mix(Y) (one kernel: the mixing runs in
+//                    the projection GEMM's epilogue);  Pbar, lse = attention(Q~, K~, V~)
 //   dPbar  = the mixing of dO with R in alpha's place (stacked; dPbar_{h',j} = sum_h R[h,h'P+j] dO_h)
 //   dR     = sum over tokens and columns of dO_h Pbar_k                 (gram_tc)
 //   D      = rowdot(dPbar, Pbar)                                       (rowdot)
@@ -35,7 +36,7 @@ cudaError_t launch_bwd_dw_tc(const void *X, const void *const dY[3], long long T
                              cudaStream_t st, int *status);
 
 struct BwdLayout {
-    size_t y, qkv, vb, pbar, lse, dpst, dv, ds, dy, part, ctr, total;
+    size_t y, wp, qkv, vb, pbar, lse, dpst, dv, ds, dy, part, ctr, total;
     size_t ld_bytes;   // lse and D: [B*H][bwd_ld_stride(L)] floats each
 };
 
@@ -48,6 +49,7 @@ static BwdLayout bwd_layout(const Shape &sh) {
     BwdLayout l{};
     size_t o = 0;
     l.y = o;    o += al256(3 * T * D * 2);
+    l.wp = o;   o += al256(sliced_weights_bytes(sh));
     l.qkv = o;  o += al256(3 * (size_t)sh.qkv_elems() * 2);
     l.vb = o;   o += al256((size_t)sh.qkv_elems() * 2);
     l.pbar = o; o += al256(T * HP * sh.d * 2);
@@ -99,8 +101,11 @@ static cudaError_t bwd_forward_pieces(const void *X, const void *W_Q, const void
     const int ld = bwd_ld_stride(sh.L());
     cudaError_t e = cudaMemsetAsync(lse, 0, lay.ld_bytes, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(Dv, 0, lay.ld_bytes, st);
-    if (e == cudaSuccess) e = launch_project_heads(X, W_Q, W_K, W_V, sh, Y, st, status);
-    if (e == cudaSuccess) e = launch_mix(Y, alpha_Q, alpha_K, alpha_V, sh, QKV, st, status);
+    // Q~ K~ V~ as the forward computes them, and the head projections Y for dalpha
+    if (e == cudaSuccess) e = launch_slice_weights(W_Q, W_K, W_V, sh, ws + lay.wp, st);
+    if (e == cudaSuccess)
+        e = launch_project_mix(X, ws + lay.wp, alpha_Q, alpha_K, alpha_V, sh, 0, (long long)sh.B * sh.N, QKV, Y, st,
+                               status);
     if (e == cudaSuccess)
         e = launch_attention_lse(QKV, sh, mask_mode, window, IHA_DTYPE_BF16, Pbar, lse, ld, st, status,
                                  reinterpret_cast<unsigned int *>(ws + lay.ctr));

@@ -92,12 +92,27 @@ cudaError_t launch_project(const void *X, const void *Wt, const Shape &sh, int d
 cudaError_t launch_project_heads(const void *X, const void *WQ, const void *WK, const void *WV, const Shape &sh,
                                  void *Y, cudaStream_t st, int *status);
 
+// Steps 1+2 fused (bf16; project_mix_supported): the head projections on the tensor cores
+// with the pseudo-head mixing in the GEMM epilogue.  launch_slice_weights first writes
+// W_Q, W_K, W_V slice-major into Wp (sliced_weights_bytes(sh) bytes, 16-byte aligned);
+// launch_project_mix then maps token rows [tok0, tok0 + ntok) of X [B*N][D] into the stacked
+// QKV [3][B][H][N*P][d] (bf16 Qbar/Kbar, f16 Vbar; 32-byte aligned) and, when Y is not NULL,
+// writes the head projections Y [B*N][3][H*d] bf16 too.
+bool project_mix_supported(const Shape &sh);
+size_t sliced_weights_bytes(const Shape &sh);
+cudaError_t launch_slice_weights(const void *WQ, const void *WK, const void *WV, const Shape &sh, void *Wp,
+                                 cudaStream_t st);
+cudaError_t launch_project_mix(const void *X, const void *Wp, const float *aQ, const float *aK, const float *aV,
+                               const Shape &sh, long long tok0, long long ntok, void *QKV, void *Y, cudaStream_t st,
+                               int *status);
+
 // The pseudo-head mixing of Y into the stacked QKV layout (bf16 Qbar/Kbar, f16 Vbar).
 cudaError_t launch_mix(const void *Y, const float *aQ, const float *aK, const float *aV, const Shape &sh, void *QKV,
                        cudaStream_t st, int *status);
 
-// Which way the library computes steps 1+2: true = project the heads then mix (bf16,
-// P >= 2, H <= 16, H*P <= 128: 1/P of the folded GEMM's work), false = fold alpha into W.
+// Which way the library computes steps 1+2: true = the head projections with the mixing in
+// the GEMM epilogue (bf16, P >= 2, H <= 16, H*P <= 128: 1/P of the folded GEMM's work),
+// false = fold alpha into W, then one GEMM.
 inline bool unfolded_route(const Shape &sh, int dtype) {
     return dtype == 1 && sh.P >= 2 && sh.H <= 16 && sh.H * sh.P <= 128;
 }

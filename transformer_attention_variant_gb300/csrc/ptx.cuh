@@ -204,6 +204,15 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap *map, uint64_t *ba
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y, int z,
+                                            int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
 // Prefetch a tile of a rank-3 tensor map into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
@@ -320,6 +329,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
     return d;
 }
 
+// The same fields for a 64-byte (layout 4) or 32-byte (layout 6) swizzle: atoms of 8 rows of
+// 64 or 32 bytes (512 / 256 bytes, aligned to that size).
+__device__ __forceinline__ uint64_t sdesc_swz(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              int swizzle_bytes) {
+    uint64_t d = 0;
+    d |= uint64_t((smem_addr >> 4) & 0x3FFF);
+    d |= uint64_t((lbo_bytes >> 4) & 0x3FFF) << 16;
+    d |= uint64_t((sbo_bytes >> 4) & 0x3FFF) << 32;
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(swizzle_bytes == 32 ? 6 : swizzle_bytes == 64 ? 4 : 2) << 61;
+    return d;
+}
+
 // The same descriptor as two 32-bit words: the high word (stride byte offset, version,
 // layout) is usually one constant for all operands of a kernel, and the low word (start,
 // leading byte offset) of start + off is the low word of start plus off >> 4 (addresses
@@ -405,6 +427,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// An empty statement that reads and rewrites 16 registers: placed after tmem_ld_wait() it
+// orders every later use of those registers (filled by an earlier tcgen05.ld) after the wait.
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]));
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------------------------
@@ -458,6 +488,13 @@ __device__ __forceinline__ void fadd2(float &d0, float &d1, float a0, float a1, 
     asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
     asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(R) : "l"(A), "l"(B));
     asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(R));
+}
+
+// One 32-byte store of eight 32-bit words (sm_100+); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a[0]), "r"(a[1]),
+                 "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3])
+                 : "memory");
 }
 
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }

@@ -30,9 +30,11 @@ inline EncodeTiledFn encode_tiled_fn() {
 
 // A rank-`rank` 16-bit tensor map (bf16, or f16 when f16 is true): dims[0] is the
 // contiguous dimension; strides_bytes[i] is the byte stride of dimension i+1.
-// Out-of-bounds elements of a load read as zero.
+// Out-of-bounds elements of a load read as zero.  swizzle_bytes: 128 (default), 64 or 32
+// (the box's inner extent must not exceed it), or 0 for none.
 inline bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                           const uint64_t *strides_bytes, const uint32_t *box, bool f16 = false) {
+                           const uint64_t *strides_bytes, const uint32_t *box, bool f16 = false,
+                           int swizzle_bytes = 128) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     cuuint64_t gdim[5], gstride[4];
@@ -44,7 +46,11 @@ inline bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const u
         if (i + 1 < rank) gstride[i] = strides_bytes[i];
     }
     CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), gdim,
-                    gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle_bytes == 0    ? CU_TENSOR_MAP_SWIZZLE_NONE
+                    : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                    : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                          : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
