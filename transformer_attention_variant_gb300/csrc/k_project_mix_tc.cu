@@ -423,25 +423,38 @@ size_t sliced_weights_bytes(const Shape &sh) {
 }
 
 // Wp_s[k][sl*SC + m*CW + c] = W_s[k][m*d + sl*CW + c] (zero in a slice's padding columns),
-// SC = slice columns; 16 bytes per thread.
+// SC = slice columns.  A thread moves 4 16-byte units of one output row (their loads in
+// flight together); consecutive threads write consecutive units.
+constexpr int SW_UNITS = 4;
 __global__ void __launch_bounds__(256)
 slice_weights_kernel(const uint4 *__restrict__ W0, const uint4 *__restrict__ W1, const uint4 *__restrict__ W2,
                      uint4 *__restrict__ Wp, int D, int H, int d, int cw, int sc, int nslices) {
     const long long row_out = (long long)nslices * sc / 8;   // 16-byte units per row of Wp_s
     const long long total = 3LL * D * row_out;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int s = (int)(i / (D * row_out));
-        const long long r = i % (D * row_out);
-        const int k = (int)(r / row_out), u = (int)(r % row_out);
-        const int sl = u / (sc / 8), n = (u % (sc / 8)) * 8;   // column within the slice
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (n < H * cw) {
-            const int m = n / cw, c = n % cw;
-            const uint4 *W = s == 0 ? W0 : (s == 1 ? W1 : W2);
-            v = W[((long long)k * H * d + (long long)m * d + sl * cw + c) / 8];
+    const long long stride = (long long)gridDim.x * blockDim.x * SW_UNITS;
+    for (long long i0 = (blockIdx.x * (long long)blockDim.x) * SW_UNITS + threadIdx.x; i0 < total; i0 += stride) {
+        uint4 v[SW_UNITS];
+#pragma unroll
+        for (int u = 0; u < SW_UNITS; ++u) {
+            const long long i = i0 + (long long)u * blockDim.x;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < total) {
+                const int s = (int)(i / (D * row_out));
+                const long long r = i % (D * row_out);
+                const int k = (int)(r / row_out), un = (int)(r % row_out);
+                const int sl = un / (sc / 8), n = (un % (sc / 8)) * 8;   // column within the slice
+                if (n < H * cw) {
+                    const int m = n / cw, c = n % cw;
+                    const uint4 *W = s == 0 ? W0 : (s == 1 ? W1 : W2);
+                    v[u] = W[((long long)k * H * d + (long long)m * d + sl * cw + c) / 8];
+                }
+            }
         }
-        Wp[i] = v;
+#pragma unroll
+        for (int u = 0; u < SW_UNITS; ++u) {
+            const long long i = i0 + (long long)u * blockDim.x;
+            if (i < total) Wp[i] = v[u];
+        }
     }
 }
 
@@ -453,8 +466,8 @@ cudaError_t launch_slice_weights(const void *WQ, const void *WK, const void *WV,
         return cudaErrorInvalidValue;
     const int cw = pm_slice_width(sh.H, sh.d), sc = pm_slice_cols(sh.H, cw);
     const long long units = 3LL * sh.D() * (sh.d / cw) * sc / 8;
-    long long blocks = (units + 255) / 256;
-    const long long cap = 8LL * device_sm_count();
+    long long blocks = (units + 256 * SW_UNITS - 1) / (256 * SW_UNITS);
+    const long long cap = 16LL * device_sm_count();
     if (blocks > cap) blocks = cap;
     slice_weights_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4 *>(WQ), static_cast<const uint4 *>(WK),
                                                            static_cast<const uint4 *>(WV), static_cast<uint4 *>(Wp),
