@@ -398,7 +398,7 @@ def run_gpu(args, w):
         roof = {"kernel": "proj_gemm_tc", "bound": "tensor", "achieved": ach, "peak": peaks["bf16"],
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16"],
                 "frac_of_sustained": ach / peaks["bf16_sustained"], "peak_source": peaks["source"]}
-        traffic_key = "project"
+        traffic_key = dom
     else:
         b = {"contract": wk["bytes_contract"], "fold": wk["bytes_fold"], "slice_weights": wk["bytes_slice"]}[dom]
         ach = b / (kmean[dom] * 1e-3) / 1e9
