@@ -36,6 +36,7 @@ enum WaitSite {
     kSiteProjMma = 2,
     kSiteProjEpilogue = 3,
     kSiteProjMmaAcc = 4,
+    kSiteProjStore = 5,
     kSiteAttnProducer = 16,
     kSiteAttnMmaQ = 17,
     kSiteAttnMmaK = 18,

@@ -59,11 +59,11 @@ static int pm_stages(int H, int HPp, bool tma_out) {
     return tma_out ? 3 : (pm_alpha_bytes(H, HPp) <= 24576 ? 4 : 3);
 }
 static int pm_smem(int H, int HPp, bool tma_out) {
-    return pm_stages(H, HPp, tma_out) * PM_STAGE_BYTES + pm_alpha_bytes(H, HPp) + (tma_out ? PM_OUT_BYTES : 0) + 256 +
+    return pm_stages(H, HPp, tma_out) * PM_STAGE_BYTES + pm_alpha_bytes(H, HPp) + (tma_out ? PM_OUT_BYTES : 0) + 512 +
            1024;
 }
-static_assert(4 * PM_STAGE_BYTES + 24576 + 1280 <= 232448 && 3 * PM_STAGE_BYTES + 49152 + 1280 <= 232448 &&
-                  3 * PM_STAGE_BYTES + 24576 + PM_OUT_BYTES + 1280 <= 232448,
+static_assert(4 * PM_STAGE_BYTES + 24576 + 1536 <= 232448 && 3 * PM_STAGE_BYTES + 49152 + 1536 <= 232448 &&
+                  3 * PM_STAGE_BYTES + 24576 + PM_OUT_BYTES + 1536 <= 232448,
               "shared memory");
 
 struct PMParams {
@@ -106,7 +106,9 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint64_t *empty = full + PM_MAX_STAGES;
     uint64_t *tfull = empty + PM_MAX_STAGES;
     uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    uint64_t *blk_full = tempty + 2;                       // [4 quarters][PM_OUT_BUFS] (TMA_OUT)
+    uint64_t *blk_free = blk_full + 4 * PM_OUT_BUFS;       // [4 quarters][PM_OUT_BUFS]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(blk_free + 4 * PM_OUT_BUFS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = warp_id(), lane = lane_id();
@@ -120,6 +122,10 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], PM_EPI_THREADS);
+        }
+        for (int i = 0; i < 4 * PM_OUT_BUFS; ++i) {
+            mbar_init(&blk_full[i], 64);   // every thread of the quarter's two epilogue warps
+            mbar_init(&blk_free[i], 1);    // the thread that sent the buffer's store
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -215,6 +221,48 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 mma_commit(&tfull[acc]);
             }
         }
+      } else if (TMA_OUT && lane == 0) {
+        // ------------------------- TMA stores of the staged output -------------------------
+        // Warp 2 serves lane quarters 0 and 1, warp 3 quarters 2 and 3, taking their blocks
+        // in the order the epilogue fills them: for each block, wait until the quarter's two
+        // warps have filled the staging buffer, send it, and free the buffer of the store
+        // sent before once that store has read it (so two stores are in flight).
+        const int jb = p.P < 4 ? p.P : 4;
+        (void)jb;
+        int n = 0;               // blocks taken so far (per quarter: n / 2)
+        int prev = -1;           // barrier index of the previous store still being read
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            const int nt = tile % p.num_n_tiles, mt = tile / p.num_n_tiles;
+            const int s = nt / p.nslices, c0 = (nt % p.nslices) * CW;
+            const CUtensorMap *mo = s == 0 ? &tmO0 : (s == 1 ? &tmO1 : &tmO2);
+            for (int k = 0; ok && k < CW / 16; ++k) {
+                for (int hb = 0; ok && hb < p.HPp; hb += 4) {
+                    for (int qq = 0; qq < 2; ++qq, ++n) {
+                        const int q = 2 * (warp - 2) + qq;
+                        const int blk = n / 2;                         // the quarter's block number
+                        const int bi = q * PM_OUT_BUFS + blk % PM_OUT_BUFS;
+                        if (!mbar_wait(&blk_full[bi], (blk / PM_OUT_BUFS) & 1, p.status, kSiteProjStore, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const int g0 = mt * PM_M + q * 32;
+                        if (g0 < p.M && hb < HP) {
+                            const long long gq = p.tok0 + g0;
+                            const uint8_t *stg = sOut + bi * PM_OUT_BUF_BYTES;
+                            tma_store_5d(mo, stg, c0 + 16 * k, (int)(gq % p.N_tok), hb % p.P, hb / p.P,
+                                         (int)(gq / p.N_tok));
+                        }
+                        bulk_commit();                                 // an empty group keeps the count
+                        bulk_wait_read(1);                             // the previous store has read its buffer
+                        if (prev >= 0) mbar_arrive(&blk_free[prev]);
+                        prev = bi;
+                    }
+                }
+            }
+        }
+        bulk_wait_all();
+        if (prev >= 0) mbar_arrive(&blk_free[prev]);
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PM_REGS_EPILOGUE));
@@ -270,15 +318,10 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             }
             if (TMA_OUT) {
                 // The two warps of the quarter take the two 8-column halves of each 16-column
-                // chunk in lockstep; per block of 4 pseudo-heads they fill one staging buffer
-                // [4][32 tokens][16 columns], meet at the quarter's barrier, and one thread sends
-                // it with a TMA store (its 32-byte rows are whole sectors of stacked rows).
-                const int g0 = mt * PM_M + q * 32;                  // the quarter's first token row
-                const bool qvalid = g0 < p.M;                       // all 32 valid or none (M % 32 == 0)
-                const long long gq = p.tok0 + g0, bq = gq / p.N_tok, tq0 = gq % p.N_tok;
-                const CUtensorMap *mo = s == 0 ? &tmO0 : (s == 1 ? &tmO1 : &tmO2);
-                const bool issuer = half == 0 && lane == 0;
-                const int jb = p.P < 4 ? p.P : 4;                   // pseudo-heads j per box (x heads)
+                // chunk; per block of 4 pseudo-heads they fill one staging buffer
+                // [4][32 tokens][16 columns] and arrive on its barrier; a thread of warp 2 or 3
+                // sends it with a TMA store (its 32-byte rows are whole sectors of stacked rows)
+                // and frees it once the store has read it.
 #pragma unroll 1
                 for (int k = 0; k < CW / 16; ++k) {
                     const int grp = 2 * k + half;
@@ -311,7 +354,13 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                     for (int e = 0; e < 4; ++e) o[i][e] = __ffma2_rn(a[i], y[m][e], o[i][e]);
                             }
                         }
-                        uint8_t *stg = sOut + (q * PM_OUT_BUFS + out_blk % PM_OUT_BUFS) * PM_OUT_BUF_BYTES;
+                        const int bi = q * PM_OUT_BUFS + out_blk % PM_OUT_BUFS;
+                        uint8_t *stg = sOut + bi * PM_OUT_BUF_BYTES;
+                        // the store that last read this buffer is done (its first use needs no wait)
+                        if (out_blk >= PM_OUT_BUFS &&
+                            !mbar_wait(&blk_free[bi], ((out_blk / PM_OUT_BUFS) - 1) & 1, p.status, kSiteProjEpilogue,
+                                       abort_flag))
+                            break;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             uint32_t w[4];
@@ -322,19 +371,9 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                 make_uint4(w[0], w[1], w[2], w[3]);
                         }
                         fence_proxy_async_smem();   // the staging writes before the TMA store reads them
-                        asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
-                        if (issuer) {
-                            if (qvalid && hb < HP) {
-                                tma_store_5d(mo, stg, c0 + 16 * k, (int)tq0, hb % p.P, hb / p.P, (int)bq);
-                                bulk_commit();
-                            }
-                            // the buffer the block after next fills is the one sent two blocks ago:
-                            // its read must be done before this thread reaches the next barrier
-                            bulk_wait_read(1);
-                        }
+                        mbar_arrive(&blk_full[bi]);
                     }
                 }
-                (void)jb;
             } else {
             // Each thread takes the 8-column groups half, half + 2, ... of the slice: the group's
                 // projections of all H heads are loaded from TMEM once and every pseudo-head is mixed
@@ -390,7 +429,6 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
-        if (TMA_OUT && half == 0 && lane == 0) bulk_wait_all();   // the staged stores are done
     }
     tc_fence_before();
     __syncthreads();
