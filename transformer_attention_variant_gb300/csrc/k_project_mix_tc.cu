@@ -20,7 +20,7 @@
 // next tile's main loop); warps 2-3 idle.  Warps 4-11: epilogue, one token row per thread;
 // the two warps of a TMEM lane quarter take alternate 8-column groups.  A group's
 // projections of all H heads are loaded from TMEM once, mixed into every pseudo-head with
-// alpha_s (fp32 pairs staged in shared memory) by packed fp32x2 FMAs, rounded (bf16; f16 for
+// alpha_s (fp32, staged in shared memory) by packed fp32x2 FMAs, rounded (bf16; f16 for
 // Vbar, the type the attention kernel's P V product reads) and stored 16 bytes at a time.
 // Tiles are ordered column-slice fastest, so the CTAs working at one time write every
 // slice of the same token rows and each stacked row's pieces meet in L2 (ordered the other
@@ -51,10 +51,10 @@ constexpr int PM_STAGE_BYTES = PM_A_BYTES + PM_B_BYTES_MAX;
 // [4 pseudo-heads][32 tokens][16 columns] bf16.
 constexpr int PM_OUT_BUF_BYTES = 4 * 32 * 16 * 2, PM_OUT_BUFS = 3;
 constexpr int PM_OUT_BYTES = 4 * PM_OUT_BUFS * PM_OUT_BUF_BYTES;   // 48 KB
-// alpha_s[m][hj] as duplicated pairs {a, a} (the packed FMA's operand): 3*H*HPp*8 bytes.
+// alpha_s[m][hj], fp32: 3*H*HPp*4 bytes.
 // Direct-store epilogue: a 4-stage ring when alpha takes at most 24 KB (H*P <= 64), else 3;
 // TMA-store epilogue: 3 stages and the staging buffers.
-static int pm_alpha_bytes(int H, int HPp) { return 3 * H * HPp * 8; }
+static int pm_alpha_bytes(int H, int HPp) { return 3 * H * HPp * 4; }
 static int pm_stages(int H, int HPp, bool tma_out) {
     return tma_out ? 3 : (pm_alpha_bytes(H, HPp) <= 24576 ? 4 : 3);
 }
@@ -101,7 +101,7 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint8_t *sA = smem;
     uint8_t *sB = sA + NS * PM_A_BYTES;
     uint8_t *sOut = sB + NS * PM_B_BYTES_MAX;                             // TMA_OUT staging (1 KB aligned)
-    float2 *sAl = reinterpret_cast<float2 *>(sOut + (TMA_OUT ? PM_OUT_BYTES : 0));   // [s][m][HPp] pairs {a, a}
+    float *sAl = reinterpret_cast<float *>(sOut + (TMA_OUT ? PM_OUT_BYTES : 0));   // [s][m][HPp]
     uint64_t *full = reinterpret_cast<uint64_t *>(sAl + 3 * H * p.HPp);
     uint64_t *empty = full + PM_MAX_STAGES;
     uint64_t *tfull = empty + PM_MAX_STAGES;
@@ -150,7 +150,7 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const int s = i / (H * p.HPp), r = i % (H * p.HPp), m = r / p.HPp, hj = r % p.HPp;
         const float *al = s == 0 ? p.alpha[0] : (s == 1 ? p.alpha[1] : p.alpha[2]);
         const float a = hj < HP ? al[m * HP + hj] : 0.f;
-        sAl[(s * H + m) * p.HPp + hj] = make_float2(a, a);
+        sAl[(s * H + m) * p.HPp + hj] = a;
     }
     tc_fence_before();
     __syncthreads();
@@ -290,7 +290,7 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             // row (b, h, t*P + j) of set s starts at base + (b*H + h)*N*P*d + t*P*d + j*d
             __nv_bfloat16 *base = p.qkv + s * p.s_stride + (b * p.H * p.N_tok + t) * Pd + c0;
             const long long h_stride = (long long)p.N_tok * Pd;
-            const float2 *al_s = sAl + s * H * p.HPp;
+            const float *al_s = sAl + s * H * p.HPp;
             const uint32_t tacc = tmem_base + lane_addr + acc * 256;
             if (p.y && half == 0) {   // the head projections themselves, when asked for
                 const long long D = (long long)H * p.d;
@@ -344,10 +344,9 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
                         for (int m = 0; m < NH; ++m) {
                             if (HT > 0 || m < H) {
-                                const float4 q0 = *reinterpret_cast<const float4 *>(al_s + m * p.HPp + hb);
-                                const float4 q1 = *reinterpret_cast<const float4 *>(al_s + m * p.HPp + hb + 2);
-                                const float2 a[4] = {make_float2(q0.x, q0.y), make_float2(q0.z, q0.w),
-                                                     make_float2(q1.x, q1.y), make_float2(q1.z, q1.w)};
+                                const float4 q4 = *reinterpret_cast<const float4 *>(al_s + m * p.HPp + hb);
+                                const float2 a[4] = {make_float2(q4.x, q4.x), make_float2(q4.y, q4.y),
+                                                     make_float2(q4.z, q4.z), make_float2(q4.w, q4.w)};
 #pragma unroll
                                 for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -367,7 +366,11 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
                                 w[e] = f16 ? pack_f16x2(o[i][e].x, o[i][e].y) : pack_bf16x2(o[i][e].x, o[i][e].y);
-                            *reinterpret_cast<uint4 *>(stg + (i * 32 + lane) * 32 + half * 16) =
+                            // 32-byte rows, 16-byte halves swapped on every other group of four rows
+                            // (the tensor map's 32-byte swizzle): the warp's 32 stores hit 8
+                            // different bank groups
+                            const int row = i * 32 + lane;
+                            *reinterpret_cast<uint4 *>(stg + row * 32 + ((half ^ ((row >> 2) & 1)) << 4)) =
                                 make_uint4(w[0], w[1], w[2], w[3]);
                         }
                         fence_proxy_async_smem();   // the staging writes before the TMA store reads them
@@ -398,10 +401,9 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
                         for (int m = 0; m < NH; ++m) {
                             if (HT > 0 || m < H) {
-                                const float4 q0 = *reinterpret_cast<const float4 *>(al_s + m * p.HPp + hb);
-                                const float4 q1 = *reinterpret_cast<const float4 *>(al_s + m * p.HPp + hb + 2);
-                                const float2 a[4] = {make_float2(q0.x, q0.y), make_float2(q0.z, q0.w),
-                                                     make_float2(q1.x, q1.y), make_float2(q1.z, q1.w)};
+                                const float4 q4 = *reinterpret_cast<const float4 *>(al_s + m * p.HPp + hb);
+                                const float2 a[4] = {make_float2(q4.x, q4.x), make_float2(q4.y, q4.y),
+                                                     make_float2(q4.z, q4.z), make_float2(q4.w, q4.w)};
 #pragma unroll
                                 for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -535,13 +537,13 @@ static cudaError_t launch_pm(const CUtensorMap &tmA, const void *Wp, const PMPar
             return cudaErrorInvalidValue;
         if (TMA_OUT) {
             // set s of QKV [B][H][N*P][d] as (c, t, j, h, b); a box = 16 columns x 32 tokens x 4
-            // pseudo-heads (min(P,4) values of j times 4/min(P,4) heads), no swizzle
+            // pseudo-heads (min(P,4) values of j times 4/min(P,4) heads), 32-byte swizzle
             const int jb = sh.P < 4 ? sh.P : 4;
             const uint64_t dims5[5] = {(uint64_t)sh.d, (uint64_t)sh.N, (uint64_t)sh.P, (uint64_t)sh.H, (uint64_t)sh.B};
             const uint64_t str5[4] = {(uint64_t)sh.P * sh.d * 2, (uint64_t)sh.d * 2,
                                       (uint64_t)sh.N * sh.P * sh.d * 2, (uint64_t)sh.H * sh.N * sh.P * sh.d * 2};
             const uint32_t box5[5] = {16, 32, (uint32_t)jb, (uint32_t)(4 / jb), 1};
-            if (!make_tmap_bf16(&tmO[s], p.qkv + s * p.s_stride, 5, dims5, str5, box5, false, 0))
+            if (!make_tmap_bf16(&tmO[s], p.qkv + s * p.s_stride, 5, dims5, str5, box5, false, 32))
                 return cudaErrorInvalidValue;
         } else {
             tmO[s] = tmB[s];   // unused
@@ -593,7 +595,7 @@ cudaError_t launch_project_mix(const void *X, const void *Wp, const float *aQ, c
     p.num_m_tiles = (int)((ntok + PM_M - 1) / PM_M);
     p.status = status;
     // TMA-store epilogue: whole 32-token groups of one batch element, blocks of 4 pseudo-heads
-    // that a box can hold, and alpha pairs within 24 KB; otherwise direct stores
+    // that a box can hold, and alpha within 24 KB; otherwise direct stores
     const bool tma_out = sh.N % 32 == 0 && tok0 % 32 == 0 && ntok % 32 == 0 &&
                          (sh.P == 1 || sh.P == 2 || sh.P == 4 || sh.P == 8) && (sh.H * sh.P) % 4 == 0 &&
                          pm_alpha_bytes(sh.H, p.HPp) <= 24576;
