@@ -341,10 +341,19 @@ proj_mix_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         for (int i = 0; i < 4; ++i)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) o[i][e] = make_float2(0.f, 0.f);
+                        // alpha of the block, four heads ahead of its use (the shared-memory load
+                        // latency stays off the FMA chain)
+                        const float *al_b = al_s + hb;
+                        float4 qr[4];
+#pragma unroll
+                        for (int m = 0; m < 4; ++m)
+                            if (HT > 0 || m < H) qr[m] = *reinterpret_cast<const float4 *>(al_b + m * p.HPp);
 #pragma unroll
                         for (int m = 0; m < NH; ++m) {
                             if (HT > 0 || m < H) {
-                                const float4 q4 = *reinterpret_cast<const float4 *>(al_s + m * p.HPp + hb);
+                                const float4 q4 = qr[m & 3];
+                                if (m + 4 < NH && (HT > 0 || m + 4 < H))
+                                    qr[m & 3] = *reinterpret_cast<const float4 *>(al_b + (m + 4) * p.HPp);
                                 const float2 a[4] = {make_float2(q4.x, q4.x), make_float2(q4.y, q4.y),
                                                      make_float2(q4.z, q4.z), make_float2(q4.w, q4.w)};
 #pragma unroll
