@@ -238,7 +238,8 @@ IHA_API int iha_mix_heads(const void *Y, const float *alpha_Q, const float *alph
                           int B, int N, int H, int d, int P, int dtype, void *QKV, void *stream);
 
 /* Step 3: masked softmax attention over each head's stacked sequence.
- * QKV as written by iha_project; Pbar [B][N][H][P][d].  This entry point has no workspace,
+ * QKV as written by iha_project; Pbar [B][N][H][P][d]; both 16-byte aligned
+ * (IHA_ERR_INVALID_ARG otherwise).  This entry point has no workspace,
  * so for bf16 each call takes the next of 1024 library-owned work counters (zeroed on
  * `stream` before the kernel): at most 1024 calls may be executing or queued on different
  * streams at once, and a CUDA graph that captured this call uses the same counter on every

@@ -116,6 +116,8 @@ def test_step_entry_points_reject_bad_arguments(iha):
     assert iha.iha_project(FAKE, FAKE, 1, 8, 2, 64, 0, 1, FAKE) == 1
     assert iha.iha_attention(FAKE, 1, 8, 2, 64, 2, 2, 0, 1, FAKE) == 1
     assert iha.iha_attention(FAKE, 1, 8, 2, 48, 2, 1, 0, 1, FAKE) == 2
+    assert iha.iha_attention(FAKE, 1, 8, 2, 64, 2, 1, 0, 1, FAKE + 2) == 1    # Pbar not 16-aligned
+    assert iha.iha_attention(FAKE + 8, 1, 8, 2, 64, 2, 1, 0, 1, FAKE) == 1    # QKV not 16-aligned
     assert iha.iha_contract(FAKE, None, 1, 8, 2, 64, 2, 1, FAKE) == 1
     assert iha.iha_forward(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 64, 2, 1, 0, FAKE) == 1
     assert iha.iha_forward_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 64, 2, 5, 0, FAKE, 1) == 1

@@ -506,6 +506,7 @@ int iha_mix_heads(const void *Y, const float *alpha_Q, const float *alpha_K, con
 int iha_attention(const void *QKV, int B, int N, int H, int d, int P, int mask_mode, int window, int dtype,
                   void *Pbar, void *stream) {
     if (!QKV || !Pbar) return IHA_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(QKV) | reinterpret_cast<uintptr_t>(Pbar)) & 15) != 0) return IHA_ERR_INVALID_ARG;
     int rc = validate_shape(B, N, H, d, P, dtype);
     if (rc == IHA_OK) rc = validate_mask(mask_mode, window);
     if (rc != IHA_OK) return rc;
