@@ -472,37 +472,31 @@ size_t sliced_weights_bytes(const Shape &sh) {
 }
 
 // Wp_s[k][sl*SC + m*CW + c] = W_s[k][m*d + sl*CW + c] (zero in a slice's padding columns),
-// SC = slice columns.  A thread moves 4 16-byte units of one output row (their loads in
-// flight together); consecutive threads write consecutive units.
-constexpr int SW_UNITS = 4;
+// SC = slice columns.  A block moves SW_ROWS whole rows (row = (s, k)); each thread takes
+// the same 16-byte unit of every one of them, so their loads are in flight together, and
+// consecutive threads write consecutive units.  A warp's loads are whole 32-byte sectors
+// (the two 16-byte units of a head's slice).  Indices fit 32 bits: 3*D rows of at most
+// d/16 * 256 / 8 units.
+constexpr int SW_ROWS = 4;
 __global__ void __launch_bounds__(256)
 slice_weights_kernel(const uint4 *__restrict__ W0, const uint4 *__restrict__ W1, const uint4 *__restrict__ W2,
                      uint4 *__restrict__ Wp, int D, int H, int d, int cw, int sc, int nslices) {
-    const long long row_out = (long long)nslices * sc / 8;   // 16-byte units per row of Wp_s
-    const long long total = 3LL * D * row_out;
-    const long long stride = (long long)gridDim.x * blockDim.x * SW_UNITS;
-    for (long long i0 = (blockIdx.x * (long long)blockDim.x) * SW_UNITS + threadIdx.x; i0 < total; i0 += stride) {
-        uint4 v[SW_UNITS];
+    const int units_per_slice = sc / 8, row_out = nslices * units_per_slice, row_in = H * d / 8;
+    for (int row0 = blockIdx.x * SW_ROWS; row0 < 3 * D; row0 += gridDim.x * SW_ROWS) {
+        for (int un = threadIdx.x; un < row_out; un += blockDim.x) {
+            const int sl = un / units_per_slice, n = (un % units_per_slice) * 8;   // column within the slice
+            const bool live = n < H * cw;
+            const int src = live ? ((n / cw) * d + sl * cw + n % cw) / 8 : 0;
+            uint4 v[SW_ROWS];
 #pragma unroll
-        for (int u = 0; u < SW_UNITS; ++u) {
-            const long long i = i0 + (long long)u * blockDim.x;
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (i < total) {
-                const int s = (int)(i / (D * row_out));
-                const long long r = i % (D * row_out);
-                const int k = (int)(r / row_out), un = (int)(r % row_out);
-                const int sl = un / (sc / 8), n = (un % (sc / 8)) * 8;   // column within the slice
-                if (n < H * cw) {
-                    const int m = n / cw, c = n % cw;
-                    const uint4 *W = s == 0 ? W0 : (s == 1 ? W1 : W2);
-                    v[u] = W[((long long)k * H * d + (long long)m * d + sl * cw + c) / 8];
-                }
+            for (int u = 0; u < SW_ROWS; ++u) {
+                const int row = row0 + u, s = row / D, k = row - s * D;
+                const uint4 *W = s == 0 ? W0 : (s == 1 ? W1 : W2);
+                v[u] = (live && row < 3 * D) ? W[(long long)k * row_in + src] : make_uint4(0u, 0u, 0u, 0u);
             }
-        }
 #pragma unroll
-        for (int u = 0; u < SW_UNITS; ++u) {
-            const long long i = i0 + (long long)u * blockDim.x;
-            if (i < total) Wp[i] = v[u];
+            for (int u = 0; u < SW_ROWS; ++u)
+                if (row0 + u < 3 * D) Wp[(long long)(row0 + u) * row_out + un] = v[u];
         }
     }
 }
@@ -514,8 +508,8 @@ cudaError_t launch_slice_weights(const void *WQ, const void *WK, const void *WV,
          reinterpret_cast<uintptr_t>(Wp)) & 15)
         return cudaErrorInvalidValue;
     const int cw = pm_slice_width(sh.H, sh.d), sc = pm_slice_cols(sh.H, cw);
-    const long long units = 3LL * sh.D() * (sh.d / cw) * sc / 8;
-    long long blocks = (units + 256 * SW_UNITS - 1) / (256 * SW_UNITS);
+    const long long rows = 3LL * sh.D();
+    long long blocks = (rows + SW_ROWS - 1) / SW_ROWS;
     const long long cap = 16LL * device_sm_count();
     if (blocks > cap) blocks = cap;
     slice_weights_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4 *>(WQ), static_cast<const uint4 *>(WK),
