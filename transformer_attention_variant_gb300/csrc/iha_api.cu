@@ -152,8 +152,12 @@ static cudaStream_t *copy_streams() {
 // iha_forward_host on the unfolded bf16 route with the copies overlapped with the work:
 // W and X go up on the two copy streams, X in FH_CHUNKS token chunks, and the projection and
 // mixing of a chunk start as soon as that chunk (and W and alpha) have landed; the contraction runs in token
-// chunks and each chunk's output goes down while the next is computed.  `st` waits for both
-// copy streams at the end, so the call completes on `st` as the plain sequence does.
+// chunks and each chunk's output goes down while the next is computed.  All uploads go on
+// copy stream 0 in the order the work needs them (W, alpha, R, then the X chunks) and all
+// downloads on copy stream 1: copies queued on two streams in the same direction did not
+// share the host link but ran one stream after the other, so an even split delayed W.  `st`
+// waits for both copy streams at the end, so the call completes on `st` as the plain
+// sequence does.
 constexpr int FH_CHUNKS = 4;
 static int forward_host_overlapped(const void *X, const void *WQ, const void *WK, const void *WV, const float *aQ,
                                    const float *aK, const float *aV, const float *R, const Shape &sh, int mask_mode,
@@ -169,8 +173,8 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
     uint8_t *Wp = w8 + lay.wt, *QKV = w8 + lay.qkv, *Pbar = w8 + lay.pbar;
     unsigned int *ticket = reinterpret_cast<unsigned int *>(w8 + lay.ctr);
     int *status = status_ptr();
-    // events: 0 start, 1-2 W ready (one per copy stream), 3.. X chunks, then contraction chunks,
-    // then the two copy streams' last copies
+    // events: 0 start, 1 W ready, 2 unused, 3.. X chunks, then contraction chunks, then the two
+    // copy streams' last copies
     constexpr int NEV = 3 + 2 * FH_CHUNKS + 2;
     cudaEvent_t ev[NEV] = {};
     cudaError_t e = cudaSuccess;
@@ -184,28 +188,26 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
     uint8_t *outh = static_cast<uint8_t *>(out);
     if (e == cudaSuccess) e = cudaEventRecord(ev[0], st);   // after earlier work on st
     for (int c = 0; c < 2 && e == cudaSuccess; ++c) e = cudaStreamWaitEvent(cs[c], ev[0], 0);
-    // weights: W_Q, W_K, alpha_Q on copy stream 0; W_V, alpha_K, alpha_V, R on copy stream 1
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dWQ, WQ, wb, cudaMemcpyHostToDevice, cs[0]);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dWK, WK, wb, cudaMemcpyHostToDevice, cs[0]);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(daQ, aQ, ab, cudaMemcpyHostToDevice, cs[0]);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dWV, WV, wb, cudaMemcpyHostToDevice, cs[1]);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(daK, aK, ab, cudaMemcpyHostToDevice, cs[1]);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(daV, aV, ab, cudaMemcpyHostToDevice, cs[1]);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dR, R, ab, cudaMemcpyHostToDevice, cs[1]);
-    if (e == cudaSuccess) e = cudaEventRecord(ev[1], cs[0]);
-    if (e == cudaSuccess) e = cudaEventRecord(ev[2], cs[1]);
-    // X in chunks, alternating copy streams
+    // uploads, in the order the work needs them, on copy stream 0
+    const cudaStream_t up = cs[0], down = cs[1];
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dWQ, WQ, wb, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dWK, WK, wb, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dWV, WV, wb, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(daQ, aQ, ab, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(daK, aK, ab, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(daV, aV, ab, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dR, R, ab, cudaMemcpyHostToDevice, up);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[1], up);
     for (int i = 0; i < FH_CHUNKS && e == cudaSuccess; ++i) {
         long long r0, r1;
         chunk(i, r0, r1);
         if (r1 > r0)
             e = cudaMemcpyAsync(static_cast<uint8_t *>(dX) + r0 * row_x, Xh + r0 * row_x, (r1 - r0) * row_x,
-                                cudaMemcpyHostToDevice, cs[i & 1]);
-        if (e == cudaSuccess) e = cudaEventRecord(ev[3 + i], cs[i & 1]);
+                                cudaMemcpyHostToDevice, up);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[3 + i], up);
     }
     // projection and mixing chunk by chunk, straight into the stacked layout
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[1], 0);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[2], 0);
     if (e == cudaSuccess) e = launch_slice_weights(dWQ, dWK, dWV, sh, Wp, st);
     for (int i = 0; i < FH_CHUNKS && e == cudaSuccess; ++i) {
         long long r0, r1;
@@ -224,10 +226,10 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
             e = launch_contract_tc(Pbar + r0 * row_p, dR, Shape{1, (int)(r1 - r0), sh.H, sh.d, sh.P},
                                    static_cast<uint8_t *>(dOut) + r0 * row_x, st, status);
         if (e == cudaSuccess) e = cudaEventRecord(ev[3 + FH_CHUNKS + i], st);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs[i & 1], ev[3 + FH_CHUNKS + i], 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(down, ev[3 + FH_CHUNKS + i], 0);
         if (e == cudaSuccess && r1 > r0)
             e = cudaMemcpyAsync(outh + r0 * row_x, static_cast<uint8_t *>(dOut) + r0 * row_x, (r1 - r0) * row_x,
-                                cudaMemcpyDeviceToHost, cs[i & 1]);
+                                cudaMemcpyDeviceToHost, down);
     }
     // The call completes on st: st waits for everything queued on the copy streams -- also
     // after an error, so that no copy still runs when the caller reuses its buffers (without
