@@ -616,7 +616,10 @@ GRAM_TOL = 2.0 ** -6
     # pseudo-keys); a window >= N (= causal); H*P = 128 with P = 8; one head (D = 64, narrower
     # than one GEMM tile, and one row of the token grams)
     (1, 1, 2, 64, 1, C, 0), (2, 60, 4, 128, 2, WN, 1), (1, 90, 2, 64, 3, WN, 500), (1, 40, 16, 64, 8, C, 0),
-    (3, 33, 1, 64, 2, C, 0)])
+    (3, 33, 1, 64, 2, C, 0),
+    # the large workloads' heads (H = 16, d = 128, D = 2048: the gradient GEMMs at full width)
+    # with P = 4 causal and P = 2 windowed, stacked length 2048 (16 resident tiles per head)
+    (1, 512, 16, 128, 4, C, 0), (1, 1024, 16, 128, 2, WN, 256)])
 def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
     from oracle import backward as bwd
     w = gi.Workload("bwd", B=B, N=N, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=90 + P)
@@ -651,7 +654,9 @@ def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
 
 
 @pytest.mark.parametrize("B,N,H,d,P,mode,window", [
-    (2, 150, 4, 64, 2, C, 0), (1, 300, 8, 128, 4, WN, 40), (1, 77, 4, 128, 1, NM, 0)])
+    (2, 150, 4, 64, 2, C, 0), (1, 300, 8, 128, 4, WN, 40), (1, 77, 4, 128, 1, NM, 0),
+    # the causal P = 4 workload at full size, as the training benchmark runs it
+    (1, 8192, 16, 128, 4, C, 0)])
 def test_training_pair_matches_recompute(iha, B, N, H, d, P, mode, window):
     """iha_forward_train + iha_backward_saved give iha_forward's output (P >= 2: the same
     route) and iha_backward's gradients bit for bit."""
