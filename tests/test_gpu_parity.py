@@ -459,6 +459,33 @@ def test_layer_stack(iha, P_local, N):
     assert torch.equal(out, x)
 
 
+def test_layer_stack_full_size(iha):
+    """The stack the benchmark times (causal P=4 N=8192 layer's shape: four window-256 P=4
+    layers, then the global P=1 causal layer): bit for bit the chain of single-layer calls,
+    and each layer against the oracle on its own input at the full-size sampled rows."""
+    B, N, H, d = 1, 8192, 16, 128
+    layers = gi.make_stack_inputs(B, N, H, d, "bf16", seed=80, schedule=gi.local_global_schedule(N, 4))
+    keys = ("W_Q", "W_K", "W_V", "alpha_Q", "alpha_K", "alpha_V", "R")
+    dev = [{k: L[k].to("cuda:0").contiguous() for k in keys} for L in layers]
+    for dl, L in zip(dev, layers):
+        dl.update(P=L["P"], mask_mode=L["mask_mode"], window=L["window"])
+    X = layers[0]["X"].to("cuda:0").contiguous()
+    out = torch.full_like(X, float("nan"))
+    iha.check(iha.iha_forward_stack(X, dev, B, N, H, d, iha.IHA_DTYPE_BF16, out), "iha_forward_stack")
+    torch.cuda.synchronize()
+    x = X
+    for dl, L in zip(dev, layers):
+        w = L["workload"]
+        y = run_gpu(iha, w, dinp=dict({k: dl[k] for k in keys}, X=x))
+        inp = {k: L[k] for k in keys}
+        inp["X"] = x.cpu()
+        rows = sample_rows(w)
+        got = y.double().cpu().numpy().reshape(B * N, w.D)
+        assert_parity(w, got[rows], oracle_rows(w, inp, rows=rows, projection="numpy"))
+        x = y
+    assert torch.equal(out, x)
+
+
 # ---------------------------------------------------------------------------
 # incremental decoding: prefill a prompt, then decode token by token; every decoded row
 # must be the row the forward pass gives that token of the whole sequence (the oracle)
