@@ -173,9 +173,9 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
     uint8_t *Wp = w8 + lay.wt, *QKV = w8 + lay.qkv, *Pbar = w8 + lay.pbar;
     unsigned int *ticket = reinterpret_cast<unsigned int *>(w8 + lay.ctr);
     int *status = status_ptr();
-    // events: 0 start, 1 W ready, 2 unused, 3.. X chunks, then contraction chunks, then the two
-    // copy streams' last copies
-    constexpr int NEV = 3 + 2 * FH_CHUNKS + 2;
+    // events: 0 start, 1 W ready, 2.. X chunks, then contraction chunks, then the two copy
+    // streams' last copies
+    constexpr int NEV = 2 + 2 * FH_CHUNKS + 2;
     cudaEvent_t ev[NEV] = {};
     cudaError_t e = cudaSuccess;
     int made = 0;
@@ -204,7 +204,7 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
         if (r1 > r0)
             e = cudaMemcpyAsync(static_cast<uint8_t *>(dX) + r0 * row_x, Xh + r0 * row_x, (r1 - r0) * row_x,
                                 cudaMemcpyHostToDevice, up);
-        if (e == cudaSuccess) e = cudaEventRecord(ev[3 + i], up);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[2 + i], up);
     }
     // projection and mixing chunk by chunk, straight into the stacked layout
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[1], 0);
@@ -212,7 +212,7 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
     for (int i = 0; i < FH_CHUNKS && e == cudaSuccess; ++i) {
         long long r0, r1;
         chunk(i, r0, r1);
-        e = cudaStreamWaitEvent(st, ev[3 + i], 0);
+        e = cudaStreamWaitEvent(st, ev[2 + i], 0);
         if (e == cudaSuccess && r1 > r0)
             e = launch_project_mix(dX, Wp, daQ, daK, daV, sh, r0, r1 - r0, QKV, nullptr, st, status);
     }
@@ -225,8 +225,8 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
         if (r1 > r0)
             e = launch_contract_tc(Pbar + r0 * row_p, dR, Shape{1, (int)(r1 - r0), sh.H, sh.d, sh.P},
                                    static_cast<uint8_t *>(dOut) + r0 * row_x, st, status);
-        if (e == cudaSuccess) e = cudaEventRecord(ev[3 + FH_CHUNKS + i], st);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(down, ev[3 + FH_CHUNKS + i], 0);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[2 + FH_CHUNKS + i], st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(down, ev[2 + FH_CHUNKS + i], 0);
         if (e == cudaSuccess && r1 > r0)
             e = cudaMemcpyAsync(outh + r0 * row_x, static_cast<uint8_t *>(dOut) + r0 * row_x, (r1 - r0) * row_x,
                                 cudaMemcpyDeviceToHost, down);
@@ -235,7 +235,7 @@ static int forward_host_overlapped(const void *X, const void *WQ, const void *WK
     // after an error, so that no copy still runs when the caller reuses its buffers (without
     // the events, the host waits for the copy streams instead).
     for (int c = 0; c < 2; ++c) {
-        const int k = 3 + 2 * FH_CHUNKS + c;
+        const int k = 2 + 2 * FH_CHUNKS + c;
         cudaError_t e2 = k < made ? cudaEventRecord(ev[k], cs[c]) : cudaErrorInvalidValue;
         if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, ev[k], 0);
         if (e2 != cudaSuccess) {
