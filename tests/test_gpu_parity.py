@@ -373,8 +373,12 @@ def test_caller_workspace_and_default_stream_entry(iha):
 
 
 @pytest.mark.parametrize("B,N,H,d,P,mode,window", [
-    (2, 150, 2, 64, 2, C, 0),        # unfolded route: copies overlapped with chunked work
-    (1, 777, 4, 128, 3, WN, 60),     # chunks of 194-195 tokens
+    (2, 150, 2, 64, 2, C, 0),        # unfolded route, attention per batch element
+    (3, 130, 2, 128, 4, WN, 40),     # three batch elements: three chunks
+    (1, 700, 4, 128, 4, C, 0),       # one sequence: one attention after the last projection chunk
+    (1, 520, 2, 64, 2, WN, 100),     # the same under a window
+    (1, 300, 2, 64, 2, NM, 0),       # and without a mask
+    (1, 777, 4, 128, 3, WN, 60),     # P does not divide 256: one attention, chunks of 194-195 tokens
     (2, 99, 4, 64, 1, C, 0)])        # folded route (P = 1): the plain sequence
 def test_forward_host_buffers(iha, B, N, H, d, P, mode, window):
     w = W("host", B=B, N=N, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=45)

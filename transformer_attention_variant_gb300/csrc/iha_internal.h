@@ -136,6 +136,16 @@ cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode
 cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
                              void *Pbar, cudaStream_t st, int *status, unsigned int *ticket = nullptr);
 
+// The attention of part of a layer (bf16): stacked-query blocks of 256 rows
+// [qb_begin, qb_begin + qb_count) of heads b*H + h in [bh_begin, bh_begin + bh_count).  Each
+// row's result is the one the whole-layer launch gives it (the same work items).
+struct AttnRange {
+    int bh_begin, bh_count, qb_begin, qb_count;
+};
+constexpr int kAttnRowsPerBlock = 256;
+cudaError_t launch_attention_range(const void *QKV, const Shape &sh, int mask_mode, int window, void *Pbar,
+                                   const AttnRange &range, cudaStream_t st, int *status, unsigned int *ticket);
+
 // Bytes of the control slot every workspace ends with (the attention's work counter).
 constexpr size_t kCtrlBytes = 256;
 

@@ -58,6 +58,7 @@ static_assert(128 * AT_REGS_CONTROL + 256 * AT_REGS_SOFTMAX <= AT_THREADS * AT_L
 constexpr float AT_RESCALE_THRESHOLD = 8.0f;
 constexpr int AT_ITEM_SLOTS = 4;   // work items handed from the TMA warp to the other roles
 constexpr int AT_TICKETS = 1024;   // per-launch work counters (a ring; see launch_attn_tc)
+static_assert(kAttnRowsPerBlock == 2 * AT_BM, "a work item is one query block of AttnRange");
 
 template <int DH>
 struct AttnCfg {
@@ -81,8 +82,9 @@ struct AttnParams {
     int N, H, P, L;        // L = N*P
     int mask_mode, window;
     float scale_log2;      // log2(e) / sqrt(d)
-    int num_qblocks;
-    int num_heads;         // B * H
+    int num_qblocks;       // query blocks of this launch: qb_begin .. qb_begin + num_qblocks - 1
+    int num_heads;         // heads (b*H + h) of this launch: bh_begin .. bh_begin + num_heads - 1
+    int qb_begin, bh_begin;
     int head_group;        // heads per scheduling group
     int stage_o;           // epilogue through shared memory and TMA (P divides 128)
     unsigned int *ticket;  // this launch's work counter (0 at launch)
@@ -108,7 +110,7 @@ __device__ __forceinline__ void key_interval(const AttnParams &p, int r, int &lo
     if (p.mask_mode == 2) lo = max(lo, (t - p.window + 1) * p.P);
 }
 
-// Work item i (0 <= i < B*H*num_qblocks) -> (bh, qb): heads in groups of p.head_group
+// Work item i (0 <= i < num_heads*num_qblocks) -> (bh, qb): heads in groups of p.head_group
 // (chosen so that a group's K and V fit in L2); within a group, query blocks heaviest
 // (latest) first across the group's heads.  The CTAs working at one time then share one
 // group's K/V in L2, and the light blocks of each group fill the tail of its round.
@@ -117,8 +119,8 @@ __device__ __forceinline__ void item_coords(const AttnParams &p, long long i, in
     const int g = (int)(i / per_group);
     const int j = (int)(i % per_group);
     const int g_heads = min(p.head_group, p.num_heads - g * p.head_group);
-    bh = g * p.head_group + j % g_heads;
-    qb = p.num_qblocks - 1 - j / g_heads;
+    bh = p.bh_begin + g * p.head_group + j % g_heads;
+    qb = p.qb_begin + p.num_qblocks - 1 - j / g_heads;
 }
 
 // Work counters: a launch takes one (reset to 0 on its stream before the kernel) and its
@@ -657,7 +659,8 @@ static unsigned int *attn_ticket(unsigned int *own, cudaStream_t st, cudaError_t
 
 template <int DH>
 static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mode, int window, void *Pbar,
-                                  float *lse, int lse_stride, cudaStream_t st, int *status, unsigned int *ticket) {
+                                  float *lse, int lse_stride, cudaStream_t st, int *status, unsigned int *ticket,
+                                  const AttnRange *range = nullptr) {
     using C = AttnCfg<DH>;
     const long long L = sh.L(), BH = (long long)sh.B * sh.H;
     const __nv_bfloat16 *base = (const __nv_bfloat16 *)QKV;
@@ -691,7 +694,10 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     p.mask_mode = mask_mode;
     p.window = window;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
-    p.num_qblocks = (int)((L + 2 * AT_BM - 1) / (2 * AT_BM));
+    const int all_qblocks = (int)((L + 2 * AT_BM - 1) / (2 * AT_BM));
+    p.qb_begin = range ? range->qb_begin : 0;
+    p.num_qblocks = range ? range->qb_count : all_qblocks;
+    p.bh_begin = range ? range->bh_begin : 0;
     p.stage_o = stage_o ? 1 : 0;
     p.lse = lse;
     p.lse_stride = lse_stride;
@@ -700,16 +706,19 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     if (e != cudaSuccess) return e;
     e = check_register_contract(attn_fwd_tc<DH>, AT_LAUNCH_REGS);
     if (e != cudaSuccess) return e;
-    p.num_heads = (int)BH;
+    p.num_heads = range ? range->bh_count : (int)BH;
+    if (p.num_qblocks <= 0 || p.num_heads <= 0 || p.qb_begin < 0 || p.bh_begin < 0 ||
+        p.qb_begin + p.num_qblocks > all_qblocks || p.bh_begin + p.num_heads > BH)
+        return cudaErrorInvalidValue;
     {
         const long long kv_bytes_per_head = 2LL * L * DH * 2;   // K and V of one (b, h)
         // 64 MB of the 129 MB L2 per group: measured best of 24..128 MB on causal and windowed
         // workloads (causal P=4: 2.90 ms at 64 MB, 2.99 ms at 48 MB)
         long long g = (64LL << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
-        p.head_group = (int)(g < 1 ? 1 : (g > BH ? BH : g));
+        p.head_group = (int)(g < 1 ? 1 : (g > p.num_heads ? p.num_heads : g));
     }
     // persistent: one CTA per SM, each looping over work items
-    const long long items = BH * p.num_qblocks;
+    const long long items = (long long)p.num_heads * p.num_qblocks;
     const unsigned grid = (unsigned)(items < device_sm_count() ? items : device_sm_count());
     p.ticket = attn_ticket(ticket, st, e);
     if (!p.ticket) return e;
@@ -720,6 +729,15 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
 cudaError_t launch_attention(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype, void *Pbar,
                              cudaStream_t st, int *status, unsigned int *ticket) {
     return launch_attention_lse(QKV, sh, mask_mode, window, dtype, Pbar, nullptr, 0, st, status, ticket);
+}
+
+cudaError_t launch_attention_range(const void *QKV, const Shape &sh, int mask_mode, int window, void *Pbar,
+                                   const AttnRange &range, cudaStream_t st, int *status, unsigned int *ticket) {
+    if (sh.d == 128)
+        return launch_attn_tc<128>(QKV, sh, mask_mode, window, Pbar, nullptr, 0, st, status, ticket, &range);
+    if (sh.d == 64)
+        return launch_attn_tc<64>(QKV, sh, mask_mode, window, Pbar, nullptr, 0, st, status, ticket, &range);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attention_lse(const void *QKV, const Shape &sh, int mask_mode, int window, int dtype,
