@@ -85,6 +85,8 @@ struct AttnParams {
     int num_qblocks;       // query blocks of this launch: qb_begin .. qb_begin + num_qblocks - 1
     int num_heads;         // heads (b*H + h) of this launch: bh_begin .. bh_begin + num_heads - 1
     int qb_begin, bh_begin;
+    int ramp;              // light query blocks per head (window mode: rows whose window the
+                           // sequence start clips), run after all the others
     int head_group;        // heads per scheduling group
     int stage_o;           // epilogue through shared memory and TMA (P divides 128)
     unsigned int *ticket;  // this launch's work counter (0 at launch)
@@ -110,17 +112,27 @@ __device__ __forceinline__ void key_interval(const AttnParams &p, int r, int &lo
     if (p.mask_mode == 2) lo = max(lo, (t - p.window + 1) * p.P);
 }
 
-// Work item i (0 <= i < num_heads*num_qblocks) -> (bh, qb): heads in groups of p.head_group
-// (chosen so that a group's K and V fit in L2); within a group, query blocks heaviest
-// (latest) first across the group's heads.  The CTAs working at one time then share one
-// group's K/V in L2, and the light blocks of each group fill the tail of its round.
+// Work item i (0 <= i < num_heads*num_qblocks) -> (bh, qb).  First the query blocks above the
+// ramp: heads in groups of p.head_group (chosen so that a group's K and V fit in L2); within a
+// group, query blocks heaviest (latest) first across the group's heads.  The CTAs working at
+// one time then share one group's K/V in L2.  Then the ramp blocks of every head, heaviest
+// first: in window mode the other blocks are all alike, and the lighter ramp blocks are what
+// fills the launch's last round (run per group, the last group's alike blocks ended it).
 __device__ __forceinline__ void item_coords(const AttnParams &p, long long i, int &bh, int &qb) {
-    const long long per_group = (long long)p.head_group * p.num_qblocks;
-    const int g = (int)(i / per_group);
-    const int j = (int)(i % per_group);
-    const int g_heads = min(p.head_group, p.num_heads - g * p.head_group);
-    bh = p.bh_begin + g * p.head_group + j % g_heads;
-    qb = p.qb_begin + p.num_qblocks - 1 - j / g_heads;
+    const int qa = p.num_qblocks - p.ramp;   // blocks above the ramp, per head
+    const long long na = (long long)p.num_heads * qa;
+    if (i < na) {
+        const long long per_group = (long long)p.head_group * qa;
+        const int g = (int)(i / per_group);
+        const int j = (int)(i % per_group);
+        const int g_heads = min(p.head_group, p.num_heads - g * p.head_group);
+        bh = p.bh_begin + g * p.head_group + j % g_heads;
+        qb = p.qb_begin + p.num_qblocks - 1 - j / g_heads;
+    } else {
+        const long long j = i - na;
+        bh = p.bh_begin + (int)(j % p.num_heads);
+        qb = p.qb_begin + p.ramp - 1 - (int)(j / p.num_heads);
+    }
 }
 
 // Work counters: a launch takes one (reset to 0 on its stream before the kernel) and its
@@ -707,6 +719,12 @@ static cudaError_t launch_attn_tc(const void *QKV, const Shape &sh, int mask_mod
     e = check_register_contract(attn_fwd_tc<DH>, AT_LAUNCH_REGS);
     if (e != cudaSuccess) return e;
     p.num_heads = range ? range->bh_count : (int)BH;
+    {
+        // ramp: query blocks whose first row's window reaches back past the sequence start
+        const long long ramp_rows = mask_mode == 2 ? (long long)window * sh.P : 0;
+        const long long r = (ramp_rows + 2 * AT_BM - 1) / (2 * AT_BM) - p.qb_begin;
+        p.ramp = (int)(r < 0 ? 0 : (r > p.num_qblocks ? p.num_qblocks : r));
+    }
     if (p.num_qblocks <= 0 || p.num_heads <= 0 || p.qb_begin < 0 || p.bh_begin < 0 ||
         p.qb_begin + p.num_qblocks > all_qblocks || p.bh_begin + p.num_heads > BH)
         return cudaErrorInvalidValue;
