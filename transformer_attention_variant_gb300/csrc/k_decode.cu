@@ -34,13 +34,17 @@ constexpr int DC_NCH_MAX = 64;    // KV chunks per (b, h)
 // Warp 0 moves the slab into shared memory with one bulk copy per row (no registers held,
 // so three CTAs fit on an SM and the whole of W is in flight at once); then a lane owns 8
 // columns and warp w the rows w, w+8, ..., and the 8 warps' sums are added in shared
-// memory.  BM batch rows per pass.
+// memory.  BM batch rows per pass.  ONE_PASS (B <= BM): the 8 warps' sums go into the slab's
+// space once every warp is done with the slab, so a CTA holds about 66 KB and three fit on an
+// SM for every BM (with a buffer of their own, 98 KB at BM = 4 allowed two per SM and the
+// 384 CTAs ran in two waves: 17.5 against 8.5 us at B = 4).
 constexpr int DP_SLAB = DC_KROWS_MAX * 256 * 2;   // 64 KB
-template <int BM>
+static_assert((size_t)8 * DC_BMAX * 256 * 4 <= (size_t)DP_SLAB, "the warps' sums fit in the slab");
+template <int BM, bool ONE_PASS>
 constexpr size_t dp_smem_bytes() {
-    return DP_SLAB + (size_t)BM * DC_KROWS_MAX * 4 + (size_t)8 * BM * 256 * 4 + 16 + 128;
+    return DP_SLAB + (size_t)BM * DC_KROWS_MAX * 4 + (ONE_PASS ? 0 : (size_t)8 * BM * 256 * 4) + 16 + 128;
 }
-template <int BM>
+template <int BM, bool ONE_PASS>
 __global__ void __launch_bounds__(256)
 decode_proj(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ WQ,
             const __nv_bfloat16 *__restrict__ WK, const __nv_bfloat16 *__restrict__ WV, int B, int D,
@@ -56,8 +60,8 @@ decode_proj(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *slab = psm;                                                    // [krows][256] bf16
     float *xs = reinterpret_cast<float *>(psm + DP_SLAB);                   // [BM][krows]
-    float *red = xs + BM * DC_KROWS_MAX;                                    // [8 warps][BM][256]
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + 8 * BM * 256);
+    float *red = ONE_PASS ? reinterpret_cast<float *>(slab) : xs + BM * DC_KROWS_MAX;   // [8 warps][BM][256]
+    uint64_t *full = reinterpret_cast<uint64_t *>(ONE_PASS ? xs + BM * DC_KROWS_MAX : red + 8 * BM * 256);
     if (threadIdx.x == 0) {
         mbar_init(full, 1);
         fence_barrier_init();
@@ -105,6 +109,7 @@ decode_proj(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict
             }
         }
         // reduce over the 8 warps
+        if (ONE_PASS) __syncthreads();   // every warp is done with the slab the sums overwrite
 #pragma unroll
         for (int b = 0; b < BM; ++b)
             if (b < nb)
@@ -363,10 +368,11 @@ cudaError_t launch_decode(const void *x, const void *WQ, const void *WK, const v
                 kern<<<g1, 256, smem1, st>>>((const __nv_bfloat16 *)x, (const __nv_bfloat16 *)WQ,
                                              (const __nv_bfloat16 *)WK, (const __nv_bfloat16 *)WV, B, D, Yp, status);
         };
-        if (bm == 1) run(decode_proj<1>, dp_smem_bytes<1>());
-        else if (bm == 2) run(decode_proj<2>, dp_smem_bytes<2>());
-        else if (bm == 4) run(decode_proj<4>, dp_smem_bytes<4>());
-        else run(decode_proj<8>, dp_smem_bytes<8>());
+        if (bm == 1) run(decode_proj<1, true>, dp_smem_bytes<1, true>());
+        else if (bm == 2) run(decode_proj<2, true>, dp_smem_bytes<2, true>());
+        else if (bm == 4) run(decode_proj<4, true>, dp_smem_bytes<4, true>());
+        else if (B <= 8) run(decode_proj<8, true>, dp_smem_bytes<8, true>());
+        else run(decode_proj<8, false>, dp_smem_bytes<8, false>());
         if (e != cudaSuccess) return e;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
