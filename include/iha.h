@@ -202,8 +202,9 @@ IHA_API int iha_project(const void *X, const void *Wt, int B, int N, int H, int 
 
 /* Which way steps 1+2 run for this shape (what iha_forward_ex does):
  *   1 = unfolded: iha_slice_weights then iha_project_mix, the head projections with the
- *       mixing in the GEMM epilogue (bf16, P >= 2, H <= 16, H*P <= 128 -- the GEMM does 1/P
- *       of the folded GEMM's work, and the head projections never reach memory);
+ *       mixing in the GEMM epilogue (bf16, H <= 16, H*P <= 128 -- the GEMM does 1/P of the
+ *       folded GEMM's work, the head projections never reach memory, and at P = 1 the
+ *       weights are only reordered, not folded);
  *   0 = folded:   iha_fold_weights then iha_project;
  *  -1 = invalid sizes or dtype. */
 IHA_API int iha_projection_route(int H, int d, int P, int dtype);
@@ -324,8 +325,8 @@ IHA_API int iha_backward(const void *X, const void *W_Q, const void *W_K, const 
 
 /* A training step without recomputation, on the shapes iha_backward takes:
  * iha_forward_train computes the layer output `out` [B][N][H*d] (bfloat16; bit-identical to
- *   iha_forward's when iha_projection_route() is 1, i.e. P >= 2; for P = 1 iha_forward folds
- *   alpha into W and rounds differently) and leaves the forward pieces the gradients need
+ *   iha_forward's: every shape it takes is on the unfolded route) and leaves the forward
+ *   pieces the gradients need
  *   (head projections, stacked pseudo-queries/keys/values, the attention output and each
  *   row's softmax normaliser) in `workspace`, which is required here:
  *   iha_backward_workspace_bytes(...) bytes, 256-byte aligned.

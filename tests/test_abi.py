@@ -92,7 +92,7 @@ def test_forward_rejects_bad_arguments(iha, kw, status):
 def test_projection_route(iha):
     assert iha.iha_projection_route(16, 128, 4, iha.IHA_DTYPE_BF16) == 1
     assert iha.iha_projection_route(16, 64, 2, iha.IHA_DTYPE_BF16) == 1
-    assert iha.iha_projection_route(16, 128, 1, iha.IHA_DTYPE_BF16) == 0
+    assert iha.iha_projection_route(16, 128, 1, iha.IHA_DTYPE_BF16) == 1
     assert iha.iha_projection_route(32, 64, 2, iha.IHA_DTYPE_BF16) == 0
     assert iha.iha_projection_route(4, 32, 2, iha.IHA_DTYPE_F32) == 0
     assert iha.iha_projection_route(4, 96, 2, iha.IHA_DTYPE_BF16) == -1

@@ -269,7 +269,7 @@ def test_step_entry_points_match_forward(iha, P):
     ref = run_gpu(iha, w, dinp=dinp)
     dt = iha.IHA_DTYPE_BF16
     route = iha.iha_projection_route(w.H, w.d, w.P, dt)
-    assert route == (1 if P >= 2 else 0)
+    assert route == 1
     s = torch.cuda.current_stream()
     ora = oracle_rows(w, inp)
     for r in (0, 1, 2):
@@ -689,8 +689,8 @@ def test_backward_matches_oracle(iha, B, N, H, d, P, mode, window):
     # the causal P = 4 workload at full size, as the training benchmark runs it
     (1, 8192, 16, 128, 4, C, 0)])
 def test_training_pair_matches_recompute(iha, B, N, H, d, P, mode, window):
-    """iha_forward_train + iha_backward_saved give iha_forward's output (P >= 2: the same
-    route) and iha_backward's gradients bit for bit."""
+    """iha_forward_train + iha_backward_saved give iha_forward's output (the same route at
+    every P) and iha_backward's gradients bit for bit."""
     from oracle import backward as bwd
     w = gi.Workload("train", B=B, N=N, H=H, d=d, P=P, mask_mode=mode, window=window, dtype="bf16", seed=31 + P)
     inp = gi.make_inputs(w)
@@ -720,8 +720,5 @@ def test_training_pair_matches_recompute(iha, B, N, H, d, P, mode, window):
     assert rc == iha.IHA_OK, f"device status {rc} word {code:#x}"
     for k in bwd.PARAMS:
         assert torch.equal(g_saved[k], g_full[k]), k
-    if P >= 2:
-        assert torch.equal(out, run_gpu(iha, w, inp))
-    else:   # the forward folds alpha into W for P = 1: same layer, other rounding
-        assert_parity(w, out.double().cpu().numpy(), oracle_rows(w, inp))
+    assert torch.equal(out, run_gpu(iha, w, inp))
 

@@ -1,6 +1,6 @@
 // iha_api.cu -- the C ABI declared in include/iha.h: argument validation, workspace
-// layout, the per-device status word, and the launch sequence fold -> project ->
-// attention -> contract of "Interleaved Head Attention" Algorithm 1.
+// layout, the per-device status word, and the launch sequence (slice -> project+mix, or
+// fold -> project) -> attention -> contract of "Interleaved Head Attention" Algorithm 1.
 #include <cuda_runtime.h>
 
 #include <climits>

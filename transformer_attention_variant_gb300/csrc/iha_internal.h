@@ -112,10 +112,11 @@ cudaError_t launch_mix(const void *Y, const float *aQ, const float *aK, const fl
                        cudaStream_t st, int *status);
 
 // Which way the library computes steps 1+2: true = the head projections with the mixing in
-// the GEMM epilogue (bf16, P >= 2, H <= 16, H*P <= 128: 1/P of the folded GEMM's work),
-// false = fold alpha into W, then one GEMM.
+// the GEMM epilogue (bf16, H <= 16, H*P <= 128: 1/P of the folded GEMM's work; at P = 1 the
+// same GEMM, without the fold's pass over the weights), false = fold alpha into W, then one
+// GEMM.
 inline bool unfolded_route(const Shape &sh, int dtype) {
-    return dtype == 1 && sh.P >= 2 && sh.H <= 16 && sh.H * sh.P <= 128;
+    return dtype == 1 && sh.H <= 16 && sh.H * sh.P <= 128;
 }
 
 // The mixing kernel for nsets projections: Y [t][y_sets][H][d] (the first nsets of each
