@@ -39,8 +39,8 @@
  *     per-device status word and reported by iha_check_device_status().
  *   - The library looks up the device addresses of its per-device state (the
  *     status word, the attention work-counter ring, the array behind
- *     iha_forward_noalloc) on first use on each device and keeps them for the
- *     life of the process.  cudaDeviceReset() invalidates them: no call may
+ *     iha_forward_noalloc) and creates the two copy streams of iha_forward_host on
+ *     first use on each device, and keeps them for the life of the process.  cudaDeviceReset() invalidates them: no call may
  *     follow a device reset in the same process.
  */
 #ifndef IHA_H
