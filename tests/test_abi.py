@@ -125,6 +125,25 @@ def test_step_entry_points_reject_bad_arguments(iha):
     assert iha.iha_selftest_wait_timeout(None, 20000) == 1
 
 
+def test_host_buffer_layout_and_checks(iha):
+    """iha_host_buffer_bytes is X, W_Q, W_K, W_V, alpha_Q/K/V, R and out (each from a
+    256-byte boundary) followed by iha_forward_ex's workspace; iha_forward_host refuses a
+    caller-given device buffer that is smaller or not 256-byte aligned before any copy."""
+    al = lambda x: (x + 255) // 256 * 256
+    bf16 = iha.IHA_DTYPE_BF16
+    for B, N, H, d, P in ((1, 64, 2, 64, 2), (2, 100, 16, 128, 4), (1, 33, 5, 64, 3), (3, 7, 16, 128, 1)):
+        D = H * d
+        x, w, a = B * N * D * 2, D * D * 2, H * H * P * 4
+        expect = al(x) + 3 * al(w) + 4 * al(a) + al(x) + iha.iha_workspace_bytes(B, N, H, d, P, bf16)
+        need = iha.iha_host_buffer_bytes(B, N, H, d, P, bf16)
+        assert need == expect, (B, N, H, d, P)
+        args = [FAKE] * 8 + [B, N, H, d, P, 1, 0, FAKE, bf16, None]
+        assert iha.iha_forward_host(*args, FAKE * 2, need - 1) == iha.IHA_ERR_WORKSPACE
+        assert iha.iha_forward_host(*args, FAKE * 2 + 128, need) == iha.IHA_ERR_WORKSPACE
+    assert iha.iha_host_buffer_bytes(1, 64, 2, 96, 2, bf16) == 0     # bf16 needs d in {64, 128}
+    assert iha.iha_host_buffer_bytes(0, 64, 2, 64, 2, bf16) == 0
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     """Importing the binding when libiha.so is absent raises, naming the fix;
     there is no fallback path."""
